@@ -1,0 +1,222 @@
+"""fp64 CPU oracle for the fused GEMM + epilogue path -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It wraps ``gbf_oracle.c`` (plain C,
+single-threaded, fp64, one bf16 rounding at the end) through ctypes and
+shares no code with the CUDA library in ``tcgen05_tmem_bf16_gb300``.
+
+bf16 tensors are passed as numpy ``uint16`` arrays holding the raw bits;
+packed int4 weights as ``uint8`` arrays (K x N/2, high nibble = even column).
+
+Every function here follows the passage cited in ``gbf_oracle.c``:
+  * gemm_epilogue  -- "Fusion and Epilogues", epilogue-fusion bullet;
+                      "Kernel fusion" guide, Concept.
+  * swiglu         -- "Fusion Thinking", Pattern 2 (Fused SwiGLU).
+  * w4a16 / dequant_int4 -- "Fusion Thinking", Pattern 3 (Dequant + GEMM).
+  * unfused modes  -- "kernel fusion" wiki, the activation-after-matmul case.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gbf_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libgbf_oracle.so")
+
+ACT = {"identity": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
+LAYOUT = {"kn": 0, "nk": 1}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile gbf_oracle.c with gcc (no fast-math, no FMA contraction so
+    x86 and Arm hosts give the same fp64 results)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        D = ctypes.c_double
+        I = ctypes.c_int
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = D
+        lib.oracle_bf16_from_f64.argtypes = [D]
+        lib.oracle_bf16_from_f64.restype = ctypes.c_uint16
+        lib.oracle_act.argtypes = [I, D]
+        lib.oracle_act.restype = D
+        lib.oracle_gemm_epilogue.argtypes = [P, P, I, P, P, P, I64, I64, I64, D, D, I, I,
+                                             P, P, I64, P, P]
+        lib.oracle_gemm_epilogue.restype = I
+        lib.oracle_swiglu.argtypes = [P, P, P, I, P, I64, I64, I64, D, D, I, I,
+                                      P, P, I64, P, P]
+        lib.oracle_swiglu.restype = I
+        lib.oracle_w4a16.argtypes = [P, P, P, I64, P, P, P, I64, I64, I64, D, D, I,
+                                     P, P, I64, P, P]
+        lib.oracle_w4a16.restype = I
+        lib.oracle_dequant_int4.argtypes = [P, P, I64, I64, I64, P]
+        lib.oracle_dequant_int4.restype = I
+        lib.oracle_pointwise_epilogue.argtypes = [P, P, P, P, I64, I64, D, D, I, P]
+        lib.oracle_pointwise_epilogue.restype = I
+        lib.oracle_swiglu_pointwise.argtypes = [P, P, P, I64, I64, D, D, I, P]
+        lib.oracle_swiglu_pointwise.restype = I
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, f"bf16 bits expected as uint16, got {a.dtype}"
+    return a
+
+
+def _idx(M, N, rows, cols):
+    if rows is None:
+        return None, None, M * N
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    assert rows.shape == cols.shape
+    return rows, cols, rows.size
+
+
+def _outputs(count, want_f64):
+    ob = np.empty(count, dtype=np.uint16)
+    of = np.empty(count, dtype=np.float64) if want_f64 else None
+    return ob, of
+
+
+def _finish(rc, ob, of, M, N, rows, want_f64):
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    if rows is None:
+        ob = ob.reshape(M, N)
+        of = of.reshape(M, N) if of is not None else None
+    return (ob, of) if want_f64 else ob
+
+
+# ---- scalar helpers ---------------------------------------------------------
+
+def bf16_from_f64(v: float) -> int:
+    return int(_load().oracle_bf16_from_f64(float(v)))
+
+
+def bf16_to_f64(h: int) -> float:
+    return float(_load().oracle_bf16_to_f64(int(h) & 0xFFFF))
+
+
+def act(name: str, v: float) -> float:
+    return float(_load().oracle_act(ACT[name], float(v)))
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bits (uint16) to float64 (no arithmetic)."""
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---- the path ---------------------------------------------------------------
+
+def gemm_epilogue(A, B, layout, C=None, bias=None, residual=None, *, M, N, K,
+                  alpha=1.0, beta=0.0, act="identity", unfused=False,
+                  rows=None, cols=None, want_f64=False):
+    """out = bf16(act(alpha*A*B~ + beta*C + bias) + residual); B~ = B (KxN
+    layout "kn") or W^T (W is NxK, layout "nk").  With rows/cols given, only
+    those (m, n) elements are computed (1-D results)."""
+    lib = _load()
+    A, B, C, bias, residual = map(_u16, (A, B, C, bias, residual))
+    r, c, count = _idx(M, N, rows, cols)
+    ob, of = _outputs(count, want_f64)
+    rc = lib.oracle_gemm_epilogue(_ptr(A), _ptr(B), LAYOUT[layout], _ptr(C), _ptr(bias),
+                                  _ptr(residual), M, N, K, float(alpha), float(beta),
+                                  ACT[act], int(bool(unfused)), _ptr(r), _ptr(c), count,
+                                  _ptr(ob), _ptr(of))
+    return _finish(rc, ob, of, M, N, rows, want_f64)
+
+
+def swiglu(x, w_gate, w_up, layout, C=None, *, M, N, K, alpha=1.0, beta=0.0,
+           act="silu", unfused=False, rows=None, cols=None, want_f64=False):
+    """h = bf16(act(alpha*g)*(alpha*u) + beta*C), g = x*Wg~, u = x*Wu~."""
+    lib = _load()
+    x, w_gate, w_up, C = map(_u16, (x, w_gate, w_up, C))
+    r, c, count = _idx(M, N, rows, cols)
+    ob, of = _outputs(count, want_f64)
+    rc = lib.oracle_swiglu(_ptr(x), _ptr(w_gate), _ptr(w_up), LAYOUT[layout], _ptr(C),
+                           M, N, K, float(alpha), float(beta), ACT[act],
+                           int(bool(unfused)), _ptr(r), _ptr(c), count, _ptr(ob), _ptr(of))
+    return _finish(rc, ob, of, M, N, rows, want_f64)
+
+
+def w4a16(A, Wq, scales, group_size, C=None, bias=None, residual=None, *, M, N, K,
+          alpha=1.0, beta=0.0, act="identity", rows=None, cols=None, want_f64=False):
+    """gemm_epilogue with B~[k][n] = bf16((q[k][n]-8)*s[k/G][n])."""
+    lib = _load()
+    A, scales, C, bias, residual = map(_u16, (A, scales, C, bias, residual))
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    r, c, count = _idx(M, N, rows, cols)
+    ob, of = _outputs(count, want_f64)
+    rc = lib.oracle_w4a16(_ptr(A), _ptr(Wq), _ptr(scales), int(group_size), _ptr(C),
+                          _ptr(bias), _ptr(residual), M, N, K, float(alpha), float(beta),
+                          ACT[act], _ptr(r), _ptr(c), count, _ptr(ob), _ptr(of))
+    return _finish(rc, ob, of, M, N, rows, want_f64)
+
+
+def dequant_int4(Wq, scales, group_size, *, K, N):
+    lib = _load()
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    scales = _u16(scales)
+    out = np.empty((K, N), dtype=np.uint16)
+    if lib.oracle_dequant_int4(_ptr(Wq), _ptr(scales), int(group_size), K, N, _ptr(out)) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
+
+
+def pointwise_epilogue(D, C=None, bias=None, residual=None, *, M, N, alpha=1.0,
+                       beta=0.0, act="identity"):
+    lib = _load()
+    D, C, bias, residual = map(_u16, (D, C, bias, residual))
+    out = np.empty((M, N), dtype=np.uint16)
+    if lib.oracle_pointwise_epilogue(_ptr(D), _ptr(C), _ptr(bias), _ptr(residual), M, N,
+                                     float(alpha), float(beta), ACT[act], _ptr(out)) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
+
+
+def swiglu_pointwise(g, u, C=None, *, M, N, alpha=1.0, beta=0.0, act="silu"):
+    lib = _load()
+    g, u, C = map(_u16, (g, u, C))
+    out = np.empty((M, N), dtype=np.uint16)
+    if lib.oracle_swiglu_pointwise(_ptr(g), _ptr(u), _ptr(C), M, N, float(alpha),
+                                   float(beta), ACT[act], _ptr(out)) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out

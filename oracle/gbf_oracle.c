@@ -1,0 +1,332 @@
+/*
+ * gbf_oracle.c -- plain, slow, single-threaded fp64 CPU oracle for the fused
+ * GEMM + epilogue path.  TEST INFRASTRUCTURE ONLY: it is used by tests/,
+ * by the smoke check and by the CPU-baseline leg of the benchmark.  No
+ * product code path links or calls it, and it shares no code, header or
+ * constant with the CUDA library.
+ *
+ * What it computes (each function cites the passage it follows):
+ *
+ *   gemm_epilogue   out = bf16( act(alpha*A*B + beta*C + bias) + residual )
+ *       "Fusion and Epilogues" (metalworking.vercel.app), bullet
+ *       "Epilogue fusion, the mechanical form": the GEMM ending alpha*AB +
+ *       beta*C, bias, activation, applied on the way to the one write.
+ *       "Kernel fusion" (guide.dupenodi.dev), section "Concept": bias,
+ *       activation, scaling, residual add.  Order: bias inside the
+ *       activation, residual outside it.
+ *   swiglu          h = bf16( act(alpha*g) * (alpha*u) + beta*C ),
+ *                   g = x*W_gate^T, u = x*W_up^T
+ *       "Fusion Thinking", Pattern 2 (Fused SwiGLU): gate and up products of
+ *       the same x, silu(gate)*up, level 2 = both products in one GEMM with
+ *       SwiGLU in its epilogue.
+ *   w4a16           w[k][n] = bf16((q[k][n] - 8) * s[k/G][n]), then the
+ *                   gemm_epilogue formula with B = w.
+ *       "Fusion Thinking", Pattern 3 (Dequant + GEMM): packed 2 x int4 per
+ *       byte along N, high nibble first (interleave(w_hi, w_lo)), zero point
+ *       8, per-group bf16 scales, result fed to the matrix product.
+ *   unfused modes   the same results with the intermediate written as bf16
+ *       between the product and the pointwise pass ("kernel fusion",
+ *       infraphysics.net: "the activation-after-matmul case"; "Fusion
+ *       Thinking", Pattern 2 un-fused and Pattern 3 un-fused).
+ *
+ * Arithmetic: every product and sum in fp64 (double), rounded once to bf16
+ * at the end with round-to-nearest-even; in the unfused modes the bf16
+ * intermediates are rounded the same way.  Activations use the host libm:
+ *   relu(v)      = max(v, 0)
+ *   silu(v)      = v * sigmoid(v) = v / (1 + exp(-v))
+ *   gelu_tanh(v) = 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))
+ * (the tanh form of GELU; the pages name SiLU but define no GELU).
+ *
+ * Parity pins live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
+
+enum { ACT_IDENTITY = 0, ACT_RELU = 1, ACT_SILU = 2, ACT_GELU_TANH = 3 };
+enum { LAYOUT_KN = 0, LAYOUT_NK = 1 };
+
+/* ---- bf16 <-> double ---------------------------------------------------- */
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+double oracle_bf16_to_f64(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16, ties to even, in one step (no detour
+ * through binary32, which would round twice).  bf16 keeps 8 significant bits
+ * for normal numbers (exponent >= -126); below that the spacing is fixed at
+ * 2^-133.  Values at or beyond 2^128 after rounding become infinity. */
+uint16_t oracle_bf16_from_f64(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isinf(a))
+        return sign | 0x7F80;
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);           /* a in [2^(e-1), 2^e) */
+    int top = e - 1;
+    int ulp_exp = (top < -126 ? -126 : top) - 7;
+    double q = ldexp(a, -ulp_exp); /* exact power-of-two scaling */
+    double r = nearbyint(q);       /* default rounding mode: ties to even */
+    double rounded = ldexp(r, ulp_exp);
+    if (rounded >= 0x1p128)
+        return sign | 0x7F80;
+    float f = (float)rounded;      /* exact: at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)((u >> 16) & 0x7FFF);
+}
+
+/* ---- activations -------------------------------------------------------- */
+
+double oracle_act(int act, double v)
+{
+    switch (act) {
+    case ACT_IDENTITY:
+        return v;
+    case ACT_RELU:
+        return v > 0.0 ? v : 0.0;
+    case ACT_SILU:
+        return v / (1.0 + exp(-v));
+    case ACT_GELU_TANH: {
+        const double c = sqrt(2.0 / M_PI);
+        return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));
+    }
+    default:
+        return NAN;
+    }
+}
+
+/* ---- element kernels ---------------------------------------------------- */
+
+/* B~[k][n]: B[k][n] for the K x N layout, W[n][k] for the N x K layout. */
+static double b_at(const uint16_t *B, int layout, int64_t N, int64_t K,
+                   int64_t k, int64_t n)
+{
+    if (layout == LAYOUT_KN)
+        return oracle_bf16_to_f64(B[k * N + n]);
+    return oracle_bf16_to_f64(B[n * K + k]);
+}
+
+/* sum_k A[m][k] * B~[k][n] in fp64, k ascending. */
+static double dot_ab(const uint16_t *A, const uint16_t *B, int layout,
+                     int64_t N, int64_t K, int64_t m, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+        acc += oracle_bf16_to_f64(A[m * K + k]) * b_at(B, layout, N, K, k, n);
+    return acc;
+}
+
+/* act(alpha*acc + beta*C + bias) + residual, fp64. Null operands are zero;
+ * C is ignored when null (so beta does not matter then). */
+static double epilogue(double acc, const uint16_t *C, const uint16_t *bias,
+                       const uint16_t *residual, int64_t N, int64_t m,
+                       int64_t n, double alpha, double beta, int act)
+{
+    double v = alpha * acc;
+    if (C)
+        v += beta * oracle_bf16_to_f64(C[m * N + n]);
+    if (bias)
+        v += oracle_bf16_to_f64(bias[n]);
+    v = oracle_act(act, v);
+    if (residual)
+        v += oracle_bf16_to_f64(residual[m * N + n]);
+    return v;
+}
+
+/* Dequantised weight w[k][n] = bf16((q - 8) * s[k/G][n]) as a double.
+ * Wq is K x N/2 bytes; byte j of row k holds column 2j in its high nibble
+ * and column 2j+1 in its low nibble. */
+static double w4_at(const uint8_t *Wq, const uint16_t *scales, int64_t G,
+                    int64_t N, int64_t k, int64_t n)
+{
+    uint8_t byte = Wq[k * (N / 2) + n / 2];
+    int q = (n % 2 == 0) ? (byte >> 4) & 0xF : byte & 0xF;
+    double s = oracle_bf16_to_f64(scales[(k / G) * N + n]);
+    return oracle_bf16_to_f64(oracle_bf16_from_f64(((double)q - 8.0) * s));
+}
+
+/* Element iteration helper: idx_m/idx_n == NULL means all M x N in row-major
+ * order (count must then be M*N); otherwise count explicit (m, n) pairs. */
+static void elem(const int64_t *idx_m, const int64_t *idx_n, int64_t N,
+                 int64_t i, int64_t *m, int64_t *n)
+{
+    if (idx_m) {
+        *m = idx_m[i];
+        *n = idx_n[i];
+    } else {
+        *m = i / N;
+        *n = i % N;
+    }
+}
+
+static void emit(int64_t i, double v, uint16_t *out_bf16, double *out_f64)
+{
+    if (out_bf16)
+        out_bf16[i] = oracle_bf16_from_f64(v);
+    if (out_f64)
+        out_f64[i] = v;
+}
+
+/* ---- public entry points ------------------------------------------------
+ * Every function writes `count` results: out_bf16[i] (rounded once) and/or
+ * out_f64[i] (the fp64 value before that rounding).  Returns 0, or -1 on a
+ * bad argument. */
+
+/* Fused GEMM + epilogue ("Fusion and Epilogues", epilogue fusion bullet;
+ * "Kernel fusion" guide, Concept).  unfused != 0 rounds the plain product
+ * D = A*B to bf16 before the pointwise pass, as a separate GEMM kernel that
+ * writes D to memory would ("kernel fusion" wiki, activation after a matrix
+ * product). */
+int oracle_gemm_epilogue(const uint16_t *A, const uint16_t *B, int layout,
+                         const uint16_t *C, const uint16_t *bias,
+                         const uint16_t *residual, int64_t M, int64_t N,
+                         int64_t K, double alpha, double beta, int act,
+                         int unfused, const int64_t *idx_m,
+                         const int64_t *idx_n, int64_t count,
+                         uint16_t *out_bf16, double *out_f64)
+{
+    if (M < 0 || N < 0 || K < 0 || (layout != LAYOUT_KN && layout != LAYOUT_NK))
+        return -1;
+    if (!idx_m && count != M * N)
+        return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m, n;
+        elem(idx_m, idx_n, N, i, &m, &n);
+        if (m < 0 || m >= M || n < 0 || n >= N)
+            return -1;
+        double acc = dot_ab(A, B, layout, N, K, m, n);
+        if (unfused)
+            acc = oracle_bf16_to_f64(oracle_bf16_from_f64(acc));
+        emit(i, epilogue(acc, C, bias, residual, N, m, n, alpha, beta, act),
+             out_bf16, out_f64);
+    }
+    return 0;
+}
+
+/* Gate/up dual GEMM with the GLU ending ("Fusion Thinking", Pattern 2):
+ * g = x*W_gate~, u = x*W_up~ (same layout rule as gemm_epilogue),
+ * h = act(alpha*g) * (alpha*u) + beta*C.  unfused != 0 rounds g and u to
+ * bf16 first, as two separate GEMMs writing them to memory would. */
+int oracle_swiglu(const uint16_t *x, const uint16_t *w_gate,
+                  const uint16_t *w_up, int layout, const uint16_t *C,
+                  int64_t M, int64_t N, int64_t K, double alpha, double beta,
+                  int act, int unfused, const int64_t *idx_m,
+                  const int64_t *idx_n, int64_t count, uint16_t *out_bf16,
+                  double *out_f64)
+{
+    if (M < 0 || N < 0 || K < 0 || (layout != LAYOUT_KN && layout != LAYOUT_NK))
+        return -1;
+    if (!idx_m && count != M * N)
+        return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m, n;
+        elem(idx_m, idx_n, N, i, &m, &n);
+        if (m < 0 || m >= M || n < 0 || n >= N)
+            return -1;
+        double g = dot_ab(x, w_gate, layout, N, K, m, n);
+        double u = dot_ab(x, w_up, layout, N, K, m, n);
+        if (unfused) {
+            g = oracle_bf16_to_f64(oracle_bf16_from_f64(g));
+            u = oracle_bf16_to_f64(oracle_bf16_from_f64(u));
+        }
+        double h = oracle_act(act, alpha * g) * (alpha * u);
+        if (C)
+            h += beta * oracle_bf16_to_f64(C[m * N + n]);
+        emit(i, h, out_bf16, out_f64);
+    }
+    return 0;
+}
+
+/* Weight-only int4 GEMM ("Fusion Thinking", Pattern 3): the gemm_epilogue
+ * formula with B~[k][n] = bf16((q[k][n] - 8) * s[k/G][n]).  The unfused
+ * composition materialises the same bf16 weight, so it has the same
+ * result; there is no separate unfused mode. */
+int oracle_w4a16(const uint16_t *A, const uint8_t *Wq, const uint16_t *scales,
+                 int64_t G, const uint16_t *C, const uint16_t *bias,
+                 const uint16_t *residual, int64_t M, int64_t N, int64_t K,
+                 double alpha, double beta, int act, const int64_t *idx_m,
+                 const int64_t *idx_n, int64_t count, uint16_t *out_bf16,
+                 double *out_f64)
+{
+    if (M < 0 || N < 0 || K < 0 || G <= 0 || N % 2 != 0 || K % G != 0)
+        return -1;
+    if (!idx_m && count != M * N)
+        return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m, n;
+        elem(idx_m, idx_n, N, i, &m, &n);
+        if (m < 0 || m >= M || n < 0 || n >= N)
+            return -1;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += oracle_bf16_to_f64(A[m * K + k]) * w4_at(Wq, scales, G, N, k, n);
+        emit(i, epilogue(acc, C, bias, residual, N, m, n, alpha, beta, act),
+             out_bf16, out_f64);
+    }
+    return 0;
+}
+
+/* The dequantised weight on its own, K x N bf16 ("Fusion Thinking",
+ * Pattern 3 un-fused: w_bf16 = dequantize(w_quant, scales)). */
+int oracle_dequant_int4(const uint8_t *Wq, const uint16_t *scales, int64_t G,
+                        int64_t K, int64_t N, uint16_t *w_out)
+{
+    if (K < 0 || N < 0 || G <= 0 || N % 2 != 0 || K % G != 0)
+        return -1;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n)
+            w_out[k * N + n] = oracle_bf16_from_f64(w4_at(Wq, scales, G, N, k, n));
+    return 0;
+}
+
+/* The pointwise pass alone, given an already-rounded bf16 product D
+ * (used to check the unfused composition stage by stage). */
+int oracle_pointwise_epilogue(const uint16_t *D, const uint16_t *C,
+                              const uint16_t *bias, const uint16_t *residual,
+                              int64_t M, int64_t N, double alpha, double beta,
+                              int act, uint16_t *out_bf16)
+{
+    if (M < 0 || N < 0)
+        return -1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            out_bf16[m * N + n] = oracle_bf16_from_f64(
+                epilogue(oracle_bf16_to_f64(D[m * N + n]), C, bias, residual,
+                         N, m, n, alpha, beta, act));
+    return 0;
+}
+
+/* The GLU pointwise pass alone, given bf16 g and u. */
+int oracle_swiglu_pointwise(const uint16_t *g, const uint16_t *u,
+                            const uint16_t *C, int64_t M, int64_t N,
+                            double alpha, double beta, int act,
+                            uint16_t *out_bf16)
+{
+    if (M < 0 || N < 0)
+        return -1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double h = oracle_act(act, alpha * oracle_bf16_to_f64(g[m * N + n])) *
+                       (alpha * oracle_bf16_to_f64(u[m * N + n]));
+            if (C)
+                h += beta * oracle_bf16_to_f64(C[m * N + n]);
+            out_bf16[m * N + n] = oracle_bf16_from_f64(h);
+        }
+    return 0;
+}

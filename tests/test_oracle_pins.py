@@ -1,0 +1,365 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each test ties one part of the oracle to something independent of it: a
+hand-worked example under tests/golden/, a library routine (numpy matmul,
+torch's bf16 cast and activations) in a special case, exact integer
+arithmetic, or an invariant.  A plausible mistake in the oracle (a dropped
+term, a wrong sign, a transposed operand, the other nibble order, a wrong
+group index, a wrong GELU constant, round-half-up) fails at least one of
+them.  CPU only.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def bits(x):
+    """Exact bf16 bit patterns of values that are already bf16-exact."""
+    arr = np.asarray(x, dtype=np.float32)
+    b = to_bf16_bits(arr)
+    assert np.array_equal(oracle.bf16_bits_to_f64(b), arr.astype(np.float64)), "value not bf16-exact"
+    return b
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+@pytest.mark.parametrize("value,expected", [
+    (1.0, 0x3F80),
+    (-2.0, 0xC000),
+    (1.0 + 2.0 ** -8, 0x3F80),                 # tie -> even (down)
+    (1.0 + 3 * 2.0 ** -8, 0x3F82),             # tie -> even (up)
+    (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),    # just above the tie
+    (1.0 + 2.0 ** -8 - 2.0 ** -40, 0x3F80),    # just below the tie
+    (2.0 ** -126, 0x0080),                     # smallest normal
+    (2.0 ** -133, 0x0001),                     # smallest subnormal
+    (2.0 ** -134, 0x0000),                     # tie between 0 and 2^-133 -> even
+    (3 * 2.0 ** -134, 0x0002),                 # tie between 1 and 2 ulps -> even
+    ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),    # largest finite
+    ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),    # tie at the top rounds to even = inf
+    (float("inf"), 0x7F80),
+    (-float("inf"), 0xFF80),
+    (-0.0, 0x8000),
+    (0.0, 0x0000),
+])
+def test_bf16_round_nearest_even_hand_values(value, expected):
+    assert oracle.bf16_from_f64(value) == expected
+
+
+def test_bf16_nan():
+    h = oracle.bf16_from_f64(float("nan"))
+    assert (h & 0x7F80) == 0x7F80 and (h & 0x007F) != 0
+
+
+def test_bf16_round_matches_torch_cast_on_float32_values():
+    # For values that are exact float32, one RNE step to bf16 is what torch's
+    # float32 -> bf16 cast does; compare 20k random values spanning the range.
+    rng = np.random.Generator(np.random.PCG64(1234))
+    mant = rng.standard_normal(20000).astype(np.float32)
+    expo = rng.integers(-140, 120, size=20000)
+    vals = (mant * np.float32(2.0) ** expo.astype(np.float32)).astype(np.float32)
+    vals = vals[np.isfinite(vals)]
+    want = to_bf16_bits(vals)
+    got = np.array([oracle.bf16_from_f64(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_widening_round_trip_all_patterns():
+    lib = oracle._load()
+    for h in range(0, 1 << 16, 7):
+        if (h & 0x7F80) == 0x7F80 and (h & 0x7F):
+            continue  # NaN payloads
+        assert lib.oracle_bf16_from_f64(lib.oracle_bf16_to_f64(h)) == h
+
+
+# ---------------------------------------------------------------- activations
+
+def test_activation_special_values():
+    assert oracle.act("silu", 0.0) == 0.0
+    assert oracle.act("gelu_tanh", 0.0) == 0.0
+    assert oracle.act("relu", -3.5) == 0.0
+    assert oracle.act("relu", 2.25) == 2.25
+    assert oracle.act("identity", -1.5) == -1.5
+    assert oracle.act("silu", -800.0) == 0.0        # v * sigmoid(v) -> 0
+    assert oracle.act("silu", 800.0) == 800.0
+
+
+def test_silu_and_gelu_tanh_match_torch_float64():
+    xs = torch.linspace(-12, 12, 4801, dtype=torch.float64)
+    silu = torch.nn.functional.silu(xs)
+    gelu = torch.nn.functional.gelu(xs, approximate="tanh")
+    for x, s, g in zip(xs.tolist(), silu.tolist(), gelu.tolist()):
+        assert oracle.act("silu", x) == pytest.approx(s, rel=1e-13, abs=1e-300)
+        assert oracle.act("gelu_tanh", x) == pytest.approx(g, rel=1e-12, abs=1e-15)
+
+
+def test_gelu_tanh_is_an_approximation_of_erf_gelu():
+    # The tanh form stays within ~5e-4 of x*Phi(x) (textbook bound) and is
+    # not the erf form itself.
+    worst = 0.0
+    for x in np.linspace(-6, 6, 1201):
+        exact = 0.5 * x * (1 + math.erf(x / math.sqrt(2)))
+        worst = max(worst, abs(oracle.act("gelu_tanh", float(x)) - exact))
+    assert 1e-5 < worst < 5e-4
+
+
+# ---------------------------------------------------------------- GEMM + epilogue
+
+def test_epilogue_hand_worked_example():
+    g = _golden("epilogue_hand.json")
+    A, B, C = bits(g["A"]), bits(g["B_kn"]), bits(g["C"])
+    bias, res = bits(g["bias"]), bits(g["residual"])
+    W = np.ascontiguousarray(B.T)
+    for act in ("relu", "identity"):
+        want = np.array([int(h, 16) for h in g[act]["out_bits"]], dtype=np.uint16).reshape(2, 2)
+        for layout, Bm in (("kn", B), ("nk", W)):
+            got = oracle.gemm_epilogue(A, Bm, layout, C, bias, res, M=2, N=2, K=3,
+                                       alpha=g["alpha"], beta=g["beta"], act=act)
+            assert np.array_equal(got, want), (act, layout, got, want)
+    plain = oracle.gemm_epilogue(A, B, "kn", M=2, N=2, K=3, want_f64=True)[1]
+    assert np.array_equal(plain, np.array(g["AB"], dtype=np.float64))
+
+
+def test_plain_product_matches_numpy_matmul():
+    # alpha=1, beta=0, no bias/residual, identity: the plain product.
+    rng = np.random.Generator(np.random.PCG64(7))
+    M, N, K = 5, 7, 33
+    A = to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    B = to_bf16_bits(rng.standard_normal((K, N)).astype(np.float32))
+    Af, Bf = oracle.bf16_bits_to_f64(A), oracle.bf16_bits_to_f64(B)
+    _, got = oracle.gemm_epilogue(A, B, "kn", M=M, N=N, K=K, want_f64=True)
+    np.testing.assert_allclose(got, Af @ Bf, rtol=1e-12, atol=1e-12)
+    _, got_nk = oracle.gemm_epilogue(A, np.ascontiguousarray(B.T), "nk", M=M, N=N, K=K,
+                                     want_f64=True)
+    np.testing.assert_allclose(got_nk, Af @ Bf, rtol=1e-12, atol=1e-12)
+
+
+def test_integer_inputs_are_exact_and_rounded_once():
+    rng = np.random.Generator(np.random.PCG64(8))
+    M, N, K = 9, 12, 200
+    A = rng.integers(-16, 17, size=(M, K)).astype(np.float32)
+    B = rng.integers(-16, 17, size=(K, N)).astype(np.float32)
+    exact = A.astype(np.int64) @ B.astype(np.int64)
+    _, f64 = oracle.gemm_epilogue(bits(A), bits(B), "kn", M=M, N=N, K=K, want_f64=True)
+    assert np.array_equal(f64, exact.astype(np.float64))
+    out = oracle.gemm_epilogue(bits(A), bits(B), "kn", M=M, N=N, K=K)
+    assert np.array_equal(out, to_bf16_bits(exact.astype(np.float32)))
+
+
+def test_identity_b_reduces_to_pointwise_of_a():
+    # B = I: out = act(alpha*A + beta*C + bias) + residual, with torch's
+    # float64 activation as the independent reference.
+    rng = np.random.Generator(np.random.PCG64(9))
+    n = 16
+    A = to_bf16_bits(rng.standard_normal((n, n)).astype(np.float32))
+    C = to_bf16_bits(rng.standard_normal((n, n)).astype(np.float32))
+    bias = to_bf16_bits(rng.standard_normal(n).astype(np.float32))
+    res = to_bf16_bits(rng.standard_normal((n, n)).astype(np.float32))
+    eye = bits(np.eye(n))
+    f = oracle.bf16_bits_to_f64
+    for act, fn in (("silu", torch.nn.functional.silu),
+                    ("gelu_tanh", lambda t: torch.nn.functional.gelu(t, approximate="tanh")),
+                    ("relu", torch.relu), ("identity", lambda t: t)):
+        pre = torch.from_numpy(0.75 * f(A) + 0.25 * f(C) + f(bias)[None, :])
+        want = fn(pre).numpy() + f(res)
+        _, got = oracle.gemm_epilogue(A, eye, "kn", C, bias, res, M=n, N=n, K=n,
+                                      alpha=0.75, beta=0.25, act=act, want_f64=True)
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
+
+
+def test_zero_a_gives_closed_form_and_null_operands_are_zero():
+    n = 8
+    A = np.zeros((n, 5), dtype=np.uint16)
+    B = bits(np.arange(40, dtype=np.float32).reshape(5, n))
+    C = bits(np.full((n, n), 2.0))
+    bias_v = np.arange(n) * 0.5 - 2.0
+    bias = bits(bias_v)
+    res = bits(np.full((n, n), -1.0))
+    out = oracle.gemm_epilogue(A, B, "kn", C, bias, res, M=n, N=n, K=5, alpha=3.0,
+                               beta=0.5, act="relu")
+    want = np.maximum(1.0 + bias_v, 0)[None, :] - 1.0
+    assert np.array_equal(out, to_bf16_bits(np.broadcast_to(want, (n, n)).astype(np.float32)))
+    # Null C ignores beta entirely; K = 0 is an empty sum.
+    out0 = oracle.gemm_epilogue(A[:, :0].copy(), B[:0].copy(), "kn", None, bias, None,
+                                M=n, N=n, K=0, beta=123.0, act="identity")
+    assert np.array_equal(out0, np.broadcast_to(bias, (n, n)))
+
+
+def test_sampled_elements_equal_full_output():
+    rng = np.random.Generator(np.random.PCG64(10))
+    M, N, K = 6, 10, 17
+    A = to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    B = to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32))
+    C = to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    full = oracle.gemm_epilogue(A, B, "nk", C, M=M, N=N, K=K, alpha=0.5, beta=2.0, act="silu")
+    r = np.array([0, 5, 3, 2]); c = np.array([9, 0, 4, 4])
+    part = oracle.gemm_epilogue(A, B, "nk", C, M=M, N=N, K=K, alpha=0.5, beta=2.0,
+                                act="silu", rows=r, cols=c)
+    assert np.array_equal(part, full[r, c])
+
+
+def test_unfused_mode_rounds_the_product_first():
+    # unfused = bf16(D) then the pointwise pass; with torch's bf16 cast of the
+    # numpy product as D the two stages agree with the one-call unfused mode.
+    rng = np.random.Generator(np.random.PCG64(11))
+    M, N, K = 8, 16, 64
+    A = to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    B = to_bf16_bits(rng.standard_normal((K, N)).astype(np.float32))
+    C = to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    f = oracle.bf16_bits_to_f64
+    D = torch.from_numpy(f(A) @ f(B)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    two_stage = oracle.pointwise_epilogue(D, C, M=M, N=N, alpha=0.5, beta=2.0, act="gelu_tanh")
+    one_call = oracle.gemm_epilogue(A, B, "kn", C, M=M, N=N, K=K, alpha=0.5, beta=2.0,
+                                    act="gelu_tanh", unfused=True)
+    assert np.array_equal(two_stage, one_call)
+
+
+# ---------------------------------------------------------------- SwiGLU
+
+def test_swiglu_hand_worked_example():
+    g = _golden("swiglu_hand.json")
+    x, wg, wu, C = bits(g["x"]), bits(g["wg_kn"]), bits(g["wu_kn"]), bits(g["C"])
+    for case in g["cases"]:
+        for layout, a, b in (("kn", wg, wu), ("nk", np.ascontiguousarray(wg.T),
+                                               np.ascontiguousarray(wu.T))):
+            _, h = oracle.swiglu(x, a, b, layout, C if case["use_c"] else None, M=2, N=2, K=3,
+                                 alpha=case["alpha"], beta=case["beta"], act="relu",
+                                 want_f64=True)
+            assert np.array_equal(h, np.array(case["h"], dtype=np.float64)), (case, layout)
+
+
+def test_swiglu_silu_matches_library_composition():
+    # alpha=1, beta=0: h = silu(g) * u with g, u from numpy matmul and torch's
+    # float64 SiLU.
+    rng = np.random.Generator(np.random.PCG64(12))
+    M, N, K = 6, 9, 40
+    x = to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    wg = to_bf16_bits((rng.standard_normal((N, K)) / 4).astype(np.float32))
+    wu = to_bf16_bits((rng.standard_normal((N, K)) / 4).astype(np.float32))
+    f = oracle.bf16_bits_to_f64
+    gm, um = f(x) @ f(wg).T, f(x) @ f(wu).T
+    want = torch.nn.functional.silu(torch.from_numpy(gm)).numpy() * um
+    _, h = oracle.swiglu(x, wg, wu, "nk", M=M, N=N, K=K, act="silu", want_f64=True)
+    np.testing.assert_allclose(h, want, rtol=1e-12, atol=1e-14)
+    # Same weights for gate and up: h = silu(g) * g.
+    _, hh = oracle.swiglu(x, wg, wg, "nk", M=M, N=N, K=K, act="silu", want_f64=True)
+    np.testing.assert_allclose(hh, torch.nn.functional.silu(torch.from_numpy(gm)).numpy() * gm,
+                               rtol=1e-12, atol=1e-14)
+    # Unfused mode: g and u rounded to bf16 first.
+    gb = torch.from_numpy(gm).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ub = torch.from_numpy(um).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.swiglu_pointwise(gb, ub, M=M, N=N),
+                          oracle.swiglu(x, wg, wu, "nk", M=M, N=N, K=K, unfused=True))
+
+
+# ---------------------------------------------------------------- W4A16
+
+def test_w4a16_hand_worked_example():
+    g = _golden("w4a16_hand.json")
+    A, s, bias = bits(g["A"]), bits(g["scales"]), bits(g["bias"])
+    Wq = np.array(g["Wq"], dtype=np.uint8)
+    w = oracle.dequant_int4(Wq, s, g["group_size"], K=2, N=2)
+    assert np.array_equal(oracle.bf16_bits_to_f64(w), np.array(g["w"]))
+    _, out = oracle.w4a16(A, Wq, s, 2, M=1, N=2, K=2, want_f64=True)
+    assert np.array_equal(out, np.array(g["out_no_bias"]))
+    _, out = oracle.w4a16(A, Wq, s, 2, None, bias, M=1, N=2, K=2, want_f64=True)
+    assert np.array_equal(out, np.array(g["out_bias"]))
+
+
+def test_w4a16_code_eight_is_zero_weight():
+    rng = np.random.Generator(np.random.PCG64(13))
+    M, N, K, G = 3, 8, 256, 128
+    A = to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    Wq = np.full((K, N // 2), 0x88, dtype=np.uint8)
+    s = to_bf16_bits(rng.uniform(0.005, 0.02, (K // G, N)).astype(np.float32))
+    C = to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    bias = to_bf16_bits(rng.standard_normal(N).astype(np.float32))
+    res = to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    assert not np.any(oracle.bf16_bits_to_f64(oracle.dequant_int4(Wq, s, G, K=K, N=N)))
+    got = oracle.w4a16(A, Wq, s, G, C, bias, res, M=M, N=N, K=K, alpha=2.0, beta=0.5,
+                       act="relu")
+    zero_a = np.zeros_like(A)
+    want = oracle.gemm_epilogue(zero_a, np.zeros((K, N), np.uint16), "kn", C, bias, res,
+                                M=M, N=N, K=K, alpha=2.0, beta=0.5, act="relu")
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("which", ["hi", "lo"])
+def test_w4a16_single_nibble_probe_fixes_nibble_order(which):
+    # Only one code differs from 8: byte j of row k0.  The high nibble feeds
+    # column 2j, the low nibble column 2j+1 (interleave(w_hi, w_lo)).
+    M, N, K, G = 2, 16, 256, 128
+    k0, j, q = 130, 5, 13
+    Wq = np.full((K, N // 2), 0x88, dtype=np.uint8)
+    Wq[k0, j] = (q << 4) | 8 if which == "hi" else (8 << 4) | q
+    col = 2 * j if which == "hi" else 2 * j + 1
+    A = bits(np.arange(M * K, dtype=np.float32).reshape(M, K) % 7 - 3)
+    s = bits(np.full((K // G, N), 0.25))
+    _, out = oracle.w4a16(A, Wq, s, G, M=M, N=N, K=K, want_f64=True)
+    want = np.zeros((M, N))
+    want[:, col] = oracle.bf16_bits_to_f64(A[:, k0]) * (q - 8) * 0.25
+    assert np.array_equal(out, want)
+
+
+def test_w4a16_group_scales_index_k_over_group_size():
+    # Power-of-two scales, different per group and column, integer
+    # activations: every product is exact, so the fp64 result is exact and
+    # equals an independent numpy evaluation with the scales repeated G times
+    # along K.
+    rng = np.random.Generator(np.random.PCG64(14))
+    M, N, K, G = 4, 32, 512, 128
+    A = bits(rng.integers(-4, 5, size=(M, K)).astype(np.float32))
+    Wq = rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+    expo = rng.integers(-8, -2, size=(K // G, N))
+    s = bits((2.0 ** expo).astype(np.float32))
+    codes = np.empty((K, N), dtype=np.int64)
+    codes[:, 0::2] = Wq >> 4
+    codes[:, 1::2] = Wq & 0xF
+    w = (codes - 8) * np.repeat(2.0 ** expo, G, axis=0)
+    want = oracle.bf16_bits_to_f64(A) @ w
+    _, got = oracle.w4a16(A, Wq, s, G, M=M, N=N, K=K, want_f64=True)
+    assert np.array_equal(got, want)
+
+
+def test_w4a16_equals_dequantise_then_gemm():
+    rng = np.random.Generator(np.random.PCG64(15))
+    M, N, K, G = 5, 24, 384, 128
+    A = to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    Wq = rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+    s = to_bf16_bits(rng.uniform(0.005, 0.02, (K // G, N)).astype(np.float32))
+    C = to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    w = oracle.dequant_int4(Wq, s, G, K=K, N=N)
+    a = oracle.w4a16(A, Wq, s, G, C, M=M, N=N, K=K, alpha=0.5, beta=1.5, act="gelu_tanh")
+    b = oracle.gemm_epilogue(A, w, "kn", C, M=M, N=N, K=K, alpha=0.5, beta=1.5,
+                             act="gelu_tanh")
+    assert np.array_equal(a, b)
+    # Each dequantised weight is one RNE rounding of the exact (q-8)*s.
+    f = oracle.bf16_bits_to_f64
+    codes = np.empty((K, N), dtype=np.int64)
+    codes[:, 0::2] = Wq >> 4
+    codes[:, 1::2] = Wq & 0xF
+    exact = (codes - 8) * np.repeat(f(s), G, axis=0)
+    assert np.array_equal(w, to_bf16_bits(exact.astype(np.float32)))
+
+
+def test_oracle_rejects_bad_arguments():
+    A = np.zeros((2, 4), np.uint16)
+    with pytest.raises(ValueError):
+        oracle.w4a16(A, np.zeros((4, 1), np.uint8), np.zeros((1, 2), np.uint16), 3,
+                     M=2, N=2, K=4)
+    with pytest.raises(ValueError):
+        oracle.gemm_epilogue(A, np.zeros((4, 2), np.uint16), "kn", M=2, N=2, K=4,
+                             rows=np.array([2]), cols=np.array([0]))

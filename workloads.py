@@ -1,0 +1,148 @@
+"""Seeded synthetic inputs for the fused GEMM + epilogue path.
+
+This module is the one piece shared by the CUDA side (tests, bench) and the
+oracle side: it draws random inputs and holds none of the method's
+arithmetic.  bf16 values are produced by drawing float32 samples with numpy's
+PCG64 generator and converting them with torch's bf16 cast; they are returned
+as numpy ``uint16`` bit patterns.  Packed int4 weights are uniform random
+bytes (so both nibbles are uniform codes 0..15).
+
+Workloads are the five configurations of the fused-GEMM study:
+  tiny       M=64  K=256  N=128   A,B,C,bias ~N(0,1), out=silu(0.5AB+C+bias)
+  prefill    M=N=K=4096           A~N(0,1), W (NxK)~N(0,1/64), bias~N(0,0.1),
+                                  residual~N(0,1), out=AW^T+bias+residual
+  swiglu     M=2048 N=14336 K=4096  x~N(0,1), Wg,Wu (NxK)~N(0,1/64)
+  w4a16      M=16 K=8192 N=28672  A~N(0,1), codes uniform 0..15,
+                                  scales uniform [0.005,0.02], group 128
+  sweep      N=K=8192, M in {1,16,128,1024,8192}, A,B~N(0,1/sqrt(K)),
+             C~N(0,1), bias~N(0,0.1), out=gelu_tanh(0.75AB+0.25C+bias)
+
+N(0, x) is read as mean 0 and VARIANCE x (std = sqrt(x)); ``sigma_is_std``
+switches to reading x as the standard deviation.
+Seeds: 0x5EED0000 + 16*config_id + tensor_index.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+SEED_BASE = 0x5EED0000
+
+SWEEP_M = (1, 16, 128, 1024, 8192)
+
+CONFIGS = {
+    "tiny": dict(id=1, op="gemm", M=64, N=128, K=256, layout="kn", alpha=0.5, beta=1.0,
+                 act="silu", has_c=True, has_bias=True, has_res=False),
+    "prefill": dict(id=2, op="gemm", M=4096, N=4096, K=4096, layout="nk", alpha=1.0,
+                    beta=0.0, act="identity", has_c=False, has_bias=True, has_res=True),
+    "swiglu": dict(id=3, op="swiglu", M=2048, N=14336, K=4096, layout="nk", alpha=1.0,
+                   beta=0.0, act="silu", has_c=False),
+    "w4a16": dict(id=4, op="w4a16", M=16, N=28672, K=8192, group=128, alpha=1.0,
+                  beta=0.0, act="identity", has_c=False, has_bias=False, has_res=False),
+    "sweep": dict(id=5, op="gemm", M=None, N=8192, K=8192, layout="kn", alpha=0.75,
+                  beta=0.25, act="gelu_tanh", has_c=True, has_bias=True, has_res=False),
+}
+
+
+def rng_for(config_id: int, tensor_index: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(SEED_BASE + 16 * config_id + tensor_index))
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 array -> bf16 bit patterns (uint16) via torch's bf16 cast."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bf16_normal(rng: np.random.Generator, shape, spread: float,
+                sigma_is_std: bool = False) -> np.ndarray:
+    std = spread if sigma_is_std else math.sqrt(spread)
+    return to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(std))
+
+
+def bf16_uniform(rng: np.random.Generator, shape, lo: float, hi: float) -> np.ndarray:
+    return to_bf16_bits(rng.uniform(lo, hi, size=shape).astype(np.float32))
+
+
+def int4_packed(rng: np.random.Generator, K: int, N: int) -> np.ndarray:
+    """K x N/2 bytes, every nibble a uniform code in 0..15."""
+    return rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+
+
+def make(name: str, M: int | None = None, sigma_is_std: bool = False,
+         shape: dict | None = None) -> dict:
+    """Inputs of one workload as numpy arrays plus its scalar parameters.
+
+    ``shape`` overrides M/N/K (and group) to draw a smaller case with the same
+    distributions; ``M`` picks the row count of the sweep."""
+    cfg = dict(CONFIGS[name])
+    if M is not None:
+        cfg["M"] = M
+    if shape:
+        cfg.update(shape)
+    if cfg["M"] is None:
+        raise ValueError("the sweep workload needs M")
+    cid, Mv, Nv, Kv = cfg["id"], cfg["M"], cfg["N"], cfg["K"]
+    s = sigma_is_std
+    out = dict(cfg)
+    if name == "tiny":
+        out["A"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), 1.0, s)
+        out["B"] = bf16_normal(rng_for(cid, 1), (Kv, Nv), 1.0, s)
+        out["C"] = bf16_normal(rng_for(cid, 2), (Mv, Nv), 1.0, s)
+        out["bias"] = bf16_normal(rng_for(cid, 3), (Nv,), 1.0, s)
+        out["residual"] = None
+    elif name == "prefill":
+        out["A"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), 1.0, s)
+        out["B"] = bf16_normal(rng_for(cid, 1), (Nv, Kv), 1.0 / 64.0, s)
+        out["C"] = None
+        out["bias"] = bf16_normal(rng_for(cid, 3), (Nv,), 0.1, s)
+        out["residual"] = bf16_normal(rng_for(cid, 4), (Mv, Nv), 1.0, s)
+    elif name == "swiglu":
+        out["x"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), 1.0, s)
+        out["w_gate"] = bf16_normal(rng_for(cid, 1), (Nv, Kv), 1.0 / 64.0, s)
+        out["w_up"] = bf16_normal(rng_for(cid, 2), (Nv, Kv), 1.0 / 64.0, s)
+        out["C"] = None
+    elif name == "w4a16":
+        out["A"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), 1.0, s)
+        out["Wq"] = int4_packed(rng_for(cid, 1), Kv, Nv)
+        out["scales"] = bf16_uniform(rng_for(cid, 2), (Kv // cfg["group"], Nv), 0.005, 0.02)
+        out["C"] = out["bias"] = out["residual"] = None
+    elif name == "sweep":
+        var = 1.0 / math.sqrt(Kv)
+        out["A"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), var, s)
+        out["B"] = bf16_normal(rng_for(cid, 1), (Kv, Nv), var, s)
+        out["C"] = bf16_normal(rng_for(cid, 2), (Mv, Nv), 1.0, s)
+        out["bias"] = bf16_normal(rng_for(cid, 3), (Nv,), 0.1, s)
+        out["residual"] = None
+    else:
+        raise KeyError(name)
+    return out
+
+
+def sample_indices(M: int, N: int, count: int = 4096, seed: int = 0xC0FFEE,
+                   edge: int = 128):
+    """A seeded sample of (row, col) output positions for large outputs: the
+    four corners, the rows and columns on both sides of every `edge`
+    boundary (sampled along the other axis), the ragged last row/column,
+    and uniform positions for the rest."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rows, cols = [], []
+    for r in (0, M - 1):
+        for c in (0, N - 1):
+            rows.append(r)
+            cols.append(c)
+    b_rows = sorted({x for b in range(0, M, edge) for x in (b - 1, b) if 0 <= x < M} | {M - 1})
+    b_cols = sorted({x for b in range(0, N, edge) for x in (b - 1, b) if 0 <= x < N} | {N - 1})
+    budget = max(0, count // 4)
+    for r in b_rows[:budget // 2 or 1]:
+        rows.append(r)
+        cols.append(int(rng.integers(0, N)))
+    for c in b_cols[:budget // 2 or 1]:
+        rows.append(int(rng.integers(0, M)))
+        cols.append(c)
+    while len(rows) < count:
+        rows.append(int(rng.integers(0, M)))
+        cols.append(int(rng.integers(0, N)))
+    return np.asarray(rows[:count], dtype=np.int64), np.asarray(cols[:count], dtype=np.int64)
