@@ -1,0 +1,196 @@
+/*
+ * gbfuse.h -- C ABI of the GB300 (sm_103a) fused GEMM + epilogue library.
+ *
+ * The operation: a bf16 matrix product whose pointwise ending is applied to
+ * each output tile while it is still on-chip, so the product crosses HBM
+ * once ("Fusion and Epilogues", bullet "Epilogue fusion, the mechanical
+ * form": alpha*AB + beta*C, bias and activation applied in registers on the
+ * way to the one memory write; "Kernel fusion" guide, section "Concept":
+ * bias, activation, scaling, residual add; "kernel fusion" wiki, the
+ * activation-after-matmul case).
+ *
+ * Conventions shared by every entry point
+ *   - Matrices are row-major.  bf16 arguments point at IEEE bfloat16 values;
+ *     results are rounded to bf16 round-to-nearest-even from fp32.
+ *   - Every pointer is a DEVICE pointer of the current CUDA device, owned by
+ *     the caller; the library keeps no reference after the call returns and
+ *     never allocates device memory.
+ *   - Inputs must not overlap `out`, except `residual == out` (an in-place
+ *     residual add), which is allowed.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     GBF_OK means the work was enqueued; a kernel that gives up on a
+ *     bounded wait is reported later by gbf_check_device_error().
+ *   - Errors are returned, never printed or thrown.  Argument, alignment and
+ *     shape errors are detected before anything is launched.
+ *   - Alignment: every non-null pointer 16-byte aligned; K % 8 == 0 and
+ *     N % 8 == 0 (16-byte row strides for the TMA engine).  M >= 0 is free;
+ *     M, N or K == 0 is accepted (an empty output, or with K == 0 an empty
+ *     sum, acc = 0).
+ *   - Null operands: C == NULL means beta is ignored; bias == NULL and
+ *     residual == NULL mean zero.
+ *   - Arithmetic: bf16 x bf16 products accumulated in fp32 on the tensor
+ *     cores (tcgen05, accumulators in tensor memory), epilogue in fp32,
+ *     one rounding to bf16.
+ */
+#ifndef GBFUSE_H
+#define GBFUSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GBF_API __attribute__((visibility("default")))
+#else
+#define GBF_API
+#endif
+
+/* A cudaStream_t (the two types are the same pointer type). */
+typedef struct CUstream_st *gbf_stream_t;
+
+/* Activation `act` of the epilogue. */
+#define GBF_ACT_IDENTITY 0
+#define GBF_ACT_RELU 1      /* max(v, 0) */
+#define GBF_ACT_SILU 2      /* v * sigmoid(v)  ("Fusion Thinking", Pattern 2) */
+#define GBF_ACT_GELU_TANH 3 /* 0.5 v (1 + tanh(sqrt(2/pi)(v + 0.044715 v^3))) */
+
+/* Layout of the second operand `B` / weights. */
+#define GBF_B_KN 0 /* B is K x N, N contiguous: computes A * B          */
+#define GBF_B_NK 1 /* W is N x K, K contiguous: computes A * W^T        */
+
+/* Status codes. */
+typedef int gbf_status_t;
+#define GBF_OK 0
+#define GBF_ERR_INVALID_ARG 1       /* null required pointer, bad enum, negative size */
+#define GBF_ERR_MISALIGNED 2        /* pointer not 16-byte aligned */
+#define GBF_ERR_UNSUPPORTED_SHAPE 3 /* N or K not a multiple of 8, bad group size, too large */
+#define GBF_ERR_WORKSPACE 4         /* workspace missing or too small */
+#define GBF_ERR_CUDA 5              /* a CUDA runtime/driver call failed */
+#define GBF_ERR_TIMEOUT 6           /* a kernel gave up on a bounded wait */
+#define GBF_ERR_NO_DEVICE 7         /* no sm_103-class device is current */
+
+/* Operation ids for gbf_workspace_size(). */
+#define GBF_OP_GEMM_EPILOGUE 0
+#define GBF_OP_SWIGLU 1
+#define GBF_OP_W4A16 2
+
+/*
+ * gemm_epilogue -- out[M][N] = bf16( act(alpha * A*B~ + beta*C + bias) + residual )
+ *   A         [M][K] bf16, required.
+ *   B         b_layout == GBF_B_KN: [K][N] bf16;  GBF_B_NK: W [N][K] bf16
+ *             (then B~ = W^T).  Required.
+ *   C         [M][N] bf16 or NULL.   bias [N] bf16 or NULL (broadcast over rows).
+ *   residual  [M][N] bf16 or NULL, added after the activation; may equal out.
+ *   out       [M][N] bf16, required.
+ *   workspace unused by the fused kernels (pass NULL, 0).
+ * Order of the ending: bias inside the activation, residual outside it
+ * ("Fusion and Epilogues", epilogue-fusion bullet; "Kernel fusion" guide,
+ * "Check yourself": bias, activation and residual add in one pass).
+ */
+GBF_API gbf_status_t gemm_epilogue(const void *A, const void *B, int b_layout, const void *C,
+                           const void *bias, const void *residual, void *out, int64_t M,
+                           int64_t N, int64_t K, float alpha, float beta, int act,
+                           void *workspace, size_t workspace_bytes, gbf_stream_t stream);
+
+/*
+ * swiglu_dual_gemm -- h[M][N] = bf16( act(alpha*g) * (alpha*u) + beta*C ),
+ *   g = x*Wg~, u = x*Wu~ with the same layout rule as gemm_epilogue
+ *   ("Fusion Thinking", Pattern 2, level 2: both products from one x tile in
+ *   one kernel, SiLU(gate)*up in the epilogue).  act = GBF_ACT_SILU gives
+ *   SwiGLU; GELU_TANH / RELU / IDENTITY give the other gated units.
+ *   x [M][K]; w_gate, w_up [N][K] (GBF_B_NK) or [K][N] (GBF_B_KN); C [M][N]
+ *   or NULL; h [M][N].  Workspace unused (NULL, 0).
+ */
+GBF_API gbf_status_t swiglu_dual_gemm(const void *x, const void *w_gate, const void *w_up,
+                              int w_layout, void *h, int64_t M, int64_t N, int64_t K,
+                              float alpha, float beta, const void *C, int act,
+                              void *workspace, size_t workspace_bytes, gbf_stream_t stream);
+
+/*
+ * w4a16_gemm -- the gemm_epilogue result with B~[k][n] = bf16((q[k][n] - 8) * s[k/G][n]),
+ *   dequantised on-chip ("Fusion Thinking", Pattern 3: the kernel loads int4
+ *   weights and scales directly, dequantises them on-chip, zero point 8).
+ *   Wq     [K][N/2] bytes; byte j of row k holds column 2j in its HIGH nibble
+ *          and column 2j+1 in its LOW nibble (interleave(w_hi, w_lo)).
+ *   scales [K/group_size][N] bf16.   group_size: a multiple of 64 dividing K.
+ *   A [M][K] bf16; C, bias, residual, out as in gemm_epilogue.
+ *   Requires N % 32 == 0.  Workspace unused (NULL, 0).
+ */
+GBF_API gbf_status_t w4a16_gemm(const void *A, const uint8_t *Wq, const void *scales, int group_size,
+                        const void *C, const void *bias, const void *residual, void *out,
+                        int64_t M, int64_t N, int64_t K, float alpha, float beta, int act,
+                        void *workspace, size_t workspace_bytes, gbf_stream_t stream);
+
+/*
+ * Unfused reference compositions: the same results as above, computed the
+ * way an eager framework does it, with the intermediate written to HBM and
+ * read back by a second kernel ("kernel fusion" wiki: unfused, the product
+ * writes its whole output and a second kernel reads it, applies the
+ * activation and writes it again; "Fusion Thinking", Pattern 2 un-fused and
+ * Pattern 3 un-fused).  They exist to measure the bytes fusion deletes.
+ * The intermediates live in the caller's workspace (256-byte aligned
+ * sections, gbf_workspace_size() bytes):
+ *   gemm_epilogue_unfused   D = bf16(A*B~) [M][N] at offset 0, then the
+ *                           pointwise ending D -> out.
+ *   swiglu_dual_gemm_unfused  g = bf16(x*Wg~) [M][N] at 0, u = bf16(x*Wu~)
+ *                           [M][N] at align256(2*M*N), then the GLU pass.
+ *   w4a16_gemm_unfused      w = bf16((q-8)*s) [K][N] at 0, then a bf16
+ *                           GEMM with the fused ending (identical result).
+ * The workspace contents are left in place after the call.
+ */
+GBF_API gbf_status_t gemm_epilogue_unfused(const void *A, const void *B, int b_layout, const void *C,
+                                   const void *bias, const void *residual, void *out,
+                                   int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                                   int act, void *workspace, size_t workspace_bytes,
+                                   gbf_stream_t stream);
+GBF_API gbf_status_t swiglu_dual_gemm_unfused(const void *x, const void *w_gate, const void *w_up,
+                                      int w_layout, void *h, int64_t M, int64_t N, int64_t K,
+                                      float alpha, float beta, const void *C, int act,
+                                      void *workspace, size_t workspace_bytes,
+                                      gbf_stream_t stream);
+GBF_API gbf_status_t w4a16_gemm_unfused(const void *A, const uint8_t *Wq, const void *scales,
+                                int group_size, const void *C, const void *bias,
+                                const void *residual, void *out, int64_t M, int64_t N,
+                                int64_t K, float alpha, float beta, int act, void *workspace,
+                                size_t workspace_bytes, gbf_stream_t stream);
+
+/* Workspace bytes an entry point needs (0 for the fused ones).  `op` is a
+ * GBF_OP_* id; `fused` selects the fused (1) or unfused (0) entry point. */
+GBF_API size_t gbf_workspace_size(int op, int64_t M, int64_t N, int64_t K, int fused);
+
+/* Synchronises `stream`, then reads and clears the library's device error
+ * word on the current device.  Returns GBF_OK, GBF_ERR_TIMEOUT (a kernel
+ * gave up on a bounded wait; its output is undefined) or GBF_ERR_CUDA. */
+GBF_API gbf_status_t gbf_check_device_error(gbf_stream_t stream);
+
+/* A static, human-readable name of a status code. */
+GBF_API const char *gbf_status_string(gbf_status_t status);
+
+/* Limit, in nanoseconds, of every bounded wait inside the kernels (default
+ * 2e9 = 2 s; clamped to [1e6, 6e10]).  Applies to later launches. */
+GBF_API gbf_status_t gbf_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook: when `on` is non-zero, the next launches of the fused GEMM
+ * kernels withhold one accumulator-ready signal so that the epilogue's
+ * bounded wait runs out; the kernel then records GBF_ERR_TIMEOUT and exits
+ * cleanly.  Off by default. */
+GBF_API gbf_status_t gbf_debug_inject_timeout(int on);
+
+/* Which kernel family a call with these arguments runs (for tests and the
+ * benchmark's roofline attribution): 1 = persistent 128x256-tile kernel,
+ * 2 = small-M swapped kernel with cluster split-K, 3 = W4A16 kernel,
+ * 0 = no launch (empty output), -1 = the arguments would be rejected.
+ * `*splits` (may be NULL) receives the split-K cluster size. */
+GBF_API int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int *splits);
+
+/* Library version, e.g. 100 for 1.0.0. */
+GBF_API int gbf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBFUSE_H */

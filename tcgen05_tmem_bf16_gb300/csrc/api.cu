@@ -1,0 +1,460 @@
+// api.cu -- the C ABI declared in include/gbfuse.h: argument validation,
+// TMA tensor-map encoding, kernel-family selection by shape, launch, and
+// status codes.  Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gbfuse.h"
+#include "internal.h"
+
+namespace gbf {
+
+// The device error word written by kernels that give up on a bounded wait.
+__device__ unsigned g_gbf_error_word;
+
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_inject{0};
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+  std::once_flag once;
+  DeviceInfo info;
+  unsigned* err = nullptr;
+  cudaError_t status = cudaSuccess;
+};
+DevState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// Current device, its properties and the address of its error word.
+gbf_status_t current_device(const DeviceInfo** info, unsigned** err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return GBF_ERR_NO_DEVICE;
+  DevState& d = g_dev[dev];
+  std::call_once(d.once, [&d, dev]() {
+    int sms = 0, major = 0, minor = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_gbf_error_word);
+      d.err = static_cast<unsigned*>(p);
+    }
+    d.info.sms = sms;
+    d.info.cc_major = major;
+    d.info.cc_minor = minor;
+    d.status = e;
+  });
+  if (d.status != cudaSuccess) return GBF_ERR_CUDA;
+  if (d.info.cc_major != 10 || d.info.cc_minor != 3) return GBF_ERR_NO_DEVICE;
+  *info = &d.info;
+  *err = d.err;
+  return GBF_OK;
+}
+
+bool encoder() {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// Row-major 2-D tensor [outer][inner] with `row_bytes` between rows.
+bool tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner,
+             uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+             CUtensorMapSwizzle swz) {
+  if (!encoder()) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+gbf_status_t check_common(int64_t M, int64_t N, int64_t K, int act) {
+  if (M < 0 || N < 0 || K < 0) return GBF_ERR_INVALID_ARG;
+  if (act < GBF_ACT_IDENTITY || act > GBF_ACT_GELU_TANH) return GBF_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GBF_ERR_UNSUPPORTED_SHAPE;
+  if (N % 8 != 0 || K % 8 != 0) return GBF_ERR_UNSUPPORTED_SHAPE;
+  return GBF_OK;
+}
+
+gbf_status_t check_ptrs(std::initializer_list<const void*> required,
+                        std::initializer_list<const void*> optional) {
+  for (const void* p : required) {
+    if (!p) return GBF_ERR_INVALID_ARG;
+    if (!aligned16(p)) return GBF_ERR_MISALIGNED;
+  }
+  for (const void* p : optional)
+    if (p && !aligned16(p)) return GBF_ERR_MISALIGNED;
+  return GBF_OK;
+}
+
+KernelCtl make_ctl(unsigned* err) {
+  return KernelCtl{err, static_cast<unsigned long long>(g_timeout_ns.load()), g_inject.load()};
+}
+
+gbf_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? GBF_OK : GBF_ERR_CUDA; }
+
+EpiParams make_ep(const void* C, const void* bias, const void* residual, void* out, float alpha,
+                  float beta, int act) {
+  return EpiParams{static_cast<const __nv_bfloat16*>(C), static_cast<const __nv_bfloat16*>(bias),
+                   static_cast<const __nv_bfloat16*>(residual), static_cast<__nv_bfloat16*>(out),
+                   alpha, beta, act};
+}
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+int choose_splits(int tiles, int num_kb, const DeviceInfo& dev) {
+  const int slots = dev.sms * 2;  // the swapped kernels fit two CTAs per SM
+  int s = tiles > 0 ? slots / tiles : 1;
+  s = std::max(1, std::min(s, kMaxSplits));
+  s = std::min(s, std::max(1, num_kb));
+  return s;
+}
+
+// Dense GEMM (+ dual) launch after validation.  D rows of out.
+gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, bool dual,
+                      const EpiParams& ep, int64_t M, int64_t N, int64_t K,
+                      const DeviceInfo& dev, unsigned* err, cudaStream_t stream) {
+  if (M == 0 || N == 0) return GBF_OK;
+  if (K == 0) {
+    if (dual) {
+      // act(0) * 0 + beta*C: a zero product through the GLU ending.
+      EpiParams z = ep;
+      z.alpha = 0.0f;
+      z.act = GBF_ACT_IDENTITY;
+      z.bias = nullptr;
+      z.residual = nullptr;
+      return cuda_status(launch_pointwise_epilogue(nullptr, z, M, N, dev.sms, stream));
+    }
+    return cuda_status(launch_pointwise_epilogue(nullptr, ep, M, N, dev.sms, stream));
+  }
+  const GemmPlan plan = plan_gemm(M, N, K, dual, dev);
+  const bool kn = layout == GBF_B_KN;
+  CUtensorMap tmA, tmW, tmW2;
+  const uint32_t a_rows = plan.path == kPathSwap ? plan.mpad : kBM;
+  if (!tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, kBK, a_rows,
+               CU_TENSOR_MAP_SWIZZLE_128B))
+    return GBF_ERR_CUDA;
+  uint32_t w_rows = plan.path == kPathSwap ? kSwapBN : (dual ? 128 : kPersistBN);
+  const void* ws[2] = {W, dual ? W2 : W};
+  CUtensorMap* maps[2] = {&tmW, &tmW2};
+  for (int i = 0; i < 2; ++i) {
+    bool ok = kn ? tmap_2d(maps[i], ws[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, K, N * 2, 64, kBK,
+                           CU_TENSOR_MAP_SWIZZLE_128B)
+                 : tmap_2d(maps[i], ws[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, N, K * 2, kBK,
+                           w_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return GBF_ERR_CUDA;
+  }
+  return cuda_status(launch_gemm(plan, kn, dual, tmA, tmW, tmW2, ep, static_cast<int>(M),
+                                 static_cast<int>(N), static_cast<int>(K), make_ctl(err),
+                                 stream));
+}
+
+gbf_status_t run_w4(const void* A, const uint8_t* Wq, const void* scales, int group,
+                    const EpiParams& ep, int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
+                    unsigned* err, cudaStream_t stream) {
+  if (M == 0 || N == 0) return GBF_OK;
+  if (K == 0) return cuda_status(launch_pointwise_epilogue(nullptr, ep, M, N, dev.sms, stream));
+  const GemmPlan plan = plan_w4a16(M, N, K, dev);
+  CUtensorMap tmA, tmQ, tmS;
+  if (!tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, kBK, plan.mpad,
+               CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tmap_2d(&tmQ, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, N / 2, K, N / 2, kW4BN / 2, kBK,
+               CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !tmap_2d(&tmS, scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, K / group, N * 2, kW4BN, 1,
+               CU_TENSOR_MAP_SWIZZLE_NONE))
+    return GBF_ERR_CUDA;
+  return cuda_status(launch_w4a16(plan, tmA, tmQ, tmS, ep, static_cast<int>(M),
+                                  static_cast<int>(N), static_cast<int>(K), group, make_ctl(err),
+                                  stream));
+}
+
+gbf_status_t check_w4(int64_t M, int64_t N, int64_t K, int group, int act) {
+  gbf_status_t st = check_common(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if (group <= 0) return GBF_ERR_INVALID_ARG;
+  if (group % kBK != 0 || K % group != 0 || N % 32 != 0) return GBF_ERR_UNSUPPORTED_SHAPE;
+  return GBF_OK;
+}
+
+}  // namespace
+
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo& dev) {
+  GemmPlan p;
+  if (M == 0 || N == 0 || K == 0) return p;
+  p.num_kb = ceil_div(K, kBK);
+  if (!dual && M <= 128) {
+    p.path = kPathSwap;
+    p.mpad = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
+    p.m_tiles = 1;
+    p.n_tiles = ceil_div(N, kSwapBN);
+    p.splits = choose_splits(p.n_tiles, p.num_kb, dev);
+  } else {
+    p.path = kPathPersistent;
+    p.m_tiles = ceil_div(M, kBM);
+    p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
+    p.grid = std::min(p.m_tiles * p.n_tiles, std::max(1, dev.sms));
+  }
+  return p;
+}
+
+GemmPlan plan_w4a16(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+  GemmPlan p;
+  if (M == 0 || N == 0 || K == 0) return p;
+  p.path = kPathW4;
+  p.num_kb = ceil_div(K, kBK);
+  p.mpad = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+  p.m_tiles = ceil_div(M, p.mpad);
+  p.n_tiles = ceil_div(N, kW4BN);
+  p.splits = choose_splits(p.n_tiles * p.m_tiles, p.num_kb, dev);
+  return p;
+}
+
+}  // namespace gbf
+
+using namespace gbf;
+
+extern "C" {
+
+gbf_status_t gemm_epilogue(const void* A, const void* B, int b_layout, const void* C,
+                           const void* bias, const void* residual, void* out, int64_t M,
+                           int64_t N, int64_t K, float alpha, float beta, int act,
+                           void* workspace, size_t workspace_bytes, gbf_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  gbf_status_t st = check_common(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if (b_layout != GBF_B_KN && b_layout != GBF_B_NK) return GBF_ERR_INVALID_ARG;
+  if ((st = check_ptrs({A, B, out}, {C, bias, residual})) != GBF_OK) return st;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  return run_gemm(A, B, nullptr, b_layout, false, make_ep(C, bias, residual, out, alpha, beta, act),
+                  M, N, K, *dev, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gbf_status_t swiglu_dual_gemm(const void* x, const void* w_gate, const void* w_up, int w_layout,
+                              void* h, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                              const void* C, int act, void* workspace, size_t workspace_bytes,
+                              gbf_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  gbf_status_t st = check_common(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if (w_layout != GBF_B_KN && w_layout != GBF_B_NK) return GBF_ERR_INVALID_ARG;
+  if ((st = check_ptrs({x, w_gate, w_up, h}, {C})) != GBF_OK) return st;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  return run_gemm(x, w_gate, w_up, w_layout, true,
+                  make_ep(C, nullptr, nullptr, h, alpha, beta, act), M, N, K, *dev, err,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+gbf_status_t w4a16_gemm(const void* A, const uint8_t* Wq, const void* scales, int group_size,
+                        const void* C, const void* bias, const void* residual, void* out,
+                        int64_t M, int64_t N, int64_t K, float alpha, float beta, int act,
+                        void* workspace, size_t workspace_bytes, gbf_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  gbf_status_t st = check_w4(M, N, K, group_size, act);
+  if (st != GBF_OK) return st;
+  if ((st = check_ptrs({A, Wq, scales, out}, {C, bias, residual})) != GBF_OK) return st;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  return run_w4(A, Wq, scales, group_size, make_ep(C, bias, residual, out, alpha, beta, act), M,
+                N, K, *dev, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gbf_workspace_size(int op, int64_t M, int64_t N, int64_t K, int fused) {
+  if (fused || M < 0 || N < 0 || K < 0) return 0;
+  switch (op) {
+    case GBF_OP_GEMM_EPILOGUE: return align256(static_cast<size_t>(M * N) * 2);
+    case GBF_OP_SWIGLU: return 2 * align256(static_cast<size_t>(M * N) * 2);
+    case GBF_OP_W4A16: return align256(static_cast<size_t>(K * N) * 2);
+    default: return 0;
+  }
+}
+
+gbf_status_t gemm_epilogue_unfused(const void* A, const void* B, int b_layout, const void* C,
+                                   const void* bias, const void* residual, void* out, int64_t M,
+                                   int64_t N, int64_t K, float alpha, float beta, int act,
+                                   void* workspace, size_t workspace_bytes, gbf_stream_t stream) {
+  gbf_status_t st = check_common(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if (b_layout != GBF_B_KN && b_layout != GBF_B_NK) return GBF_ERR_INVALID_ARG;
+  if ((st = check_ptrs({A, B, out}, {C, bias, residual})) != GBF_OK) return st;
+  const size_t need = gbf_workspace_size(GBF_OP_GEMM_EPILOGUE, M, N, K, 0);
+  if (need && (!workspace || workspace_bytes < need)) return GBF_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return GBF_ERR_MISALIGNED;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || N == 0) return GBF_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const EpiParams ep = make_ep(C, bias, residual, out, alpha, beta, act);
+  if (K == 0) return cuda_status(launch_pointwise_epilogue(nullptr, ep, M, N, dev->sms, s));
+  __nv_bfloat16* D = static_cast<__nv_bfloat16*>(workspace);
+  st = run_gemm(A, B, nullptr, b_layout, false,
+                make_ep(nullptr, nullptr, nullptr, D, 1.0f, 0.0f, GBF_ACT_IDENTITY), M, N, K,
+                *dev, err, s);
+  if (st != GBF_OK) return st;
+  return cuda_status(launch_pointwise_epilogue(D, ep, M, N, dev->sms, s));
+}
+
+gbf_status_t swiglu_dual_gemm_unfused(const void* x, const void* w_gate, const void* w_up,
+                                      int w_layout, void* h, int64_t M, int64_t N, int64_t K,
+                                      float alpha, float beta, const void* C, int act,
+                                      void* workspace, size_t workspace_bytes,
+                                      gbf_stream_t stream) {
+  gbf_status_t st = check_common(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if (w_layout != GBF_B_KN && w_layout != GBF_B_NK) return GBF_ERR_INVALID_ARG;
+  if ((st = check_ptrs({x, w_gate, w_up, h}, {C})) != GBF_OK) return st;
+  const size_t need = gbf_workspace_size(GBF_OP_SWIGLU, M, N, K, 0);
+  if (need && (!workspace || workspace_bytes < need)) return GBF_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return GBF_ERR_MISALIGNED;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || N == 0) return GBF_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  __nv_bfloat16* g = static_cast<__nv_bfloat16*>(workspace);
+  __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) +
+                                                      align256(static_cast<size_t>(M * N) * 2));
+  const EpiParams plain_g = make_ep(nullptr, nullptr, nullptr, g, 1.0f, 0.0f, GBF_ACT_IDENTITY);
+  const EpiParams plain_u = make_ep(nullptr, nullptr, nullptr, u, 1.0f, 0.0f, GBF_ACT_IDENTITY);
+  if ((st = run_gemm(x, w_gate, nullptr, w_layout, false, plain_g, M, N, K, *dev, err, s)) !=
+      GBF_OK)
+    return st;
+  if ((st = run_gemm(x, w_up, nullptr, w_layout, false, plain_u, M, N, K, *dev, err, s)) != GBF_OK)
+    return st;
+  return cuda_status(launch_swiglu_pointwise(
+      g, u, make_ep(C, nullptr, nullptr, h, alpha, beta, act), M, N, dev->sms, s));
+}
+
+gbf_status_t w4a16_gemm_unfused(const void* A, const uint8_t* Wq, const void* scales,
+                                int group_size, const void* C, const void* bias,
+                                const void* residual, void* out, int64_t M, int64_t N, int64_t K,
+                                float alpha, float beta, int act, void* workspace,
+                                size_t workspace_bytes, gbf_stream_t stream) {
+  gbf_status_t st = check_w4(M, N, K, group_size, act);
+  if (st != GBF_OK) return st;
+  if ((st = check_ptrs({A, Wq, scales, out}, {C, bias, residual})) != GBF_OK) return st;
+  const size_t need = gbf_workspace_size(GBF_OP_W4A16, M, N, K, 0);
+  if (need && (!workspace || workspace_bytes < need)) return GBF_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return GBF_ERR_MISALIGNED;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || N == 0) return GBF_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const EpiParams ep = make_ep(C, bias, residual, out, alpha, beta, act);
+  if (K == 0) return cuda_status(launch_pointwise_epilogue(nullptr, ep, M, N, dev->sms, s));
+  __nv_bfloat16* w = static_cast<__nv_bfloat16*>(workspace);
+  if ((st = cuda_status(launch_dequant_int4(Wq, static_cast<const __nv_bfloat16*>(scales),
+                                            group_size, K, N, w, dev->sms, s))) != GBF_OK)
+    return st;
+  return run_gemm(A, w, nullptr, GBF_B_KN, false, ep, M, N, K, *dev, err, s);
+}
+
+gbf_status_t gbf_check_device_error(gbf_stream_t stream) {
+  const DeviceInfo* dev;
+  unsigned* err;
+  gbf_status_t st = current_device(&dev, &err);
+  if (st != GBF_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GBF_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GBF_ERR_CUDA;
+  if (word == 0) return GBF_OK;
+  const unsigned zero = 0;
+  if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return GBF_ERR_CUDA;
+  return (word & 0xFFu) == GBF_ERR_TIMEOUT ? GBF_ERR_TIMEOUT : GBF_ERR_CUDA;
+}
+
+const char* gbf_status_string(gbf_status_t status) {
+  switch (status) {
+    case GBF_OK: return "ok";
+    case GBF_ERR_INVALID_ARG: return "invalid argument";
+    case GBF_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case GBF_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case GBF_ERR_WORKSPACE: return "workspace missing or too small";
+    case GBF_ERR_CUDA: return "CUDA error";
+    case GBF_ERR_TIMEOUT: return "kernel gave up on a bounded wait";
+    case GBF_ERR_NO_DEVICE: return "no sm_103 device is current";
+    default: return "unknown status";
+  }
+}
+
+gbf_status_t gbf_set_wait_timeout_ns(uint64_t ns) {
+  ns = std::max<uint64_t>(1000000ull, std::min<uint64_t>(ns, 60000000000ull));
+  g_timeout_ns.store(ns);
+  return GBF_OK;
+}
+
+gbf_status_t gbf_debug_inject_timeout(int on) {
+  g_inject.store(on ? 1 : 0);
+  return GBF_OK;
+}
+
+int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int* splits) {
+  if (splits) *splits = 0;
+  DeviceInfo dev;
+  const DeviceInfo* d = nullptr;
+  unsigned* err = nullptr;
+  if (current_device(&d, &err) == GBF_OK) dev = *d;
+  else dev.sms = 152;
+  GemmPlan p;
+  switch (op) {
+    case GBF_OP_GEMM_EPILOGUE:
+    case GBF_OP_SWIGLU:
+      if (check_common(M, N, K, 0) != GBF_OK || (b_layout != GBF_B_KN && b_layout != GBF_B_NK))
+        return -1;
+      p = plan_gemm(M, N, K, op == GBF_OP_SWIGLU, dev);
+      break;
+    case GBF_OP_W4A16:
+      if (check_w4(M, N, K, 128, 0) != GBF_OK) return -1;
+      p = plan_w4a16(M, N, K, dev);
+      break;
+    default: return -1;
+  }
+  if (splits) *splits = p.splits;
+  return p.path;
+}
+
+int gbf_version(void) { return 100; }
+
+}  // extern "C"

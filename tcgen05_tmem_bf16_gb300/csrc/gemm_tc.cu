@@ -1,0 +1,613 @@
+// gemm_tc.cu -- tcgen05/TMEM bf16 GEMM with the pointwise ending fused into
+// the epilogue, for sm_103a.
+//
+// The ending act(alpha*acc + beta*C + bias) + residual is applied to each
+// accumulator tile after it leaves tensor memory and before its one write
+// to HBM ("Fusion and Epilogues", epilogue-fusion bullet; "Kernel fusion"
+// guide, Concept).  The gate/up variant computes both products from the same
+// x tile in one MMA and applies act(gate)*up in the epilogue ("Fusion
+// Thinking", Pattern 2, level 2).
+//
+// Two kernels:
+//  * gemm_persistent_kernel -- large M.  One CTA per SM walks output tiles
+//    of 128 x 256 (dual: 128 x 128 from a 256-wide stacked [gate; up] B
+//    tile).  Warp 0 issues TMA loads into a 4-stage shared-memory ring, warp 1
+//    issues tcgen05.mma into one of two 256-column TMEM accumulators, warps
+//    4-7 drain the other accumulator through the epilogue, so the ending of
+//    tile t overlaps the main loop of tile t+1.
+//  * gemm_swap_kernel -- small M (<= 128).  Computes out^T = W~^T * A^T so
+//    that the weight tile fills the 128-row MMA and the few rows of A become
+//    the MMA's N (16..128).  The K range is split across the CTAs of a thread
+//    block cluster; partial accumulators are summed in rank order through
+//    distributed shared memory by the cluster's rank-0 CTA, which then
+//    applies the ending.  No global scratch memory is used.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gbf {
+
+constexpr int kUK = 16;  // K per tcgen05.mma, kind::f16
+
+// ============================================================ shared pieces
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Epilogue of 32 consecutive output columns of one row (persistent kernel).
+// `acc` holds fp32 bit patterns; for the dual GEMM `up` holds the up
+// product and the result is act(alpha*g) * (alpha*u) + beta*C.
+template <int ACT, bool DUAL>
+__device__ __forceinline__ void epi_row32(const uint32_t (&acc)[32], const uint32_t (&up)[32],
+                                          int64_t row, int col0, int N, const EpiParams& e) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int col = col0 + v * 8;
+    if (col >= N) break;
+    const int64_t off = row * N + col;
+    float x[8];
+    if constexpr (DUAL) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        x[i] = act_apply<ACT>(e.alpha * __uint_as_float(acc[v * 8 + i])) *
+               (e.alpha * __uint_as_float(up[v * 8 + i]));
+      if (e.C) {
+        float c[8];
+        unpack8(ldg_u4(e.C + off), c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = fmaf(e.beta, c[i], x[i]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = e.alpha * __uint_as_float(acc[v * 8 + i]);
+      if (e.C) {
+        float c[8];
+        unpack8(ldg_u4(e.C + off), c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = fmaf(e.beta, c[i], x[i]);
+      }
+      if (e.bias) {
+        float b[8];
+        unpack8(ldg_u4(e.bias + col), b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] += b[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = act_apply<ACT>(x[i]);
+      if (e.residual) {
+        float r[8];
+        unpack8(ld_u4(e.residual + off), r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] += r[i];
+      }
+    }
+    st_u4(e.out + off, pack8(x));
+  }
+}
+
+// ============================================================ persistent kernel
+
+constexpr int kPStages = 4;
+constexpr int kPABytes = kBM * kBK * 2;             // 16 KB
+constexpr int kPBBytes = kPersistBN * kBK * 2;      // 32 KB
+constexpr int kPStageBytes = kPABytes + kPBBytes;   // 48 KB
+constexpr int kPThreads = 256;
+constexpr int kPSmem = 1024 + kPStages * kPStageBytes + 256;
+constexpr int kPGroupM = 16;                        // tile raster: 16 M-tiles per group
+
+struct PersistArgs {
+  int M, N, K;
+  int m_tiles, n_tiles, num_kb;
+  EpiParams ep;
+  KernelCtl ctl;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mb, int& nb) {
+  const int per_group = kPGroupM * n_tiles;
+  const int g = t / per_group;
+  const int first_m = g * kPGroupM;
+  const int gm = min(kPGroupM, m_tiles - first_m);
+  const int local = t - g * per_group;
+  nb = local / gm;
+  mb = first_m + local % gm;
+}
+
+template <bool W_KN, bool DUAL>
+__global__ void __launch_bounds__(kPThreads, 1)
+    gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmW,
+                           const __grid_constant__ CUtensorMap tmW2, const PersistArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPStages * kPStageBytes);
+  uint64_t* empty = full + kPStages;
+  uint64_t* tfull = empty + kPStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmW);
+    if (DUAL) tma_prefetch_desc(&tmW2);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag};
+  const int num_tiles = a.m_tiles * a.n_tiles;
+  const int num_kb = a.num_kb;
+  const int out_bn = DUAL ? 128 : 256;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t fills[kPStages];
+#pragma unroll
+      for (int i = 0; i < kPStages; ++i) fills[i] = 0;
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + s * kPStageBytes;
+          uint8_t* sb = sa + kPABytes;
+          mbar_arrive_expect_tx(&full[s], kPStageBytes);
+          tma_load_2d(sa, &tmA, &full[s], kb * kBK, mb * kBM);
+          if constexpr (W_KN) {
+            // B[K][N]: four 64-column blocks of 64 k-rows (MN-major operand).
+            if constexpr (DUAL) {
+              for (int j = 0; j < 2; ++j) {
+                tma_load_2d(sb + j * 8192, &tmW, &full[s], nb * 128 + 64 * j, kb * kBK);
+                tma_load_2d(sb + (2 + j) * 8192, &tmW2, &full[s], nb * 128 + 64 * j, kb * kBK);
+              }
+            } else {
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d(sb + j * 8192, &tmW, &full[s], nb * 256 + 64 * j, kb * kBK);
+            }
+          } else {
+            // W[N][K]: rows of 64 k (K-major operand); dual stacks gate over up.
+            if constexpr (DUAL) {
+              tma_load_2d(sb, &tmW, &full[s], kb * kBK, nb * 128);
+              tma_load_2d(sb + 128 * 128, &tmW2, &full[s], kb * kBK, nb * 128);
+            } else {
+              tma_load_2d(sb, &tmW, &full[s], kb * kBK, nb * 256);
+            }
+          }
+          fills[s]++;
+          if (++s == kPStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      // Every issued copy must land before the CTA may exit.
+      for (int i = 0; i < kPStages; ++i)
+        if (fills[i]) wait_bar(&full[i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, kPersistBN, false, W_KN);
+      int s = 0;
+      uint32_t ph = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!wait_bar(&tempty[buf], aph ^ 1, ctl, kSiteMmaAccEmpty)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * 256;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(stages + s * kPStageBytes);
+          const uint32_t b0 = a0 + kPABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUK; ++k) {
+            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t bd = W_KN ? sdesc_sw128(b0 + k * 2048, 8192, 1024)
+                                     : sdesc_sw128(b0 + k * 32, 16, 1024);
+            mma_ss(d, ad, bd, idesc, (kb | k) != 0);
+          }
+          mma_commit(&empty[s]);
+          if (++s == kPStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        if (!(a.ctl.inject && local == 0)) mma_commit(&tfull[buf]);
+      }
+      mma_commit(done);
+      wait_bar(done, 0, ctl, kSiteDrain, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    int local = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+      const int buf = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      if (!wait_bar(&tfull[buf], aph, ctl, kSiteEpiAccFull)) break;
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(mb) * kBM + q * 32 + lane;
+      const uint32_t tb = tmem_base + buf * 256 + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < out_bn / 32; ++c) {
+        uint32_t acc[32], up[32];
+        tmem_ld32(tb + c * 32, acc);
+        if constexpr (DUAL) tmem_ld32(tb + 128 + c * 32, up);
+        tmem_wait_ld();
+        if (c == out_bn / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
+        }
+        if (row < a.M) {
+          const int col0 = nb * out_bn + c * 32;
+          switch (a.ep.act) {
+            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, row, col0, a.N, a.ep); break;
+            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, row, col0, a.N, a.ep); break;
+            case kActGeluTanh:
+              epi_row32<kActGeluTanh, DUAL>(acc, up, row, col0, a.N, a.ep);
+              break;
+            default: epi_row32<kActIdentity, DUAL>(acc, up, row, col0, a.N, a.ep); break;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ============================================================ swapped small-M kernel
+
+template <int MPAD>
+struct SwapCfg {
+  static constexpr int kWBytes = kSwapBN * kBK * 2;          // 16 KB weight tile
+  static constexpr int kXBytes = MPAD * kBK * 2;             // activation tile
+  static constexpr int kStageBytes = kWBytes + kXBytes;
+  static constexpr int kStages = MPAD <= 32 ? 5 : (MPAD <= 64 ? 4 : 3);
+  static constexpr uint32_t kTmemCols = MPAD < 32 ? 32 : MPAD;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
+  static_assert(kStages * kStageBytes >= 128 * MPAD * 4, "reduction buffer must fit");
+};
+
+struct SwapArgs {
+  int M, N, K;
+  int num_kb;
+  int splits;
+  EpiParams ep;
+  KernelCtl ctl;
+};
+
+// Epilogue of one output column n for 16 consecutive rows m0..m0+15.
+template <int ACT>
+__device__ __forceinline__ void epi_col16(const float (&v)[16], int64_t m0, int n, int M,
+                                          int N, const EpiParams& e) {
+  if (n >= N) return;
+  const float b = e.bias ? __bfloat162float(e.bias[n]) : 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int64_t m = m0 + j;
+    if (m >= M) break;
+    const int64_t off = m * N + n;
+    float x = e.alpha * v[j];
+    if (e.C) x = fmaf(e.beta, __bfloat162float(e.C[off]), x);
+    x = act_apply<ACT>(x + b);
+    if (e.residual) x += __bfloat162float(e.residual[off]);
+    e.out[off] = __float2bfloat16_rn(x);
+  }
+}
+
+template <int MPAD, bool W_KN>
+__global__ void __launch_bounds__(256, 2)
+    gemm_swap_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmW, const SwapArgs a) {
+  using Cfg = SwapCfg<MPAD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kStages * Cfg::kStageBytes);
+  uint64_t* empty = full + Cfg::kStages;
+  uint64_t* dfull = empty + Cfg::kStages;
+  uint64_t* done = dfull + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = a.splits;
+  const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
+  const int nb = blockIdx.y;
+  const int mb = blockIdx.z;
+  const int kb0 = static_cast<int>((static_cast<int64_t>(rank) * a.num_kb) / S);
+  const int kb1 = static_cast<int>((static_cast<int64_t>(rank + 1) * a.num_kb) / S);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cfg::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(dfull, 1);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t fills[Cfg::kStages];
+#pragma unroll
+      for (int i = 0; i < Cfg::kStages; ++i) fills[i] = 0;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) break;
+        uint8_t* sw = stages + s * Cfg::kStageBytes;
+        uint8_t* sx = sw + Cfg::kWBytes;
+        mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+        if constexpr (W_KN) {
+          tma_load_2d(sw, &tmW, &full[s], nb * kSwapBN, kb * kBK);
+          tma_load_2d(sw + 8192, &tmW, &full[s], nb * kSwapBN + 64, kb * kBK);
+        } else {
+          tma_load_2d(sw, &tmW, &full[s], kb * kBK, nb * kSwapBN);
+        }
+        tma_load_2d(sx, &tmA, &full[s], kb * kBK, mb * MPAD);
+        fills[s]++;
+        if (++s == Cfg::kStages) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      for (int i = 0; i < Cfg::kStages; ++i)
+        if (fills[i]) wait_bar(&full[i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, MPAD, W_KN, false);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t w0 = smem_u32(stages + s * Cfg::kStageBytes);
+        const uint32_t x0 = w0 + Cfg::kWBytes;
+#pragma unroll
+        for (int k = 0; k < kBK / kUK; ++k) {
+          const uint64_t ad = W_KN ? sdesc_sw128(w0 + k * 2048, 8192, 1024)
+                                   : sdesc_sw128(w0 + k * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(x0 + k * 32, 16, 1024);
+          mma_ss(tmem_base, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+        if (++s == Cfg::kStages) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      if (ok && !a.ctl.inject) mma_commit(dfull);
+      mma_commit(done);
+      wait_bar(done, 0, ctl, kSiteDrain, false);
+    }
+    __syncwarp();
+  }
+
+  // ---- epilogue warps: partial sums, cluster reduction, ending
+  const bool epi = warp >= 4;
+  const int q = warp & 3;
+  const int tid = threadIdx.x - 128;  // 0..127 for the epilogue warps = TMEM lane
+  const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  float4* red = reinterpret_cast<float4*>(stages);
+  bool have = false;
+  if (epi) {
+    have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
+    tc_fence_after();
+    if (S > 1 && rank != 0) {
+#pragma unroll 1
+      for (int c = 0; c < MPAD / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tb + c * 16, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          red[(c * 4 + v) * 128 + tid] =
+              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+      }
+    }
+  }
+  if (S > 1) cluster_sync_all();
+  if (epi && rank == 0) {
+    const int n = nb * kSwapBN + tid;
+#pragma unroll 1
+    for (int c = 0; c < MPAD / 16; ++c) {
+      uint32_t r[16];
+      tmem_ld16(tb + c * 16, r);
+      tmem_wait_ld();
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = have ? __uint_as_float(r[j]) : 0.0f;
+      for (int p = 1; p < S; ++p) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t addr =
+              mapa_shared(smem_u32(&red[(c * 4 + w) * 128 + tid]), static_cast<uint32_t>(p));
+          const float4 f = ld_dsmem_f4(addr);
+          v[4 * w] += f.x;
+          v[4 * w + 1] += f.y;
+          v[4 * w + 2] += f.z;
+          v[4 * w + 3] += f.w;
+        }
+      }
+      const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;
+      switch (a.ep.act) {
+        case kActRelu: epi_col16<kActRelu>(v, m0, n, a.M, a.N, a.ep); break;
+        case kActSilu: epi_col16<kActSilu>(v, m0, n, a.M, a.N, a.ep); break;
+        case kActGeluTanh: epi_col16<kActGeluTanh>(v, m0, n, a.M, a.N, a.ep); break;
+        default: epi_col16<kActIdentity>(v, m0, n, a.M, a.N, a.ep); break;
+      }
+    }
+  }
+  if (S > 1) cluster_sync_all();
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ============================================================ host launchers
+
+namespace {
+
+// cudaFuncSetAttribute once per kernel instantiation and device.
+template <typename K>
+cudaError_t ensure_smem_attr(K kernel, int bytes, std::atomic<uint64_t>& mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) mask.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+template <bool W_KN, bool DUAL>
+cudaError_t run_persistent(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                           const CUtensorMap& tmW2, const PersistArgs& args,
+                           cudaStream_t stream) {
+  static std::atomic<uint64_t> mask{0};
+  auto kernel = gemm_persistent_kernel<W_KN, DUAL>;
+  cudaError_t e = ensure_smem_attr(kernel, kPSmem, mask);
+  if (e != cudaSuccess) return e;
+  kernel<<<p.grid, kPThreads, kPSmem, stream>>>(tmA, tmW, tmW2, args);
+  return cudaGetLastError();
+}
+
+template <int MPAD, bool W_KN>
+cudaError_t run_swap(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                     const SwapArgs& args, cudaStream_t stream) {
+  static std::atomic<uint64_t> mask{0};
+  auto kernel = gemm_swap_kernel<MPAD, W_KN>;
+  cudaError_t e = ensure_smem_attr(kernel, SwapCfg<MPAD>::kSmem, mask);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.n_tiles, p.m_tiles);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = SwapCfg<MPAD>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, args);
+}
+
+template <bool W_KN>
+cudaError_t run_swap_mpad(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                          const SwapArgs& args, cudaStream_t stream) {
+  switch (p.mpad) {
+    case 16: return run_swap<16, W_KN>(p, tmA, tmW, args, stream);
+    case 32: return run_swap<32, W_KN>(p, tmA, tmW, args, stream);
+    case 64: return run_swap<64, W_KN>(p, tmA, tmW, args, stream);
+    case 128: return run_swap<128, W_KN>(p, tmA, tmW, args, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
+                        const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                        const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
+                        cudaStream_t stream) {
+  if (plan.path == kPathPersistent) {
+    PersistArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
+    if (w_kn)
+      return dual ? run_persistent<true, true>(plan, tmA, tmW, tmW2, args, stream)
+                  : run_persistent<true, false>(plan, tmA, tmW, tmW2, args, stream);
+    return dual ? run_persistent<false, true>(plan, tmA, tmW, tmW2, args, stream)
+                : run_persistent<false, false>(plan, tmA, tmW, tmW2, args, stream);
+  }
+  if (plan.path == kPathSwap && !dual) {
+    SwapArgs args{M, N, K, plan.num_kb, plan.splits, ep, ctl};
+    return w_kn ? run_swap_mpad<true>(plan, tmA, tmW, args, stream)
+                : run_swap_mpad<false>(plan, tmA, tmW, args, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gbf

@@ -1,0 +1,88 @@
+// internal.h -- declarations shared by the library's translation units
+// (kernel launchers and the C-ABI layer).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace gbf {
+
+// Pointwise ending of a product: act(alpha*acc + beta*C + bias) + residual.
+struct EpiParams {
+  const __nv_bfloat16* C;         // [M][N] or null
+  const __nv_bfloat16* bias;      // [N] or null
+  const __nv_bfloat16* residual;  // [M][N] or null (may alias out)
+  __nv_bfloat16* out;             // [M][N]
+  float alpha;
+  float beta;
+  int act;
+};
+
+// Per-launch control: the device error word, the wait limit and the
+// test-only timeout injection.
+struct KernelCtl {
+  unsigned* err;
+  unsigned long long timeout_ns;
+  int inject;
+};
+
+// Kernel families (gbf_kernel_path codes).
+enum Path { kPathNone = 0, kPathPersistent = 1, kPathSwap = 2, kPathW4 = 3 };
+
+struct GemmPlan {
+  int path = kPathNone;
+  int mpad = 0;      // swapped kernels: MMA N (padded rows of A per tile)
+  int splits = 1;    // swapped kernels: cluster split-K size
+  int m_tiles = 0;
+  int n_tiles = 0;
+  int num_kb = 0;    // 64-wide K blocks
+  int grid = 0;      // persistent kernel: CTAs
+};
+
+struct DeviceInfo {
+  int sms = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+};
+
+// ---- planning (api.cu) -------------------------------------------------------
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo& dev);
+GemmPlan plan_w4a16(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
+
+// ---- launchers ---------------------------------------------------------------
+// Dense bf16 GEMM with fused ending (gemm_tc.cu).  tmA: activations [M][K];
+// tmW / tmW2: weights (tmW2 = up weights of the dual GEMM).
+cudaError_t launch_gemm(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
+                        const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                        const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
+                        cudaStream_t stream);
+
+// Weight-only int4 GEMM (w4a16.cu).  tmA: activations; tmQ: packed bytes
+// [K][N/2]; tmS: scales [K/G][N].
+cudaError_t launch_w4a16(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmQ,
+                         const CUtensorMap& tmS, const EpiParams& ep, int M, int N, int K,
+                         int group, const KernelCtl& ctl, cudaStream_t stream);
+
+// Pointwise kernels of the unfused compositions (pointwise.cu).  D == null
+// means a zero product (used for K == 0).
+cudaError_t launch_pointwise_epilogue(const __nv_bfloat16* D, const EpiParams& ep, int64_t M,
+                                      int64_t N, int sms, cudaStream_t stream);
+cudaError_t launch_swiglu_pointwise(const __nv_bfloat16* g, const __nv_bfloat16* u,
+                                    const EpiParams& ep, int64_t M, int64_t N, int sms,
+                                    cudaStream_t stream);
+cudaError_t launch_dequant_int4(const uint8_t* Wq, const __nv_bfloat16* scales, int group,
+                                int64_t K, int64_t N, __nv_bfloat16* w, int sms,
+                                cudaStream_t stream);
+
+// Tile geometry shared by the planner and the kernels.
+constexpr int kBM = 128;        // MMA M: rows of TMEM / output tile height
+constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kPersistBN = 256; // persistent kernel: MMA N
+constexpr int kSwapBN = 128;    // swapped kernel: output columns per tile (= MMA M)
+constexpr int kW4BN = 256;      // W4A16 kernel: output columns per tile
+constexpr int kMaxSplits = 8;   // portable cluster size limit
+
+}  // namespace gbf

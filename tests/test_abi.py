@@ -1,0 +1,105 @@
+"""The C-ABI library loads and exports every symbol include/gbfuse.h declares;
+argument validation runs on the host and needs no GPU (no compute call is
+made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tcgen05_tmem_bf16_gb300 as gbf
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbfuse.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = text.split("#define GBF_API")[-1].split("\n", 1)[1]
+    return sorted(set(re.findall(r"^GBF_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tcgen05_tmem_bf16_gb300 import build
+    build.build()
+    return gbf.load()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unfused",
+                 "swiglu_dual_gemm_unfused", "w4a16_gemm_unfused", "gbf_workspace_size",
+                 "gbf_check_device_error", "gbf_status_string"):
+        assert name in syms
+    assert set(syms) == set(gbf.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings_and_version(lib):
+    assert gbf.gbf_status_string(0) == "ok"
+    assert "aligned" in gbf.gbf_status_string(2)
+    assert "bounded wait" in gbf.gbf_status_string(6)
+    assert gbf.gbf_status_string(99) == "unknown status"
+    assert gbf.gbf_version() == 100
+
+
+def test_workspace_sizes(lib):
+    assert gbf.gbf_workspace_size("gemm_epilogue", 4096, 4096, 4096, True) == 0
+    assert gbf.gbf_workspace_size("gemm_epilogue", 3, 8, 8, False) == 256
+    assert gbf.gbf_workspace_size("gemm_epilogue", 4096, 4096, 16, False) == 4096 * 4096 * 2
+    assert gbf.gbf_workspace_size("swiglu", 2048, 14336, 4096, False) == 2 * 2048 * 14336 * 2
+    assert gbf.gbf_workspace_size("w4a16", 16, 28672, 8192, False) == 8192 * 28672 * 2
+
+
+def test_kernel_path_planning(lib):
+    assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096) == ("persistent", 1)
+    path, splits = gbf.gbf_kernel_path("gemm_epilogue", 16, 8192, 8192, "kn")
+    assert path == "swap_splitk" and 1 <= splits <= 8
+    assert gbf.gbf_kernel_path("swiglu", 2048, 14336, 4096)[0] == "persistent"
+    path, splits = gbf.gbf_kernel_path("w4a16", 16, 28672, 8192)
+    assert path == "w4a16" and 1 <= splits <= 8
+    assert gbf.gbf_kernel_path("gemm_epilogue", 0, 8, 8)[0] == "none"
+    assert gbf.gbf_kernel_path("gemm_epilogue", 8, 12, 8)[0] == "rejected"
+    assert gbf.gbf_kernel_path("w4a16", 8, 48, 128)[0] == "rejected"   # N % 32
+
+
+def _bad(status):
+    return status not in (0, 7)  # validation errors come before the device check
+
+
+def test_validation_errors_are_returned_before_any_launch(lib):
+    a = 0x10000  # never dereferenced: every call below fails validation first
+    f = lambda **kw: gbf.gemm_epilogue(**{**dict(A=a, B=a, b_layout=1, C=None, bias=None,
+                                                 residual=None, out=a, M=8, N=8, K=8),
+                                          **kw}, stream=0, raise_on_error=False)
+    assert f(A=None) == 1
+    assert f(out=None) == 1
+    assert f(b_layout=2) == 1
+    assert f(act=4) == 1
+    assert f(M=-1) == 1
+    assert f(N=12) == 3
+    assert f(K=20) == 3
+    assert f(A=a + 8) == 2
+    assert f(bias=a + 2) == 2
+    s = gbf.w4a16_gemm(a, a, a, 100, None, None, None, a, 8, 64, 200, stream=0, raise_on_error=False)
+    assert s == 3  # group size not a multiple of 64
+    s = gbf.w4a16_gemm(a, a, a, 0, None, None, None, a, 8, 64, 128, stream=0, raise_on_error=False)
+    assert s == 1
+    s = gbf.w4a16_gemm(a, a, a, 128, None, None, None, a, 8, 48, 128, stream=0, raise_on_error=False)
+    assert s == 3  # N % 32
+    s = gbf.gemm_epilogue_unfused(a, a, 1, None, None, None, a, 8, 8, 8, workspace=None,
+                                  workspace_bytes=0, stream=0, raise_on_error=False)
+    assert s == 4
+    s = gbf.swiglu_dual_gemm(a, a, None, 1, a, 8, 8, 8, stream=0, raise_on_error=False)
+    assert s == 1
+
+
+def test_timeout_setting_is_clamped(lib):
+    assert gbf.gbf_set_wait_timeout_ns(1) == 0
+    assert gbf.gbf_set_wait_timeout_ns(2_000_000_000) == 0
