@@ -1,0 +1,558 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GEMM + epilogue path on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input: a
+single fused call (TMA staging -> tcgen05 main loop -> fused epilogue ->
+one store).  Default workload: the prefill projection with a bias +
+residual ending, A[4096x4096] * W[4096x4096]^T + bias + residual, bf16 in,
+fp32 accumulate, bf16 out.  Other workloads (--workload) are the gate/up
+SwiGLU GEMM, the W4A16 decode GEMM, the epilogue sweep (sweep-<M>) and the
+tiny case.
+
+Prints ONE JSON line.  ``value`` is whole-job TFLOP/s (FLOPs of every rank's
+steps / max over ranks of the timed region).  Inputs are resident in HBM;
+rotating input sets (>= 2x L2 in total) keep consecutive steps from reading
+each other's data out of L2.  Each launch is bracketed by CUDA events on the
+launching stream, which give the kernel's average duration for the roofline
+fraction.  Extra keys: roofline, cpu_baseline (the fp64 oracle timed on a
+bounded sample on the host cores), e2e (the same metric with host buffers and
+host<->device copies inside the timed region), clocks (nvidia-smi samples taken
+during the timed region), the unfused composition's time and the
+fused-vs-unfused speedup.
+
+--impl reference times the fp64 CPU oracle (the only reference this path
+has) on the same workload, each step a bounded sample of output elements.
+
+Multi-GPU: the path shards with no exchange step, so N GPUs run N
+independent replicas (launched by torchrun); the timed region is bracketed by
+barriers and its maximum over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+epilogue TFLOP/s or GB/s as % of roofline; fused vs unfused speedup"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tcgen05_tmem_bf16_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    capture, if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(seconds: float, units: float, world: int):
+    """(max seconds over ranks, sum of units over ranks)."""
+    if world <= 1:
+        return seconds, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.fh = open(self.path, "w")
+        self.proc = subprocess.Popen([exe, "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits", "-lms", "100"],
+                                     stdout=self.fh, stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return math.nan
+        loaded = [r for r in rows if num(r[4]) >= 50] or rows
+        sm = [num(r[1]) for r in loaded if not math.isnan(num(r[1]))]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in loaded:
+            for name, v in zip(names, r[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]),
+                "power_w_max": max(num(r[3]) for r in loaded),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workloads
+
+class Workload:
+    """Device inputs (several rotating sets), host copies for e2e, and the
+    fused/unfused calls of one workload."""
+
+    def __init__(self, name: str, dev):
+        import numpy as np
+        import torch
+
+        import tcgen05_tmem_bf16_gb300 as gbf
+        import workloads
+        from tcgen05_tmem_bf16_gb300 import roofline
+
+        self.gbf, self.np, self.torch = gbf, np, torch
+        self.name = name
+        if name.startswith("sweep-"):
+            M = int(name.split("-")[1])
+            w = workloads.make("sweep", M=M)
+        else:
+            w = workloads.make(name)
+        self.w = w
+        self.op = w["op"]
+        self.M, self.N, self.K = w["M"], w["N"], w["K"]
+        self.counts = roofline.counts_for(w)
+        host = {}
+        for key in ("A", "B", "C", "bias", "residual", "x", "w_gate", "w_up", "Wq", "scales"):
+            if w.get(key) is not None:
+                host[key] = w[key]
+        self.host_np = host
+        set_bytes = sum(v.nbytes for v in host.values()) + self.M * self.N * 2
+        self.n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes))
+        self.set_bytes = set_bytes
+
+        def up(a):
+            t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+            t = t.to(dev)
+            return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
+
+        self.sets = []
+        for _ in range(self.n_sets):
+            d = {k: up(v) for k, v in host.items()}
+            d["out"] = torch.empty(self.M, self.N, dtype=torch.bfloat16, device=dev)
+            self.sets.append(d)
+        ws = gbf.gbf_workspace_size(
+            {"gemm": "gemm_epilogue", "swiglu": "swiglu", "w4a16": "w4a16"}[self.op],
+            self.M, self.N, self.K, False)
+        self.ws_bytes = ws
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        # pinned host buffers for the end-to-end leg
+        self.pinned = {k: torch.from_numpy(v.copy()).pin_memory() for k, v in host.items()}
+        self.pinned_out = torch.empty(self.M * self.N * 2, dtype=torch.uint8).pin_memory()
+        self.h2d_bytes = sum(v.nbytes for v in host.values())
+        self.d2h_bytes = self.M * self.N * 2
+        self.path, self.splits = gbf.gbf_kernel_path(
+            {"gemm": "gemm_epilogue", "swiglu": "swiglu", "w4a16": "w4a16"}[self.op],
+            self.M, self.N, self.K, w.get("layout", "kn"))
+
+    def describe(self) -> dict:
+        w = self.w
+        d = {"M": self.M, "N": self.N, "K": self.K, "op": self.op}
+        if "layout" in w:
+            d["b_layout"] = w["layout"]
+        if self.op == "w4a16":
+            d["group_size"] = w["group"]
+        d.update(alpha=w["alpha"], beta=w["beta"], act=w["act"])
+        return d
+
+    def fused(self, i: int, stream=None):
+        s = self.sets[i % self.n_sets]
+        w, gbf = self.w, self.gbf
+        if self.op == "gemm":
+            gbf.gemm_epilogue(s["A"], s["B"], w["layout"], s.get("C"), s.get("bias"),
+                              s.get("residual"), s["out"], self.M, self.N, self.K, w["alpha"],
+                              w["beta"], w["act"], stream=stream)
+        elif self.op == "swiglu":
+            gbf.swiglu_dual_gemm(s["x"], s["w_gate"], s["w_up"], w["layout"], s["out"], self.M,
+                                 self.N, self.K, w["alpha"], w["beta"], s.get("C"), w["act"],
+                                 stream=stream)
+        else:
+            gbf.w4a16_gemm(s["A"], s["Wq"], s["scales"], w["group"], s.get("C"), s.get("bias"),
+                           s.get("residual"), s["out"], self.M, self.N, self.K, w["alpha"],
+                           w["beta"], w["act"], stream=stream)
+
+    def unfused(self, i: int, stream=None):
+        s = self.sets[i % self.n_sets]
+        w, gbf = self.w, self.gbf
+        kw = dict(workspace=self.ws, workspace_bytes=self.ws_bytes, stream=stream)
+        if self.op == "gemm":
+            gbf.gemm_epilogue_unfused(s["A"], s["B"], w["layout"], s.get("C"), s.get("bias"),
+                                      s.get("residual"), s["out"], self.M, self.N, self.K,
+                                      w["alpha"], w["beta"], w["act"], **kw)
+        elif self.op == "swiglu":
+            gbf.swiglu_dual_gemm_unfused(s["x"], s["w_gate"], s["w_up"], w["layout"], s["out"],
+                                         self.M, self.N, self.K, w["alpha"], w["beta"],
+                                         s.get("C"), w["act"], **kw)
+        else:
+            gbf.w4a16_gemm_unfused(s["A"], s["Wq"], s["scales"], w["group"], s.get("C"),
+                                   s.get("bias"), s.get("residual"), s["out"], self.M, self.N,
+                                   self.K, w["alpha"], w["beta"], w["act"], **kw)
+
+    def unfused_launches(self) -> int:
+        return 2 if self.op != "swiglu" else 3
+
+    def e2e_step(self, stream):
+        """Host->device copy of the step's inputs, the call, device->host copy
+        of the result, all on `stream`."""
+        s = self.sets[0]
+        for k, v in self.pinned.items():
+            dst = s[k]
+            dst_raw = dst.view(self.torch.int16) if dst.dtype == self.torch.bfloat16 else dst
+            src = v if v.dtype != self.torch.uint16 else v.view(self.torch.int16)
+            dst_raw.copy_(src.view(dst_raw.dtype), non_blocking=True)
+        self.fused(0, stream=stream)
+        self.pinned_out.copy_(s["out"].view(self.torch.uint8).reshape(-1), non_blocking=True)
+
+
+def time_loop(fn, steps: int, stream, per_launch: bool):
+    """Run fn(i) `steps` times on `stream`; returns (region seconds, mean
+    per-launch seconds or None)."""
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    evs = []
+    if per_launch:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+    start.record(stream)
+    for i in range(steps):
+        if per_launch:
+            evs[i][0].record(stream)
+        fn(i)
+        if per_launch:
+            evs[i][1].record(stream)
+    end.record(stream)
+    end.synchronize()
+    region = start.elapsed_time(end) / 1e3
+    per = None
+    if per_launch:
+        per = sum(a.elapsed_time(b) for a, b in evs) / len(evs) / 1e3
+    return region, per
+
+
+# ---------------------------------------------------------------- CPU (oracle) legs
+
+def oracle_elements(w: dict, rows, cols):
+    import oracle
+    op = w["op"]
+    M, N, K = w["M"], w["N"], w["K"]
+    if op == "gemm":
+        return oracle.gemm_epilogue(w["A"], w["B"], w["layout"], w.get("C"), w.get("bias"),
+                                    w.get("residual"), M=M, N=N, K=K, alpha=w["alpha"],
+                                    beta=w["beta"], act=w["act"], rows=rows, cols=cols)
+    if op == "swiglu":
+        return oracle.swiglu(w["x"], w["w_gate"], w["w_up"], w["layout"], w.get("C"), M=M, N=N,
+                             K=K, alpha=w["alpha"], beta=w["beta"], act=w["act"], rows=rows,
+                             cols=cols)
+    return oracle.w4a16(w["A"], w["Wq"], w["scales"], w["group"], w.get("C"), w.get("bias"),
+                        w.get("residual"), M=M, N=N, K=K, alpha=w["alpha"], beta=w["beta"],
+                        act=w["act"], rows=rows, cols=cols)
+
+
+def flops_per_element(w: dict) -> float:
+    return (4.0 if w["op"] == "swiglu" else 2.0) * w["K"]
+
+
+def cpu_baseline(w: dict, seconds: float = 12.0) -> dict:
+    """The oracle as it stands (single-threaded C, fp64) on seeded output
+    elements of the same workload, for about `seconds` of CPU time."""
+    import numpy as np
+    import workloads
+    rows, cols = workloads.sample_indices(w["M"], w["N"], 1 << 20, seed=0xBEEF)
+    done, t0, batch = 0, time.perf_counter(), 64
+    while True:
+        oracle_elements(w, rows[done:done + batch], cols[done:done + batch])
+        done += batch
+        el = time.perf_counter() - t0
+        if el >= seconds or done + batch > rows.size:
+            break
+        batch = min(batch * 2, 4096)
+    tflops = done * flops_per_element(w) / el / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} seeded output elements of the {w['M']}x{w['N']}x{w['K']} "
+                      f"workload ({el:.1f} s, single-threaded fp64 C oracle)"}
+
+
+def run_reference(args, workload_name):
+    """--impl reference: the fp64 CPU oracle on the same workload; each step
+    computes a bounded sample of output elements."""
+    import numpy as np
+    import workloads
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = (workloads.make("sweep", M=int(workload_name.split("-")[1]))
+         if workload_name.startswith("sweep-") else workloads.make(workload_name))
+    rows, cols = workloads.sample_indices(w["M"], w["N"], 1 << 16, seed=0xFACE)
+    t0 = time.perf_counter()
+    oracle_elements(w, rows[:32], cols[:32])
+    per_elem = max((time.perf_counter() - t0) / 32, 1e-7)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    per_step = int(max(1, min(rows.size // 2, budget / per_elem)))
+    pos = 0
+
+    def step():
+        nonlocal pos
+        if pos + per_step > rows.size:
+            pos = 0
+        oracle_elements(w, rows[pos:pos + per_step], cols[pos:pos + per_step])
+        pos += per_step
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    flops = args.steps * per_step * flops_per_element(w)
+    value = flops / el / 1e12
+    sample = (f"{per_step} seeded output elements per step of the {w['M']}x{w['N']}x{w['K']} "
+              f"workload, single-threaded fp64 C oracle")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": workload_name, **{k: w[k] for k in ("M", "N", "K")}},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- main
+
+WORKLOAD_TEXT = {
+    "prefill": "prefill projection A[4096x4096] x W[4096x4096]^T + bias + residual, bf16",
+    "swiglu": "gate/up SwiGLU dual GEMM x[2048x4096], Wg,Wu[14336x4096], bf16",
+    "w4a16": "W4A16 decode GEMM A[16x8192] x int4 W[8192x28672], group 128",
+    "tiny": "tiny fused GEMM 64x256x128, SiLU(0.5AB + C + bias)",
+}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill",
+                    help="prefill | swiglu | w4a16 | tiny | sweep-<M>")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--unfused-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        return run_reference(args, args.workload)
+
+    import torch
+    world, rank, local = dist_env()
+    if args.gpus > 1 and world == 1:
+        print("bench.py --gpus N>1 must be launched by torchrun (one rank per GPU)",
+              file=sys.stderr)
+        return 2
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from __graft_entry__ import build
+    build()
+    import tcgen05_tmem_bf16_gb300 as gbf
+    gbf.load()
+
+    dev = torch.device("cuda", local)
+    wl = Workload(args.workload, dev)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+
+    # warm-up (also checks the launch works)
+    for i in range(args.warmup):
+        wl.fused(i)
+    torch.cuda.synchronize()
+    if gbf.gbf_check_device_error() != 0:
+        raise SystemExit("kernel reported a timeout during warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    region, per_launch = time_loop(wl.fused, args.steps, stream, per_launch=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    max_region, total_flops = aggregate(region, wl.counts.flops * args.steps, world)
+    if gbf.gbf_check_device_error() != 0:
+        raise SystemExit("kernel reported a timeout in the timed region")
+    value = total_flops / max_region / 1e12
+
+    # unfused composition, same workload, same rotation of input sets
+    for i in range(3):
+        wl.unfused(i)
+    torch.cuda.synchronize()
+    un_region, _ = time_loop(wl.unfused, args.unfused_steps, stream, per_launch=False)
+    un_ms = un_region / args.unfused_steps * 1e3
+    fu_ms = max_region / args.steps * 1e3
+
+    # end to end through the public API with host buffers
+    for _ in range(2):
+        wl.e2e_step(stream)
+    torch.cuda.synchronize()
+    e2e_region, _ = time_loop(lambda i: wl.e2e_step(stream), args.e2e_steps, stream,
+                              per_launch=False)
+    e2e_max, e2e_flops = aggregate(e2e_region, wl.counts.flops * args.e2e_steps, world)
+
+    # roofline of the dominant (only) kernel of the step
+    from tcgen05_tmem_bf16_gb300 import roofline as rf
+    bnd = rf.bound(wl.counts, peaks["bf16_tflops"], peaks["hbm_gbs"])
+    long_loop = region > 0.5
+    if bnd == "tensor":
+        achieved = wl.counts.flops / per_launch / 1e12
+        peak = peaks["bf16_tflops_sustained"] if long_loop else peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = wl.counts.fused_bytes / per_launch / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    roof = {"bound": bnd, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+            "peak_source": (f"{peak_src}: " + ("bf16_tflops_sustained (back-to-back loop)"
+                                               if bnd == "tensor" and long_loop else
+                                               ("bf16_tflops (burst)" if bnd == "tensor"
+                                                else "hbm_gbs"))),
+            "kernel": {1: "gemm_persistent_kernel", 2: "gemm_swap_kernel",
+                       3: "w4a16_kernel"}.get({"persistent": 1, "swap_splitk": 2,
+                                               "w4a16": 3}.get(wl.path, 0), wl.path),
+            "splits": wl.splits,
+            "kernel_ms": per_launch * 1e3,
+            "algorithmic_flops": wl.counts.flops, "algorithmic_bytes": wl.counts.fused_bytes,
+            "roofline_ms": rf.roofline_seconds(wl.counts, peaks["bf16_tflops"],
+                                               peaks["hbm_gbs"]) * 1e3}
+    if bnd == "tensor":
+        roof["frac_of_burst_peak"] = achieved / peaks["bf16_tflops"]
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": fu_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
+                   "name": args.workload, **wl.describe(),
+                   "l2": f"{wl.n_sets} rotating input sets of {wl.set_bytes / 2**20:.0f} MiB "
+                         f"(> 2x L2)",
+                   "parallelism": f"replicas x{world}"},
+        "impl": "gbfuse",
+        "roofline": roof,
+        "unfused_ms_per_step": un_ms,
+        "speedup_vs_unfused": un_ms / fu_ms,
+        "e2e": {"value": e2e_flops / e2e_max / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl.w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

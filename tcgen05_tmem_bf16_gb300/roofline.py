@@ -1,0 +1,90 @@
+"""Algorithmic FLOP and byte counts of the fused path and its unfused
+composition, and the roofline time they imply.
+
+FLOPs: 2*M*N*K per product (two products for the gate/up GEMM); the
+epilogue's few operations per output are not counted.  Fusion does not
+change this number ("Kernel fusion" guide, "Check yourself": fusion cuts
+HBM trips and launches, not the FLOP count of the matmul).
+
+Bytes: every tensor crossing HBM exactly once -- inputs read once, the
+output written once -- with no credit or charge for re-reads caused by
+tiling.  Unfused adds the intermediate's write and read-back ("kernel
+fusion" wiki: unfused, the product writes its output and a second kernel
+reads it and writes again), and for the gate/up pair the second read of x
+by the second GEMM.  For W4A16 the weight bytes are the packed int4 bytes
+plus the bf16 scales ("Fusion Thinking", Pattern 3: W_int4 is a quarter of
+the bf16 bytes); its unfused form writes and reads back the bf16 weight.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+BF16 = 2
+
+
+@dataclass
+class Counts:
+    flops: float
+    fused_bytes: float
+    unfused_bytes: float
+
+
+def gemm_counts(M, N, K, has_c=False, has_bias=False, has_res=False) -> Counts:
+    io = M * K * BF16 + K * N * BF16 + M * N * BF16
+    io += (M * N * BF16 if has_c else 0) + (N * BF16 if has_bias else 0)
+    io += M * N * BF16 if has_res else 0
+    return Counts(2.0 * M * N * K, io, io + 2 * M * N * BF16)
+
+
+def swiglu_counts(M, N, K, has_c=False) -> Counts:
+    fused = M * K * BF16 + 2 * N * K * BF16 + M * N * BF16 + (M * N * BF16 if has_c else 0)
+    # unfused: the second GEMM reads x again; g and u are written, then read
+    # back by the pointwise pass.
+    unfused = fused + M * K * BF16 + 2 * (2 * M * N * BF16)
+    return Counts(4.0 * M * N * K, fused, unfused)
+
+
+def swiglu_unfused_pointwise_read_bytes_per_token(N: int) -> int:
+    """Bytes the separate silu(gate)*up pass reads per token (row)."""
+    return 2 * N * BF16
+
+
+def w4a16_counts(M, N, K, group, has_c=False, has_bias=False, has_res=False) -> Counts:
+    wbytes = K * N // 2 + (K // group) * N * BF16
+    io = M * K * BF16 + wbytes + M * N * BF16
+    io += (M * N * BF16 if has_c else 0) + (N * BF16 if has_bias else 0)
+    io += M * N * BF16 if has_res else 0
+    return Counts(2.0 * M * N * K, io, io + 2 * K * N * BF16)
+
+
+def int4_weight_bytes(K, N) -> int:
+    return K * N // 2
+
+
+def bf16_weight_bytes(K, N) -> int:
+    return K * N * BF16
+
+
+def roofline_seconds(c: Counts, peak_tflops: float, peak_gbs: float, fused=True) -> float:
+    b = c.fused_bytes if fused else c.unfused_bytes
+    return max(c.flops / (peak_tflops * 1e12), b / (peak_gbs * 1e9))
+
+
+def bound(c: Counts, peak_tflops: float, peak_gbs: float) -> str:
+    t_tc = c.flops / (peak_tflops * 1e12)
+    t_hbm = c.fused_bytes / (peak_gbs * 1e9)
+    return "tensor" if t_tc >= t_hbm else "hbm"
+
+
+def counts_for(cfg: dict) -> Counts:
+    op = cfg["op"]
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    if op == "gemm":
+        return gemm_counts(M, N, K, cfg.get("has_c", False), cfg.get("has_bias", False),
+                           cfg.get("has_res", False))
+    if op == "swiglu":
+        return swiglu_counts(M, N, K, cfg.get("has_c", False))
+    if op == "w4a16":
+        return w4a16_counts(M, N, K, cfg["group"], cfg.get("has_c", False),
+                            cfg.get("has_bias", False), cfg.get("has_res", False))
+    raise KeyError(op)
