@@ -157,6 +157,28 @@ GBF_API gbf_status_t w4a16_gemm_unfused(const void *A, const uint8_t *Wq, const 
                                 int64_t K, float alpha, float beta, int act, void *workspace,
                                 size_t workspace_bytes, gbf_stream_t stream);
 
+/*
+ * gemm_epilogue_unfused_noalloc -- the gemm_epilogue_unfused result for a
+ *   caller that cannot allocate device memory: code running inside a host
+ *   framework that owns every device allocation, or under a policy that
+ *   forbids new allocations once the process has started, so it has no way
+ *   to hand over a workspace.  The bf16 intermediate lives in a scratch
+ *   array built into the library instead.  The pages have no counterpart to
+ *   this entry point; it exists for such callers only.
+ *   Limit: M*N <= 4194304 elements (an 8 MiB array that every GPU loading
+ *   the library holds until the process exits); larger sizes return
+ *   GBF_ERR_WORKSPACE before anything is launched.  The first call on a
+ *   device looks up the array's device address, so make it before any
+ *   stream capture.  Every call shares the one array: calls whose work
+ *   overlaps on the GPU race on it and must be serialised by the caller.
+ *   Allocates nothing.  Other arguments and results as gemm_epilogue.
+ */
+GBF_API gbf_status_t gemm_epilogue_unfused_noalloc(const void *A, const void *B, int b_layout,
+                                                   const void *C, const void *bias,
+                                                   const void *residual, void *out, int64_t M,
+                                                   int64_t N, int64_t K, float alpha, float beta,
+                                                   int act, gbf_stream_t stream);
+
 /* Workspace bytes an entry point needs (0 for the fused ones).  `op` is a
  * GBF_OP_* id; `fused` selects the fused (1) or unfused (0) entry point. */
 GBF_API size_t gbf_workspace_size(int op, int64_t M, int64_t N, int64_t K, int fused);

@@ -30,7 +30,8 @@ PATH = {0: "none", 1: "persistent", 2: "swap_splitk", 3: "w4a16"}
 EXPORTS = ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unfused",
            "swiglu_dual_gemm_unfused", "w4a16_gemm_unfused", "gbf_workspace_size",
            "gbf_check_device_error", "gbf_status_string", "gbf_set_wait_timeout_ns",
-           "gbf_debug_inject_timeout", "gbf_kernel_path", "gbf_version")
+           "gbf_debug_inject_timeout", "gbf_kernel_path", "gbf_version",
+           "gemm_epilogue_unfused_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,9 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = I
+        lib.gemm_epilogue_unfused_noalloc.argtypes = [V, V, I, V, V, V, V, I64, I64, I64, F, F,
+                                                      I, V]
+        lib.gemm_epilogue_unfused_noalloc.restype = I
         lib.gbf_workspace_size.argtypes = [I, I64, I64, I64, I]
         lib.gbf_workspace_size.restype = SZ
         lib.gbf_check_device_error.argtypes = [V]
@@ -132,6 +136,17 @@ def gemm_epilogue_unfused(A, B, b_layout, C, bias, residual, out, M, N, K, alpha
                                       _code(act, ACT), _p(workspace), workspace_bytes,
                                       _s(stream))
     return _check(st, "gemm_epilogue_unfused", raise_on_error)
+
+
+def gemm_epilogue_unfused_noalloc(A, B, b_layout, C, bias, residual, out, M, N, K, alpha=1.0,
+                                  beta=0.0, act="identity", stream=None, raise_on_error=True):
+    """gemm_epilogue_unfused for callers that cannot allocate device memory:
+    the intermediate lives in the library's built-in scratch array
+    (M*N <= 4194304); no workspace argument."""
+    st = load().gemm_epilogue_unfused_noalloc(_p(A), _p(B), _code(b_layout, LAYOUT), _p(C),
+                                              _p(bias), _p(residual), _p(out), M, N, K, alpha,
+                                              beta, _code(act, ACT), _s(stream))
+    return _check(st, "gemm_epilogue_unfused_noalloc", raise_on_error)
 
 
 def swiglu_dual_gemm(x, w_gate, w_up, w_layout, h, M, N, K, alpha=1.0, beta=0.0, C=None,
