@@ -49,6 +49,13 @@ METRIC = "fused GEMM+epilogue TFLOP/s or GB/s as % of roofline; fused vs unfused
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
 
+WORKLOAD_TEXT = {
+    "prefill": "prefill projection A[4096x4096] x W[4096x4096]^T + bias + residual, bf16",
+    "swiglu": "gate/up SwiGLU dual GEMM x[2048x4096], Wg,Wu[14336x4096], bf16",
+    "w4a16": "W4A16 decode GEMM A[16x8192] x int4 W[8192x28672], group 128",
+    "tiny": "tiny fused GEMM 64x256x128, SiLU(0.5AB + C + bias)",
+}
+
 
 # ---------------------------------------------------------------- helpers
 
@@ -113,7 +120,7 @@ def barrier(world: int):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 100 ms while running."""
+    """nvidia-smi clock/throttle samples every 50 ms while running."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
               "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -132,7 +139,7 @@ class ClockSampler:
         os.close(fd)
         self.fh = open(self.path, "w")
         self.proc = subprocess.Popen([exe, "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                      "--format=csv,noheader,nounits", "-lms", "100"],
+                                      "--format=csv,noheader,nounits", "-lms", "50"],
                                      stdout=self.fh, stderr=subprocess.DEVNULL)
         time.sleep(0.3)
 
@@ -177,6 +184,21 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workloads
+
+def describe(w: dict) -> dict:
+    d = {"M": w["M"], "N": w["N"], "K": w["K"], "op": w["op"]}
+    if "layout" in w:
+        d["b_layout"] = w["layout"]
+    if w["op"] == "w4a16":
+        d["group_size"] = w["group"]
+    d.update(alpha=w["alpha"], beta=w["beta"], act=w["act"])
+    return d
+
+
+def config_of(name: str, w: dict, world: int) -> dict:
+    return {"workload": WORKLOAD_TEXT.get(name, name), "name": name, **describe(w),
+            "parallelism": f"replicas x{world}"}
+
 
 class Workload:
     """Device inputs (several rotating sets), host copies for e2e, and the
@@ -235,14 +257,7 @@ class Workload:
             self.M, self.N, self.K, w.get("layout", "kn"))
 
     def describe(self) -> dict:
-        w = self.w
-        d = {"M": self.M, "N": self.N, "K": self.K, "op": self.op}
-        if "layout" in w:
-            d["b_layout"] = w["layout"]
-        if self.op == "w4a16":
-            d["group_size"] = w["group"]
-        d.update(alpha=w["alpha"], beta=w["beta"], act=w["act"])
-        return d
+        return describe(self.w)
 
     def fused(self, i: int, stream=None):
         s = self.sets[i % self.n_sets]
@@ -401,7 +416,7 @@ def run_reference(args, workload_name):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": workload_name, **{k: w[k] for k in ("M", "N", "K")}},
+            "config": config_of(workload_name, w, max(1, args.gpus)),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -412,18 +427,13 @@ def run_reference(args, workload_name):
 
 # ---------------------------------------------------------------- main
 
-WORKLOAD_TEXT = {
-    "prefill": "prefill projection A[4096x4096] x W[4096x4096]^T + bias + residual, bf16",
-    "swiglu": "gate/up SwiGLU dual GEMM x[2048x4096], Wg,Wu[14336x4096], bf16",
-    "w4a16": "W4A16 decode GEMM A[16x8192] x int4 W[8192x28672], group 128",
-    "tiny": "tiny fused GEMM 64x256x128, SiLU(0.5AB + C + bias)",
-}
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 1.5 s of timed work)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill",
@@ -437,6 +447,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
 
     if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 20
         return run_reference(args, args.workload)
 
     import torch
@@ -464,6 +476,14 @@ def main(argv=None):
     for i in range(args.warmup):
         wl.fused(i)
     torch.cuda.synchronize()
+    if args.steps is None:
+        t_cal, _ = time_loop(wl.fused, 20, stream, per_launch=False)
+        args.steps = int(min(50000, max(200, 1.5 / max(t_cal / 20, 1e-6))))
+        if world > 1:
+            import torch.distributed as dist
+            k = torch.tensor([args.steps], dtype=torch.int64, device=dev)
+            dist.all_reduce(k, op=dist.ReduceOp.MIN)
+            args.steps = int(k.item())
     if gbf.gbf_check_device_error() != 0:
         raise SystemExit("kernel reported a timeout during warm-up")
 
@@ -530,11 +550,9 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": fu_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
-                   "name": args.workload, **wl.describe(),
+        "config": {**config_of(args.workload, wl.w, world),
                    "l2": f"{wl.n_sets} rotating input sets of {wl.set_bytes / 2**20:.0f} MiB "
-                         f"(> 2x L2)",
-                   "parallelism": f"replicas x{world}"},
+                         f"(> 2x L2)"},
         "impl": "gbfuse",
         "roofline": roof,
         "unfused_ms_per_step": un_ms,

@@ -37,8 +37,34 @@ constexpr int kUK = 16;  // K per tcgen05.mma, kind::f16
 
 // ============================================================ shared pieces
 
+// Round a pointer into dynamic shared memory up to 1024 bytes with pointer
+// arithmetic on the shared array itself, so the compiler keeps the shared
+// address space (ld/st.shared instead of generic accesses).
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
+// Operands of the ending for 32 consecutive columns of one row, loaded
+// before the accumulator is read from TMEM so that their latency overlaps.
+struct RowLoads {
+  uint4 c[4];
+  uint4 b[4];
+  uint4 r[4];
+};
+
+__device__ __forceinline__ void epi_row_prefetch(RowLoads& L, int64_t row, int col0, int M,
+                                                 int N, const EpiParams& e) {
+  const bool rok = row < M;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const int col = col0 + v * 8;
+    const bool ok = rok && col < N;
+    const int64_t off = row * N + col;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    L.c[v] = (ok && e.C) ? ldg_u4(e.C + off) : z;
+    L.b[v] = (ok && e.bias) ? ldg_u4(e.bias + col) : z;
+    L.r[v] = (ok && e.residual) ? ld_u4(e.residual + off) : z;  // may alias out
+  }
 }
 
 // Epilogue of 32 consecutive output columns of one row (persistent kernel).
@@ -46,7 +72,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // product and the result is act(alpha*g) * (alpha*u) + beta*C.
 template <int ACT, bool DUAL>
 __device__ __forceinline__ void epi_row32(const uint32_t (&acc)[32], const uint32_t (&up)[32],
-                                          int64_t row, int col0, int N, const EpiParams& e) {
+                                          const RowLoads& L, int64_t row, int col0, int N,
+                                          const EpiParams& e) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const int col = col0 + v * 8;
@@ -60,33 +87,20 @@ __device__ __forceinline__ void epi_row32(const uint32_t (&acc)[32], const uint3
                (e.alpha * __uint_as_float(up[v * 8 + i]));
       if (e.C) {
         float c[8];
-        unpack8(ldg_u4(e.C + off), c);
+        unpack8(L.c[v], c);
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] = fmaf(e.beta, c[i], x[i]);
       }
     } else {
+      float c[8], b[8], r[8];
+      unpack8(L.c[v], c);
+      unpack8(L.b[v], b);
+      unpack8(L.r[v], r);
+      const float beta = e.C ? e.beta : 0.0f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = e.alpha * __uint_as_float(acc[v * 8 + i]);
-      if (e.C) {
-        float c[8];
-        unpack8(ldg_u4(e.C + off), c);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = fmaf(e.beta, c[i], x[i]);
-      }
-      if (e.bias) {
-        float b[8];
-        unpack8(ldg_u4(e.bias + col), b);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] += b[i];
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = act_apply<ACT>(x[i]);
-      if (e.residual) {
-        float r[8];
-        unpack8(ld_u4(e.residual + off), r);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] += r[i];
-      }
+      for (int i = 0; i < 8; ++i)
+        x[i] = act_apply<ACT>(fmaf(beta, c[i], e.alpha * __uint_as_float(acc[v * 8 + i])) + b[i]) +
+               r[i];
     }
     st_u4(e.out + off, pack8(x));
   }
@@ -98,7 +112,7 @@ constexpr int kPStages = 4;
 constexpr int kPABytes = kBM * kBK * 2;             // 16 KB
 constexpr int kPBBytes = kPersistBN * kBK * 2;      // 32 KB
 constexpr int kPStageBytes = kPABytes + kPBBytes;   // 48 KB
-constexpr int kPThreads = 256;
+constexpr int kPThreads = 384;  // warps 0-3 roles, warps 4-11 epilogue (two warpgroups)
 constexpr int kPSmem = 1024 + kPStages * kPStageBytes + 256;
 constexpr int kPGroupM = 16;                        // tile raster: 16 M-tiles per group
 
@@ -145,7 +159,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], 8);  // one arrive per epilogue warp
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -265,37 +279,48 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
+    // Warps 4-7 and 8-11 read the same TMEM lanes (warp % 4 selects the lane
+    // quarter); the first warpgroup takes the left half of the tile's
+    // columns, the second the right half.
     const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
+    constexpr int kChunks = (DUAL ? 128 : 256) / 32;
+    constexpr int kMine = kChunks / 2;
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
       int mb, nb;
       tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
       const int buf = local & 1;
       const uint32_t aph = (local >> 1) & 1;
+      const int64_t row = static_cast<int64_t>(mb) * kBM + q * 32 + lane;
+      RowLoads L;
+      epi_row_prefetch(L, row, nb * out_bn + half * kMine * 32, a.M, a.N, a.ep);
       if (!wait_bar(&tfull[buf], aph, ctl, kSiteEpiAccFull)) break;
       tc_fence_after();
-      const int64_t row = static_cast<int64_t>(mb) * kBM + q * 32 + lane;
       const uint32_t tb = tmem_base + buf * 256 + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < out_bn / 32; ++c) {
+      for (int cc = 0; cc < kMine; ++cc) {
+        const int c = half * kMine + cc;
+        const int col0 = nb * out_bn + c * 32;
         uint32_t acc[32], up[32];
         tmem_ld32(tb + c * 32, acc);
         if constexpr (DUAL) tmem_ld32(tb + 128 + c * 32, up);
         tmem_wait_ld();
-        if (c == out_bn / 32 - 1) {
+        if (cc == kMine - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[buf]);
         }
+        const RowLoads cur = L;
+        if (cc + 1 < kMine) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep);
         if (row < a.M) {
-          const int col0 = nb * out_bn + c * 32;
           switch (a.ep.act) {
-            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, row, col0, a.N, a.ep); break;
-            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, row, col0, a.N, a.ep); break;
+            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
+            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
             case kActGeluTanh:
-              epi_row32<kActGeluTanh, DUAL>(acc, up, row, col0, a.N, a.ep);
+              epi_row32<kActGeluTanh, DUAL>(acc, up, cur, row, col0, a.N, a.ep);
               break;
-            default: epi_row32<kActIdentity, DUAL>(acc, up, row, col0, a.N, a.ep); break;
+            default: epi_row32<kActIdentity, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
           }
         }
       }
@@ -331,22 +356,29 @@ struct SwapArgs {
   KernelCtl ctl;
 };
 
-// Epilogue of one output column n for 16 consecutive rows m0..m0+15.
+// Epilogue of one output column n for 16 consecutive rows m0..m0+15.  All
+// operand loads are issued first (independent, so they overlap), then the
+// math and the stores.
 template <int ACT>
 __device__ __forceinline__ void epi_col16(const float (&v)[16], int64_t m0, int n, int M,
                                           int N, const EpiParams& e) {
   if (n >= N) return;
   const float b = e.bias ? __bfloat162float(e.bias[n]) : 0.0f;
+  float c[16], r[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int64_t m = m0 + j;
-    if (m >= M) break;
+    const bool ok = m < M;
     const int64_t off = m * N + n;
-    float x = e.alpha * v[j];
-    if (e.C) x = fmaf(e.beta, __bfloat162float(e.C[off]), x);
-    x = act_apply<ACT>(x + b);
-    if (e.residual) x += __bfloat162float(e.residual[off]);
-    e.out[off] = __float2bfloat16_rn(x);
+    c[j] = (ok && e.C) ? __bfloat162float(e.C[off]) : 0.0f;
+    r[j] = (ok && e.residual) ? __bfloat162float(e.residual[off]) : 0.0f;
+  }
+  const float beta = e.C ? e.beta : 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int64_t m = m0 + j;
+    if (m < M)
+      e.out[m * N + n] = __float2bfloat16_rn(act_apply<ACT>(fmaf(beta, c[j], e.alpha * v[j]) + b) + r[j]);
   }
 }
 
@@ -460,18 +492,24 @@ __global__ void __launch_bounds__(256, 2)
   }
 
   // ---- epilogue warps: partial sums, cluster reduction, ending
+  // With split-K every rank parks its fp32 partial in its own shared memory;
+  // after the cluster barrier the 16-row chunks of the output are shared out
+  // among the ranks (chunk c goes to rank c % S), and each chunk is summed
+  // over ranks 0..S-1 in that order (deterministic) through distributed
+  // shared memory.
   const bool epi = warp >= 4;
   const int q = warp & 3;
   const int tid = threadIdx.x - 128;  // 0..127 for the epilogue warps = TMEM lane
   const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   float4* red = reinterpret_cast<float4*>(stages);
+  constexpr int kChunks = MPAD / 16;
   bool have = false;
   if (epi) {
     have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
     tc_fence_after();
-    if (S > 1 && rank != 0) {
+    if (S > 1) {
 #pragma unroll 1
-      for (int c = 0; c < MPAD / 16; ++c) {
+      for (int c = 0; c < kChunks; ++c) {
         uint32_t r[16];
         tmem_ld16(tb + c * 16, r);
         tmem_wait_ld();
@@ -484,26 +522,35 @@ __global__ void __launch_bounds__(256, 2)
     }
   }
   if (S > 1) cluster_sync_all();
-  if (epi && rank == 0) {
+  if (epi) {
     const int n = nb * kSwapBN + tid;
 #pragma unroll 1
-    for (int c = 0; c < MPAD / 16; ++c) {
-      uint32_t r[16];
-      tmem_ld16(tb + c * 16, r);
-      tmem_wait_ld();
+    for (int c = static_cast<int>(rank); c < kChunks; c += S) {
       float v[16];
+      if (S == 1) {
+        uint32_t r[16];
+        tmem_ld16(tb + c * 16, r);
+        tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = have ? __uint_as_float(r[j]) : 0.0f;
-      for (int p = 1; p < S; ++p) {
+        for (int j = 0; j < 16; ++j) v[j] = have ? __uint_as_float(r[j]) : 0.0f;
+      } else {
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t addr =
-              mapa_shared(smem_u32(&red[(c * 4 + w) * 128 + tid]), static_cast<uint32_t>(p));
-          const float4 f = ld_dsmem_f4(addr);
-          v[4 * w] += f.x;
-          v[4 * w + 1] += f.y;
-          v[4 * w + 2] += f.z;
-          v[4 * w + 3] += f.w;
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+        for (int p = 0; p < S; ++p) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            float4 f;
+            if (p == static_cast<int>(rank)) {
+              f = red[(c * 4 + w) * 128 + tid];
+            } else {
+              f = ld_dsmem_f4(mapa_shared(smem_u32(&red[(c * 4 + w) * 128 + tid]),
+                                          static_cast<uint32_t>(p)));
+            }
+            v[4 * w] += f.x;
+            v[4 * w + 1] += f.y;
+            v[4 * w + 2] += f.z;
+            v[4 * w + 3] += f.w;
+          }
         }
       }
       const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;

@@ -75,7 +75,8 @@ __device__ __forceinline__ __nv_bfloat162 bits_bf2(uint32_t u) {
   return *reinterpret_cast<__nv_bfloat162*>(&u);
 }
 
-// Epilogue of output columns (n, n+1) for 16 rows m0..m0+15.
+// Epilogue of output columns (n, n+1) for 16 rows m0..m0+15: operand loads
+// first (independent, overlapping), then math and bf16x2 stores.
 template <int ACT>
 __device__ __forceinline__ void epi_pair16(const float (&ve)[16], const float (&vo)[16],
                                            int64_t m0, int n, int M, int N,
@@ -87,25 +88,23 @@ __device__ __forceinline__ void epi_pair16(const float (&ve)[16], const float (&
     b0 = bf16lo(b);
     b1 = bf16hi(b);
   }
+  uint32_t c[16], r[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int64_t m = m0 + j;
+    const bool ok = m < M;
+    const int64_t off = m * N + n;
+    c[j] = (ok && e.C) ? *reinterpret_cast<const uint32_t*>(e.C + off) : 0u;
+    r[j] = (ok && e.residual) ? *reinterpret_cast<const uint32_t*>(e.residual + off) : 0u;
+  }
+  const float beta = e.C ? e.beta : 0.0f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int64_t m = m0 + j;
     if (m >= M) break;
-    const int64_t off = m * N + n;
-    float x0 = e.alpha * ve[j], x1 = e.alpha * vo[j];
-    if (e.C) {
-      const uint32_t c = *reinterpret_cast<const uint32_t*>(e.C + off);
-      x0 = fmaf(e.beta, bf16lo(c), x0);
-      x1 = fmaf(e.beta, bf16hi(c), x1);
-    }
-    x0 = act_apply<ACT>(x0 + b0);
-    x1 = act_apply<ACT>(x1 + b1);
-    if (e.residual) {
-      const uint32_t r = *reinterpret_cast<const uint32_t*>(e.residual + off);
-      x0 += bf16lo(r);
-      x1 += bf16hi(r);
-    }
-    *reinterpret_cast<uint32_t*>(e.out + off) = pack_bf16x2(x0, x1);
+    const float x0 = act_apply<ACT>(fmaf(beta, bf16lo(c[j]), e.alpha * ve[j]) + b0) + bf16lo(r[j]);
+    const float x1 = act_apply<ACT>(fmaf(beta, bf16hi(c[j]), e.alpha * vo[j]) + b1) + bf16hi(r[j]);
+    *reinterpret_cast<uint32_t*>(e.out + m * N + n) = pack_bf16x2(x0, x1);
   }
 }
 
@@ -115,8 +114,9 @@ __global__ void __launch_bounds__(kW4Threads, 2)
                  const __grid_constant__ CUtensorMap tmS, const W4Args a, int group) {
   using Cfg = W4Cfg<MPAD>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte alignment by pointer arithmetic on the shared array (keeps the
+  // shared address space for the compiler).
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kStages * Cfg::kStageBytes);
   uint64_t* empty = full + Cfg::kStages;
@@ -278,7 +278,10 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     }
   }
 
-  // ---- epilogue (warps 4-7): cluster reduction of the partial sums, ending
+  // ---- epilogue (warps 4-7): cluster reduction of the partial sums, ending.
+  // Every rank parks its partial in its own shared memory; 16-row chunks are
+  // shared out among the ranks (chunk c to rank c % S) and summed over ranks
+  // 0..S-1 in order through distributed shared memory.
   const bool epi = warp >= 4;
   const int q = warp & 3;
   const int tid = threadIdx.x - 128;
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   if (epi) {
     have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
     tc_fence_after();
-    if (S > 1 && rank != 0) {
+    if (S > 1) {
 #pragma unroll 1
       for (int c = 0; c < 2 * kChunks; ++c) {
         const uint32_t col = (c < kChunks ? Cfg::kColDE : Cfg::kColDO) + (c % kChunks) * 16;
@@ -305,29 +308,40 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     }
   }
   if (S > 1) cluster_sync_all();
-  if (epi && rank == 0) {
+  if (epi) {
     const int n = nb * kW4BN + 2 * tid;
 #pragma unroll 1
-    for (int c = 0; c < kChunks; ++c) {
-      uint32_t re[16], ro[16];
-      tmem_ld16(tb + Cfg::kColDE + c * 16, re);
-      tmem_ld16(tb + Cfg::kColDO + c * 16, ro);
-      tmem_wait_ld();
+    for (int c = static_cast<int>(rank); c < kChunks; c += S) {
       float ve[16], vo[16];
+      if (S == 1) {
+        uint32_t re[16], ro[16];
+        tmem_ld16(tb + Cfg::kColDE + c * 16, re);
+        tmem_ld16(tb + Cfg::kColDO + c * 16, ro);
+        tmem_wait_ld();
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        ve[jj] = have ? __uint_as_float(re[jj]) : 0.0f;
-        vo[jj] = have ? __uint_as_float(ro[jj]) : 0.0f;
-      }
-      for (int p = 1; p < S; ++p) {
+        for (int jj = 0; jj < 16; ++jj) {
+          ve[jj] = have ? __uint_as_float(re[jj]) : 0.0f;
+          vo[jj] = have ? __uint_as_float(ro[jj]) : 0.0f;
+        }
+      } else {
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float4 fe = ld_dsmem_f4(mapa_shared(
-              smem_u32(&red[(c * 4 + w) * 128 + tid]), static_cast<uint32_t>(p)));
-          const float4 fo = ld_dsmem_f4(mapa_shared(
-              smem_u32(&red[((kChunks + c) * 4 + w) * 128 + tid]), static_cast<uint32_t>(p)));
-          ve[4 * w] += fe.x; ve[4 * w + 1] += fe.y; ve[4 * w + 2] += fe.z; ve[4 * w + 3] += fe.w;
-          vo[4 * w] += fo.x; vo[4 * w + 1] += fo.y; vo[4 * w + 2] += fo.z; vo[4 * w + 3] += fo.w;
+        for (int jj = 0; jj < 16; ++jj) ve[jj] = vo[jj] = 0.0f;
+        for (int p = 0; p < S; ++p) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            float4 fe, fo;
+            float4* pe = &red[(c * 4 + w) * 128 + tid];
+            float4* po = &red[((kChunks + c) * 4 + w) * 128 + tid];
+            if (p == static_cast<int>(rank)) {
+              fe = *pe;
+              fo = *po;
+            } else {
+              fe = ld_dsmem_f4(mapa_shared(smem_u32(pe), static_cast<uint32_t>(p)));
+              fo = ld_dsmem_f4(mapa_shared(smem_u32(po), static_cast<uint32_t>(p)));
+            }
+            ve[4 * w] += fe.x; ve[4 * w + 1] += fe.y; ve[4 * w + 2] += fe.z; ve[4 * w + 3] += fe.w;
+            vo[4 * w] += fo.x; vo[4 * w + 1] += fo.y; vo[4 * w + 2] += fo.z; vo[4 * w + 3] += fo.w;
+          }
         }
       }
       const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;
