@@ -534,9 +534,8 @@ def main(argv=None):
                                                if bnd == "tensor" and long_loop else
                                                ("bf16_tflops (burst)" if bnd == "tensor"
                                                 else "hbm_gbs"))),
-            "kernel": {1: "gemm_persistent_kernel", 2: "gemm_swap_kernel",
-                       3: "w4a16_kernel"}.get({"persistent": 1, "swap_splitk": 2,
-                                               "w4a16": 3}.get(wl.path, 0), wl.path),
+            "kernel": {"persistent": "gemm_persistent_kernel", "swap_splitk": "gemm_swap_kernel",
+                       "w4a16": "w4a16_kernel", "pair": "gemm_pair_kernel"}.get(wl.path, wl.path),
             "splits": wl.splits,
             "kernel_ms": per_launch * 1e3,
             "algorithmic_flops": wl.counts.flops, "algorithmic_bytes": wl.counts.fused_bytes,

@@ -204,6 +204,7 @@ GBF_API gbf_status_t gbf_debug_inject_timeout(int on);
 /* Which kernel family a call with these arguments runs (for tests and the
  * benchmark's roofline attribution): 1 = persistent 128x256-tile kernel,
  * 2 = small-M swapped kernel with cluster split-K, 3 = W4A16 kernel,
+ * 4 = persistent 256x256-tile kernel on CTA pairs (large M),
  * 0 = no launch (empty output), -1 = the arguments would be rejected.
  * `*splits` (may be NULL) receives the split-K cluster size. */
 GBF_API int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int *splits);

@@ -25,7 +25,7 @@ OP = {"gemm_epilogue": 0, "swiglu": 1, "w4a16": 2}
 STATUS = {0: "GBF_OK", 1: "GBF_ERR_INVALID_ARG", 2: "GBF_ERR_MISALIGNED",
           3: "GBF_ERR_UNSUPPORTED_SHAPE", 4: "GBF_ERR_WORKSPACE", 5: "GBF_ERR_CUDA",
           6: "GBF_ERR_TIMEOUT", 7: "GBF_ERR_NO_DEVICE"}
-PATH = {0: "none", 1: "persistent", 2: "swap_splitk", 3: "w4a16"}
+PATH = {0: "none", 1: "persistent", 2: "swap_splitk", 3: "w4a16", 4: "pair"}
 
 EXPORTS = ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unfused",
            "swiglu_dual_gemm_unfused", "w4a16_gemm_unfused", "gbf_workspace_size",

@@ -55,6 +55,8 @@ gbf_status_t current_device(const DeviceInfo** info, unsigned** err) {
       d.err = static_cast<unsigned*>(p);
     }
     d.info.sms = sms;
+    if (e == cudaSuccess && major == 10 && minor == 3) d.info.pairs = max_active_pairs();
+    if (d.info.pairs <= 0) d.info.pairs = sms / 2;
     d.info.cc_major = major;
     d.info.cc_minor = minor;
     d.status = e;
@@ -161,10 +163,11 @@ gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, 
   const bool kn = layout == GBF_B_KN;
   CUtensorMap tmA, tmW, tmW2;
   const uint32_t a_rows = plan.path == kPathSwap ? plan.mpad : kBM;
+  const bool pair = plan.path == kPathPair;
   if (!tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, kBK, a_rows,
                CU_TENSOR_MAP_SWIZZLE_128B))
     return GBF_ERR_CUDA;
-  uint32_t w_rows = plan.path == kPathSwap ? kSwapBN : (dual ? 128 : kPersistBN);
+  uint32_t w_rows = (plan.path == kPathSwap || pair) ? 128 : (dual ? 128 : kPersistBN);
   const void* ws[2] = {W, dual ? W2 : W};
   CUtensorMap* maps[2] = {&tmW, &tmW2};
   for (int i = 0; i < 2; ++i) {
@@ -174,6 +177,10 @@ gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, 
                            w_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return GBF_ERR_CUDA;
   }
+  if (pair)
+    return cuda_status(launch_gemm_pair(plan, kn, dual, tmA, tmW, tmW2, ep, static_cast<int>(M),
+                                        static_cast<int>(N), static_cast<int>(K), make_ctl(err),
+                                        stream));
   return cuda_status(launch_gemm(plan, kn, dual, tmA, tmW, tmW2, ep, static_cast<int>(M),
                                  static_cast<int>(N), static_cast<int>(K), make_ctl(err),
                                  stream));
@@ -190,7 +197,7 @@ gbf_status_t run_w4(const void* A, const uint8_t* Wq, const void* scales, int gr
                CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tmap_2d(&tmQ, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, N / 2, K, N / 2, kW4BN / 2, kBK,
                CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !tmap_2d(&tmS, scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, K / group, N * 2, kW4BN, 1,
+      !tmap_2d(&tmS, scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, K / group, N * 2, 256, 1,
                CU_TENSOR_MAP_SWIZZLE_NONE))
     return GBF_ERR_CUDA;
   return cuda_status(launch_w4a16(plan, tmA, tmQ, tmS, ep, static_cast<int>(M),
@@ -218,6 +225,11 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo&
     p.m_tiles = 1;
     p.n_tiles = ceil_div(N, kSwapBN);
     p.splits = choose_splits(p.n_tiles, p.num_kb, dev);
+  } else if (M >= kPairMinM && dev.pairs > 0) {
+    p.path = kPathPair;
+    p.m_tiles = ceil_div(M, 2 * kBM);
+    p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
+    p.grid = 2 * std::min(p.m_tiles * p.n_tiles, dev.pairs);
   } else {
     p.path = kPathPersistent;
     p.m_tiles = ceil_div(M, kBM);
@@ -232,7 +244,7 @@ GemmPlan plan_w4a16(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
   if (M == 0 || N == 0 || K == 0) return p;
   p.path = kPathW4;
   p.num_kb = ceil_div(K, kBK);
-  p.mpad = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+  p.mpad = M <= 16 ? 16 : 32;
   p.m_tiles = ceil_div(M, p.mpad);
   p.n_tiles = ceil_div(N, kW4BN);
   p.splits = choose_splits(p.n_tiles * p.m_tiles, p.num_kb, dev);
@@ -435,8 +447,12 @@ int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int* 
   DeviceInfo dev;
   const DeviceInfo* d = nullptr;
   unsigned* err = nullptr;
-  if (current_device(&d, &err) == GBF_OK) dev = *d;
-  else dev.sms = 152;
+  if (current_device(&d, &err) == GBF_OK) {
+    dev = *d;
+  } else {
+    dev.sms = 152;
+    dev.pairs = 76;
+  }
   GemmPlan p;
   switch (op) {
     case GBF_OP_GEMM_EPILOGUE:

@@ -40,13 +40,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const W
                                          unsigned site, bool honor_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (true) {
+  // The clock and the abort flag are checked every 64 polls only, so that a
+  // waiting warp spends its issue slots on try_wait (which suspends the warp
+  // for a while) rather than on bookkeeping.
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (honor_abort && *ctl.abort) return false;
-    if (globaltimer_ns() - t0 > ctl.timeout_ns) {
-      atomicCAS(ctl.err, 0u, kDevErrTimeout | (site << 8));
-      *ctl.abort = 1;
-      return false;
+    if ((i & 63u) == 0) {
+      if (honor_abort && *ctl.abort) return false;
+      if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+        atomicCAS(ctl.err, 0u, kDevErrTimeout | (site << 8));
+        *ctl.abort = 1;
+        return false;
+      }
     }
   }
 }

@@ -1,0 +1,327 @@
+// gemm_pair.cu -- the persistent GEMM + fused ending on CTA pairs
+// (tcgen05.mma.cta_group::2), for large M.
+//
+// Same ending and same results as gemm_persistent_kernel ("Fusion and
+// Epilogues", epilogue-fusion bullet; "Fusion Thinking", Pattern 2 level 2 for
+// the gate/up variant), computed on 256 x 256 tiles by two CTAs of a cluster
+// running on two SMs:
+//   * each CTA loads its own 128 rows of A and its own half (128 rows of the
+//     N dimension) of the B tile into its shared memory -- for the gate/up
+//     GEMM the even CTA loads the gate rows and the odd CTA the up rows, so
+//     the accumulator's columns 0-127 are the gate product and 128-255 the
+//     up product, exactly as in the single-CTA kernel;
+//   * the even CTA issues one tcgen05.mma.cta_group::2 (M=256, N=256, K=16)
+//     per step, which reads both CTAs' shared memory and writes rows 0-127 of
+//     the accumulator into its own tensor memory and rows 128-255 into the
+//     peer's;
+//   * both CTAs' TMA loads complete on the even CTA's "full" barrier, and the
+//     even CTA's commits arrive on both CTAs' "empty" and "accumulator full"
+//     barriers (multicast); the odd CTA's epilogue warps report a drained
+//     accumulator on the even CTA's barrier.
+// Per SM this halves the shared-memory fill of the B operand compared with a
+// 128 x 256 tile on one SM (32 KB instead of 48 KB per 64-deep K step for the
+// same number of MMA cycles), which is what limits the single-CTA kernel.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gbf {
+
+constexpr int kQStages = 6;
+constexpr int kQABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
+constexpr int kQBBytes = 128 * kBK * 2;        // 16 KB: this CTA's half of the B tile
+constexpr int kQStageBytes = kQABytes + kQBBytes;
+constexpr int kQThreads = 384;                 // warps 0-3 roles, 4-11 epilogue
+constexpr int kQSmem = 1024 + kQStages * kQStageBytes + 256;
+constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
+
+struct PairArgs {
+  int M, N, K;
+  int m_tiles, n_tiles, num_kb;
+  EpiParams ep;
+  KernelCtl ctl;
+};
+
+// Let in-flight copies land before an aborted CTA exits (bounded: ~2 ms).
+__device__ __forceinline__ void settle_after_abort() {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+}
+
+template <bool W_KN, bool DUAL>
+__global__ void __launch_bounds__(kQThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tmW2, const PairArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQStages * kQStageBytes);
+  uint64_t* empty = full + kQStages;
+  uint64_t* tfull = empty + kQStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank() & 1u;
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 16);  // 8 epilogue warps in each CTA of the pair
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmW);
+    if (DUAL) tma_prefetch_desc(&tmW2);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(tmem_holder, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag};
+  const int num_tiles = a.m_tiles * a.n_tiles;
+  const int num_kb = a.num_kb;
+  const int out_bn = DUAL ? 128 : 256;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      uint32_t fills[kQStages];
+#pragma unroll
+      for (int i = 0; i < kQStages; ++i) fills[i] = 0;
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        int mb, nb;
+        tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + s * kQStageBytes;
+          uint8_t* sb = sa + kQABytes;
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * kQStageBytes);
+          tma_load_2d_pair(sa, &tmA, bar, kb * kBK, mb * kQTileM + static_cast<int>(rank) * kBM);
+          const CUtensorMap* wmap = (DUAL && rank) ? &tmW2 : &tmW;
+          const int n0 = DUAL ? nb * 128 : nb * 256 + static_cast<int>(rank) * 128;
+          if constexpr (W_KN) {
+            tma_load_2d_pair(sb, wmap, bar, n0, kb * kBK);
+            tma_load_2d_pair(sb + 8192, wmap, bar, n0 + 64, kb * kBK);
+          } else {
+            tma_load_2d_pair(sb, wmap, bar, kb * kBK, n0);
+          }
+          fills[s]++;
+          if (++s == kQStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (ok) {
+        // Every copy is consumed before the MMA reports the stage empty.
+        for (int i = 0; i < kQStages; ++i)
+          if (fills[i]) wait_bar(&empty[i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
+      } else {
+        settle_after_abort();
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16(kQTileM, 256, false, W_KN);
+      int s = 0;
+      uint32_t ph = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += npairs, ++local) {
+        const int buf = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!wait_bar(&tempty[buf], aph ^ 1, ctl, kSiteMmaAccEmpty)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * 256;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(stages + s * kQStageBytes);
+          const uint32_t b0 = a0 + kQABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t bd = W_KN ? sdesc_sw128(b0 + k * 2048, 8192, 1024)
+                                     : sdesc_sw128(b0 + k * 32, 16, 1024);
+            mma_ss_pair(d, ad, bd, idesc, (kb | k) != 0);
+          }
+          mma_commit_pair(&empty[s], 0x3);
+          if (++s == kQStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        if (!(a.ctl.inject && local == 0)) mma_commit_pair(&tfull[buf], 0x3);
+      }
+      mma_commit_pair(done, 0x1);
+      wait_bar(done, 0, ctl, kSiteDrain, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
+    constexpr int kChunks = (DUAL ? 128 : 256) / 32;
+    constexpr int kMine = kChunks / 2;
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
+                                       mapa_shared(smem_u32(&tempty[1]), 0)};
+    int local = 0;
+    for (int t = pair; t < num_tiles; t += npairs, ++local) {
+      int mb, nb;
+      tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+      const int buf = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      const int64_t row =
+          static_cast<int64_t>(mb) * kQTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
+      RowLoads L;
+      epi_row_prefetch(L, row, nb * out_bn + half * kMine * 32, a.M, a.N, a.ep);
+      if (!wait_bar(&tfull[buf], aph, ctl, kSiteEpiAccFull)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + buf * 256 + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int cc = 0; cc < kMine; ++cc) {
+        const int c = half * kMine + cc;
+        const int col0 = nb * out_bn + c * 32;
+        uint32_t acc[32], up[32];
+        tmem_ld32(tb + c * 32, acc);
+        if constexpr (DUAL) tmem_ld32(tb + 128 + c * 32, up);
+        tmem_wait_ld();
+        if (cc == kMine - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(&tempty[buf]);
+            else mbar_arrive_cluster(tempty_leader[buf]);
+          }
+        }
+        const RowLoads cur = L;
+        if (cc + 1 < kMine) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep);
+        if (row < a.M) {
+          switch (a.ep.act) {
+            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
+            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
+            case kActGeluTanh:
+              epi_row32<kActGeluTanh, DUAL>(acc, up, cur, row, col0, a.N, a.ep);
+              break;
+            default: epi_row32<kActIdentity, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal it or read its memory
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+namespace {
+
+template <bool W_KN, bool DUAL>
+cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                     const CUtensorMap& tmW2, const PairArgs& args, cudaStream_t stream) {
+  static std::atomic<uint64_t> mask{0};
+  auto kernel = gemm_pair_kernel<W_KN, DUAL>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (!(mask.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+    if (e != cudaSuccess) return e;
+    mask.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid, 1, 1);
+  cfg.blockDim = dim3(kQThreads, 1, 1);
+  cfg.dynamicSmemBytes = kQSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, tmW2, args);
+}
+
+}  // namespace
+
+int max_active_pairs() {
+  // Clusters of two 1-SM CTAs that fit on the device at once.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kQThreads, 1, 1);
+  cfg.dynamicSmemBytes = kQSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  auto kernel = gemm_pair_kernel<false, false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+      cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
+                             const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                             const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
+                             cudaStream_t stream) {
+  PairArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
+  if (w_kn)
+    return dual ? run_pair<true, true>(plan, tmA, tmW, tmW2, args, stream)
+                : run_pair<true, false>(plan, tmA, tmW, tmW2, args, stream);
+  return dual ? run_pair<false, true>(plan, tmA, tmW, tmW2, args, stream)
+              : run_pair<false, false>(plan, tmA, tmW, tmW2, args, stream);
+}
+
+}  // namespace gbf

@@ -28,6 +28,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -37,75 +38,6 @@ constexpr int kUK = 16;  // K per tcgen05.mma, kind::f16
 
 // ============================================================ shared pieces
 
-// Round a pointer into dynamic shared memory up to 1024 bytes with pointer
-// arithmetic on the shared array itself, so the compiler keeps the shared
-// address space (ld/st.shared instead of generic accesses).
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
-}
-
-// Operands of the ending for 32 consecutive columns of one row, loaded
-// before the accumulator is read from TMEM so that their latency overlaps.
-struct RowLoads {
-  uint4 c[4];
-  uint4 b[4];
-  uint4 r[4];
-};
-
-__device__ __forceinline__ void epi_row_prefetch(RowLoads& L, int64_t row, int col0, int M,
-                                                 int N, const EpiParams& e) {
-  const bool rok = row < M;
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const int col = col0 + v * 8;
-    const bool ok = rok && col < N;
-    const int64_t off = row * N + col;
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    L.c[v] = (ok && e.C) ? ldg_u4(e.C + off) : z;
-    L.b[v] = (ok && e.bias) ? ldg_u4(e.bias + col) : z;
-    L.r[v] = (ok && e.residual) ? ld_u4(e.residual + off) : z;  // may alias out
-  }
-}
-
-// Epilogue of 32 consecutive output columns of one row (persistent kernel).
-// `acc` holds fp32 bit patterns; for the dual GEMM `up` holds the up
-// product and the result is act(alpha*g) * (alpha*u) + beta*C.
-template <int ACT, bool DUAL>
-__device__ __forceinline__ void epi_row32(const uint32_t (&acc)[32], const uint32_t (&up)[32],
-                                          const RowLoads& L, int64_t row, int col0, int N,
-                                          const EpiParams& e) {
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const int col = col0 + v * 8;
-    if (col >= N) break;
-    const int64_t off = row * N + col;
-    float x[8];
-    if constexpr (DUAL) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        x[i] = act_apply<ACT>(e.alpha * __uint_as_float(acc[v * 8 + i])) *
-               (e.alpha * __uint_as_float(up[v * 8 + i]));
-      if (e.C) {
-        float c[8];
-        unpack8(L.c[v], c);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = fmaf(e.beta, c[i], x[i]);
-      }
-    } else {
-      float c[8], b[8], r[8];
-      unpack8(L.c[v], c);
-      unpack8(L.b[v], b);
-      unpack8(L.r[v], r);
-      const float beta = e.C ? e.beta : 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        x[i] = act_apply<ACT>(fmaf(beta, c[i], e.alpha * __uint_as_float(acc[v * 8 + i])) + b[i]) +
-               r[i];
-    }
-    st_u4(e.out + off, pack8(x));
-  }
-}
-
 // ============================================================ persistent kernel
 
 constexpr int kPStages = 4;
@@ -114,7 +46,6 @@ constexpr int kPBBytes = kPersistBN * kBK * 2;      // 32 KB
 constexpr int kPStageBytes = kPABytes + kPBBytes;   // 48 KB
 constexpr int kPThreads = 384;  // warps 0-3 roles, warps 4-11 epilogue (two warpgroups)
 constexpr int kPSmem = 1024 + kPStages * kPStageBytes + 256;
-constexpr int kPGroupM = 16;                        // tile raster: 16 M-tiles per group
 
 struct PersistArgs {
   int M, N, K;
@@ -122,16 +53,6 @@ struct PersistArgs {
   EpiParams ep;
   KernelCtl ctl;
 };
-
-__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mb, int& nb) {
-  const int per_group = kPGroupM * n_tiles;
-  const int g = t / per_group;
-  const int first_m = g * kPGroupM;
-  const int gm = min(kPGroupM, m_tiles - first_m);
-  const int local = t - g * per_group;
-  nb = local / gm;
-  mb = first_m + local % gm;
-}
 
 template <bool W_KN, bool DUAL>
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -355,32 +276,6 @@ struct SwapArgs {
   EpiParams ep;
   KernelCtl ctl;
 };
-
-// Epilogue of one output column n for 16 consecutive rows m0..m0+15.  All
-// operand loads are issued first (independent, so they overlap), then the
-// math and the stores.
-template <int ACT>
-__device__ __forceinline__ void epi_col16(const float (&v)[16], int64_t m0, int n, int M,
-                                          int N, const EpiParams& e) {
-  if (n >= N) return;
-  const float b = e.bias ? __bfloat162float(e.bias[n]) : 0.0f;
-  float c[16], r[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int64_t m = m0 + j;
-    const bool ok = m < M;
-    const int64_t off = m * N + n;
-    c[j] = (ok && e.C) ? __bfloat162float(e.C[off]) : 0.0f;
-    r[j] = (ok && e.residual) ? __bfloat162float(e.residual[off]) : 0.0f;
-  }
-  const float beta = e.C ? e.beta : 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int64_t m = m0 + j;
-    if (m < M)
-      e.out[m * N + n] = __float2bfloat16_rn(act_apply<ACT>(fmaf(beta, c[j], e.alpha * v[j]) + b) + r[j]);
-  }
-}
 
 template <int MPAD, bool W_KN>
 __global__ void __launch_bounds__(256, 2)

@@ -30,7 +30,7 @@ struct KernelCtl {
 };
 
 // Kernel families (gbf_kernel_path codes).
-enum Path { kPathNone = 0, kPathPersistent = 1, kPathSwap = 2, kPathW4 = 3 };
+enum Path { kPathNone = 0, kPathPersistent = 1, kPathSwap = 2, kPathW4 = 3, kPathPair = 4 };
 
 struct GemmPlan {
   int path = kPathNone;
@@ -44,6 +44,7 @@ struct GemmPlan {
 
 struct DeviceInfo {
   int sms = 0;
+  int pairs = 0;  // CTA pairs (clusters of two 1-SM CTAs) that fit at once
   int cc_major = 0;
   int cc_minor = 0;
 };
@@ -59,6 +60,13 @@ cudaError_t launch_gemm(const GemmPlan& plan, bool w_kn, bool dual, const CUtens
                         const CUtensorMap& tmW, const CUtensorMap& tmW2,
                         const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
                         cudaStream_t stream);
+
+// The same on CTA pairs with tcgen05.mma.cta_group::2 (gemm_pair.cu).
+cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
+                             const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                             const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
+                             cudaStream_t stream);
+int max_active_pairs();
 
 // Weight-only int4 GEMM (w4a16.cu).  tmA: activations; tmQ: packed bytes
 // [K][N/2]; tmS: scales [K/G][N].
@@ -82,7 +90,8 @@ constexpr int kBM = 128;        // MMA M: rows of TMEM / output tile height
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kPersistBN = 256; // persistent kernel: MMA N
 constexpr int kSwapBN = 128;    // swapped kernel: output columns per tile (= MMA M)
-constexpr int kW4BN = 256;      // W4A16 kernel: output columns per tile
+constexpr int kW4BN = 512;      // W4A16 kernel: output columns per tile
 constexpr int kMaxSplits = 8;   // portable cluster size limit
+constexpr int kPairMinM = 512;  // M from which the CTA-pair kernel is used
 
 }  // namespace gbf

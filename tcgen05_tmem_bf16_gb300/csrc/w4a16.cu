@@ -14,20 +14,28 @@
 // carries only the half byte the TMA engine wrote and the transform threads
 // read once.
 //
-// Tile: 256 output columns.  Transform thread t (0..127, warps 4-7) owns
-// packed byte column t: output columns n0+2t (high nibble) and n0+2t+1 (low
-// nibble).  The even columns form one 128-row A operand (TMEM region E) and
-// the odd columns another (region O), so every thread writes only its own
-// TMEM lane, and the epilogue stores column pairs as one bf16x2.  Each
-// 64-deep K block is two MMAs per 16-deep step (E and O).
+// Tile: 512 output columns.  Transform thread t (TMEM lane t) owns packed
+// bytes 2t and 2t+1 of every k-row, i.e. output columns n0+4t .. n0+4t+3
+// (high nibble of byte 2t, low nibble of 2t, high of 2t+1, low of 2t+1).
+// Those four columns are four 128-lane A operands ("regions" 0..3), so each
+// thread writes only its own TMEM lane, a 16-bit shared-memory load per k-row
+// feeds four weights, and the epilogue stores four adjacent outputs at once.
+// One 64-deep K block = 16 MMAs (4 regions x 4 steps of 16).
+//
+// Eight transform warps form two groups; group g dequantises k-rows
+// [32g, 32g+32) of every shared-memory stage into its own TMEM buffer, so
+// one group fills while the MMAs drain the other.
 //
 // Dequantisation of a nibble q, exact as the definition wants:
 //   bits 0x4300 | q  is the bf16 value 128 + q;
 //   (128 + q) - 136 = q - 8 exactly (small integers);
 //   (q - 8) * s with one bf16 multiply = bf16_rne((q - 8) * s).
+// For a k-row pair the two 16-bit loads are joined into X = row_k | row_k+1
+// << 16; the four regions are then (X >> 4), X, (X >> 12), (X >> 8) masked
+// with 0x000F000F -- each a bf16x2 pair (k, k+1) after OR-ing 0x43004300.
 //
-// K is split across a thread-block cluster; partial sums meet in the
-// rank-0 CTA through distributed shared memory, which applies the ending.
+// K is split across a thread-block cluster; partial sums meet through
+// distributed shared memory and the ending is applied once.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,24 +48,25 @@
 
 namespace gbf {
 
-constexpr int kW4Threads = 256;
-constexpr int kW4ABytes = kBK * (kW4BN / 2);  // packed tile: 64 rows x 128 bytes = 8 KB
-static_assert(kW4ABytes == 8192, "packed tile size");
-constexpr int kW4TStages = 2;                     // TMEM A-operand stages
+constexpr int kW4Threads = 384;                 // warps 0-3 roles, 4-11 transform/epilogue
+constexpr int kW4RowBytes = kW4BN / 2;          // packed bytes per k-row of a tile: 256
+constexpr int kW4QBytes = kBK * kW4RowBytes;    // 16 KB packed tile per stage
+static_assert(kW4QBytes == 16384, "packed tile size");
+constexpr int kW4Regions = 4;
 
 template <int MPAD>
 struct W4Cfg {
   static constexpr int kXBytes = MPAD * kBK * 2;                 // activations, SW128
-  static constexpr int kScaleBytes = 1024;                       // 256 bf16 + pad
-  static constexpr int kStageBytes = kW4ABytes + kXBytes + kScaleBytes;
-  static constexpr int kStages = MPAD <= 32 ? 8 : 6;
+  static constexpr int kScaleBytes = 1024;                       // 512 bf16
+  static constexpr int kStageBytes = kW4QBytes + kXBytes + kScaleBytes;
+  static constexpr int kStages = MPAD <= 16 ? 5 : 4;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
   static constexpr uint32_t kTmemCols = 256;
-  static constexpr uint32_t kColDE = 0;
-  static constexpr uint32_t kColDO = MPAD;
-  static constexpr uint32_t kColA = 2 * MPAD;  // A stage j: E at +64j, O at +64j+32
-  static_assert(kColA + 64 * kW4TStages <= kTmemCols, "TMEM budget");
-  static_assert(kStages * kStageBytes >= 128 * 2 * MPAD * 4, "reduction buffer must fit");
+  static constexpr uint32_t kColA = kW4Regions * MPAD;  // D region r at r*MPAD
+  // A buffer of group g at kColA + 64g; region r at +16r (16 columns = 32 k).
+  static_assert(kColA + 128 <= kTmemCols, "TMEM budget");
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+  static_assert(kStages * kStageBytes >= 128 * kW4Regions * MPAD * 4, "reduction buffer");
 };
 
 struct W4Args {
@@ -68,43 +77,76 @@ struct W4Args {
   KernelCtl ctl;
 };
 
-__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 v) {
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ __nv_bfloat162 bits_bf2(uint32_t u) {
-  return *reinterpret_cast<__nv_bfloat162*>(&u);
+// One k-row pair of this thread's two packed bytes -> the four dequantised
+// bf16x2 pairs (regions 0..3).  x0, x1: the 16-bit loads of rows k and k+1
+// (zero-extended).  In explicit PTX so that each step is one instruction:
+// join (prmt), three shifts, four lop3 ((v & 0x000F000F) | 0x43004300 gives
+// bf16 128+q in each half), and per pair one sub.rn.bf16x2 (-136, exact) and
+// one mul.rn.bf16x2 (x s, the single rounding the definition asks for).
+__device__ __forceinline__ void deq_rowpair(uint32_t x0, uint32_t x1, uint32_t c136,
+                                            uint32_t s0, uint32_t s1, uint32_t s2, uint32_t s3,
+                                            uint32_t& o0, uint32_t& o1, uint32_t& o2,
+                                            uint32_t& o3) {
+  asm("{\n\t"
+      ".reg .b32 x, t0, t1, t2, t3;\n\t"
+      "prmt.b32 x, %4, %5, 0x5410;\n\t"
+      "shr.b32 t0, x, 4;\n\t"
+      "shr.b32 t2, x, 12;\n\t"
+      "shr.b32 t3, x, 8;\n\t"
+      "lop3.b32 t0, t0, 0x000F000F, 0x43004300, 0xEA;\n\t"
+      "lop3.b32 t1, x, 0x000F000F, 0x43004300, 0xEA;\n\t"
+      "lop3.b32 t2, t2, 0x000F000F, 0x43004300, 0xEA;\n\t"
+      "lop3.b32 t3, t3, 0x000F000F, 0x43004300, 0xEA;\n\t"
+      "sub.rn.bf16x2 t0, t0, %6;\n\t"
+      "sub.rn.bf16x2 t1, t1, %6;\n\t"
+      "sub.rn.bf16x2 t2, t2, %6;\n\t"
+      "sub.rn.bf16x2 t3, t3, %6;\n\t"
+      "mul.rn.bf16x2 %0, t0, %7;\n\t"
+      "mul.rn.bf16x2 %1, t1, %8;\n\t"
+      "mul.rn.bf16x2 %2, t2, %9;\n\t"
+      "mul.rn.bf16x2 %3, t3, %10;\n\t"
+      "}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(x0), "r"(x1), "r"(c136), "r"(s0), "r"(s1), "r"(s2), "r"(s3));
 }
 
-// Epilogue of output columns (n, n+1) for 16 rows m0..m0+15: operand loads
-// first (independent, overlapping), then math and bf16x2 stores.
+// Epilogue of output columns n..n+3 for 8 rows m0..m0+7: operand loads
+// first (independent, overlapping), then the math and 8-byte stores.
 template <int ACT>
-__device__ __forceinline__ void epi_pair16(const float (&ve)[16], const float (&vo)[16],
-                                           int64_t m0, int n, int M, int N,
-                                           const EpiParams& e) {
+__device__ __forceinline__ void epi_quad8(const float (&v)[kW4Regions][8], int64_t m0, int n,
+                                          int M, int N, const EpiParams& e) {
   if (n >= N) return;
-  float b0 = 0.0f, b1 = 0.0f;
+  float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   if (e.bias) {
-    const uint32_t b = *reinterpret_cast<const uint32_t*>(e.bias + n);
-    b0 = bf16lo(b);
-    b1 = bf16hi(b);
-  }
-  uint32_t c[16], r[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int64_t m = m0 + j;
-    const bool ok = m < M;
-    const int64_t off = m * N + n;
-    c[j] = (ok && e.C) ? *reinterpret_cast<const uint32_t*>(e.C + off) : 0u;
-    r[j] = (ok && e.residual) ? *reinterpret_cast<const uint32_t*>(e.residual + off) : 0u;
+    const uint2 bb = *reinterpret_cast<const uint2*>(e.bias + n);
+    b[0] = bf16lo(bb.x); b[1] = bf16hi(bb.x); b[2] = bf16lo(bb.y); b[3] = bf16hi(bb.y);
   }
   const float beta = e.C ? e.beta : 0.0f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int64_t m = m0 + j;
-    if (m >= M) break;
-    const float x0 = act_apply<ACT>(fmaf(beta, bf16lo(c[j]), e.alpha * ve[j]) + b0) + bf16lo(r[j]);
-    const float x1 = act_apply<ACT>(fmaf(beta, bf16hi(c[j]), e.alpha * vo[j]) + b1) + bf16hi(r[j]);
-    *reinterpret_cast<uint32_t*>(e.out + m * N + n) = pack_bf16x2(x0, x1);
+  for (int h = 0; h < 2; ++h) {  // two halves of 4 rows keep the register count low
+    uint2 c[4], r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t m = m0 + 4 * h + j;
+      const bool ok = m < M;
+      const int64_t off = m * N + n;
+      c[j] = (ok && e.C) ? *reinterpret_cast<const uint2*>(e.C + off) : make_uint2(0, 0);
+      r[j] = (ok && e.residual) ? *reinterpret_cast<const uint2*>(e.residual + off)
+                                : make_uint2(0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t m = m0 + 4 * h + j;
+      if (m >= M) break;
+      const float cc[4] = {bf16lo(c[j].x), bf16hi(c[j].x), bf16lo(c[j].y), bf16hi(c[j].y)};
+      const float rr[4] = {bf16lo(r[j].x), bf16hi(r[j].x), bf16lo(r[j].y), bf16hi(r[j].y)};
+      float x[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        x[q] = act_apply<ACT>(fmaf(beta, cc[q], e.alpha * v[q][4 * h + j]) + b[q]) + rr[q];
+      *reinterpret_cast<uint2*>(e.out + m * N + n) =
+          make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+    }
   }
 }
 
@@ -120,9 +162,9 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kStages * Cfg::kStageBytes);
   uint64_t* empty = full + Cfg::kStages;
-  uint64_t* afull = empty + Cfg::kStages;
-  uint64_t* aempty = afull + kW4TStages;
-  uint64_t* dfull = aempty + kW4TStages;
+  uint64_t* afull = empty + Cfg::kStages;  // [2]: transform group g -> MMA
+  uint64_t* aempty = afull + 2;            // [2]: MMA -> transform group g
+  uint64_t* dfull = aempty + 2;
   uint64_t* done = dfull + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
@@ -139,9 +181,9 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 4 + 1);  // 4 transform warps + the MMA commit
+      mbar_init(&empty[i], 8 + 1);  // 8 transform warps + the MMA commit
     }
-    for (int i = 0; i < kW4TStages; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&afull[i], 4);
       mbar_init(&aempty[i], 1);
     }
@@ -175,12 +217,14 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) break;
         uint8_t* sq = stages + s * Cfg::kStageBytes;
-        uint8_t* sx = sq + kW4ABytes;
+        uint8_t* sx = sq + kW4QBytes;
         uint8_t* ss = sx + Cfg::kXBytes;
-        mbar_arrive_expect_tx(&full[s], kW4ABytes + Cfg::kXBytes + kW4BN * 2);
-        tma_load_2d_hint(sq, &tmQ, &full[s], nb * (kW4BN / 2), kb * kBK, stream_policy);
+        const int srow = (kb * kBK) / group;
+        mbar_arrive_expect_tx(&full[s], kW4QBytes + Cfg::kXBytes + kW4BN * 2);
+        tma_load_2d_hint(sq, &tmQ, &full[s], nb * kW4RowBytes, kb * kBK, stream_policy);
         tma_load_2d(sx, &tmA, &full[s], kb * kBK, mb * MPAD);
-        tma_load_2d(ss, &tmS, &full[s], nb * kW4BN, (kb * kBK) / group);
+        tma_load_2d(ss, &tmS, &full[s], nb * kW4BN, srow);
+        tma_load_2d(ss + 512, &tmS, &full[s], nb * kW4BN + 256, srow);
         fills[s]++;
         if (++s == Cfg::kStages) {
           s = 0;
@@ -198,26 +242,31 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        const int i = kb - kb0;
-        const int j = i % kW4TStages;
-        const uint32_t tph = (i / kW4TStages) & 1;
-        if (!wait_bar(&afull[j], tph, ctl, kSiteMmaOperand) ||
-            !wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
+      for (int kb = kb0; kb < kb1 && ok; ++kb) {
+        const uint32_t gph = (kb - kb0) & 1;
+        if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t x0 = smem_u32(stages + s * Cfg::kStageBytes + kW4ABytes);
-        const uint32_t aE = tmem_base + Cfg::kColA + 64 * j;
+        const uint32_t x0 = smem_u32(stages + s * Cfg::kStageBytes + kW4QBytes);
+        for (int g = 0; g < 2; ++g) {
+          if (!wait_bar(&afull[g], gph, ctl, kSiteMmaOperand)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t abuf = tmem_base + Cfg::kColA + 64 * g;
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k) {
-          const uint64_t bd = sdesc_sw128(x0 + k * 32, 16, 1024);
-          const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-          mma_ts(tmem_base + Cfg::kColDE, aE + k * 8, bd, idesc, accum);
-          mma_ts(tmem_base + Cfg::kColDO, aE + 32 + k * 8, bd, idesc, accum);
+          for (int k = 0; k < 2; ++k) {
+            const uint64_t bd = sdesc_sw128(x0 + (2 * g + k) * 32, 16, 1024);
+            const uint32_t accum = (kb != kb0 || g != 0 || k != 0) ? 1u : 0u;
+#pragma unroll
+            for (int r = 0; r < kW4Regions; ++r)
+              mma_ts(tmem_base + r * MPAD, abuf + 16 * r + 8 * k, bd, idesc, accum);
+          }
+          mma_commit(&aempty[g]);
         }
-        mma_commit(&aempty[j]);
+        if (!ok) break;
         mma_commit(&empty[s]);
         if (++s == Cfg::kStages) {
           s = 0;
@@ -231,44 +280,47 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dequantise into TMEM
-    const int t = threadIdx.x - 128;      // packed byte column = TMEM lane
-    const int q = warp & 3;
+    const int g = (warp - 4) >> 2;          // group: k-rows [32g, 32g + 32) of each stage
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int t = q * 32 + lane;            // TMEM lane = owner of packed bytes 2t, 2t+1
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const __nv_bfloat162 c136 = __floats2bfloat162_rn(136.0f, 136.0f);
+    const uint32_t abuf = tmem_base + lane_off + Cfg::kColA + 64 * g;
+    const uint32_t c136 = 0x43084308u;  // bf16x2 (136, 136)
     int s = 0;
     uint32_t ph = 0;
     for (int kb = kb0; kb < kb1; ++kb) {
-      const int i = kb - kb0;
-      const int j = i % kW4TStages;
-      const uint32_t tph = (i / kW4TStages) & 1;
+      const uint32_t gph = (kb - kb0) & 1;
       if (!wait_bar(&full[s], ph, ctl, kSiteXformFull)) break;
-      if (!wait_bar(&aempty[j], tph ^ 1, ctl, kSiteXformEmpty)) break;
+      if (!wait_bar(&aempty[g], gph ^ 1, ctl, kSiteXformEmpty)) break;
       tc_fence_after();
       const uint8_t* sq = stages + s * Cfg::kStageBytes;
-      const uint32_t sc = *reinterpret_cast<const uint32_t*>(sq + kW4ABytes + Cfg::kXBytes + 4 * t);
-      const __nv_bfloat162 sE = bits_bf2(__byte_perm(sc, 0, 0x1010));
-      const __nv_bfloat162 sO = bits_bf2(__byte_perm(sc, 0, 0x3232));
-      uint32_t e[32], o[32];
+      const uint2 sc = *reinterpret_cast<const uint2*>(sq + kW4QBytes + Cfg::kXBytes + 8 * t);
+      const uint32_t s0 = __byte_perm(sc.x, 0, 0x1010);  // bf16x2 (s, s), column 4t
+      const uint32_t s1 = __byte_perm(sc.x, 0, 0x3232);  // column 4t+1
+      const uint32_t s2 = __byte_perm(sc.y, 0, 0x1010);  // column 4t+2
+      const uint32_t s3 = __byte_perm(sc.y, 0, 0x3232);  // column 4t+3
+      const uint8_t* rows = sq + (32 * g) * kW4RowBytes + 2 * t;
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        const uint32_t b0 = sq[(2 * r) * 128 + t];
-        const uint32_t b1 = sq[(2 * r + 1) * 128 + t];
-        const uint32_t p = __byte_perm(b0, b1, 0x0400);  // byte0 = row 2r, byte2 = row 2r+1
-        const uint32_t lo = (p & 0x000F000Fu) | 0x43004300u;
-        const uint32_t hi = ((p >> 4) & 0x000F000Fu) | 0x43004300u;
-        o[r] = bf2_bits(__hmul2(__hsub2(bits_bf2(lo), c136), sO));
-        e[r] = bf2_bits(__hmul2(__hsub2(bits_bf2(hi), c136), sE));
+      for (int h = 0; h < 2; ++h) {
+        uint32_t o0[8], o1[8], o2[8], o3[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int row = 16 * h + 2 * p;
+          const uint32_t x0 = *reinterpret_cast<const uint16_t*>(rows + row * kW4RowBytes);
+          const uint32_t x1 = *reinterpret_cast<const uint16_t*>(rows + (row + 1) * kW4RowBytes);
+          // regions: 0 = high nibble of byte 2t, 1 = low of 2t, 2 = high of 2t+1, 3 = low of 2t+1
+          deq_rowpair(x0, x1, c136, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
+        }
+        tmem_st8(abuf + 0 + 8 * h, o0);
+        tmem_st8(abuf + 16 + 8 * h, o1);
+        tmem_st8(abuf + 32 + 8 * h, o2);
+        tmem_st8(abuf + 48 + 8 * h, o3);
       }
-      const uint32_t aE = tmem_base + lane_off + Cfg::kColA + 64 * j;
-      tmem_st16(aE, *reinterpret_cast<const uint32_t(*)[16]>(&e[0]));
-      tmem_st16(aE + 16, *reinterpret_cast<const uint32_t(*)[16]>(&e[16]));
-      tmem_st16(aE + 32, *reinterpret_cast<const uint32_t(*)[16]>(&o[0]));
-      tmem_st16(aE + 48, *reinterpret_cast<const uint32_t(*)[16]>(&o[16]));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&afull[j]);
+        mbar_arrive(&afull[g]);
         mbar_arrive(&empty[s]);
       }
       if (++s == Cfg::kStages) {
@@ -278,78 +330,83 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     }
   }
 
-  // ---- epilogue (warps 4-7): cluster reduction of the partial sums, ending.
-  // Every rank parks its partial in its own shared memory; 16-row chunks are
-  // shared out among the ranks (chunk c to rank c % S) and summed over ranks
-  // 0..S-1 in order through distributed shared memory.
+  // ---- epilogue: cluster reduction of the partial sums, then the ending.
+  // Every rank parks its partial in its own shared memory; 8-row chunks go
+  // to the (rank, group) workers round-robin and are summed over ranks
+  // 0..S-1 in that order through distributed shared memory.
   const bool epi = warp >= 4;
+  const int g = (warp - 4) >> 2;
   const int q = warp & 3;
-  const int tid = threadIdx.x - 128;
+  const int tid = q * 32 + lane;
   const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
   float4* red = reinterpret_cast<float4*>(stages);
-  constexpr int kChunks = MPAD / 16;  // per region
+  constexpr int kChunks = MPAD / 8;
   bool have = false;
   if (epi) {
     have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
     tc_fence_after();
-    if (S > 1) {
+    if (S > 1 && g == 0) {
 #pragma unroll 1
-      for (int c = 0; c < 2 * kChunks; ++c) {
-        const uint32_t col = (c < kChunks ? Cfg::kColDE : Cfg::kColDO) + (c % kChunks) * 16;
-        uint32_t r[16];
-        tmem_ld16(tb + col, r);
-        tmem_wait_ld();
+      for (int r = 0; r < kW4Regions; ++r) {
+#pragma unroll 1
+        for (int c = 0; c < MPAD / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tb + r * MPAD + c * 16, v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          red[(c * 4 + v) * 128 + tid] =
-              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          for (int w = 0; w < 4; ++w)
+            red[((r * (MPAD / 4)) + c * 4 + w) * 128 + tid] =
+                make_float4(__uint_as_float(v[4 * w]), __uint_as_float(v[4 * w + 1]),
+                            __uint_as_float(v[4 * w + 2]), __uint_as_float(v[4 * w + 3]));
+        }
       }
     }
   }
   if (S > 1) cluster_sync_all();
   if (epi) {
-    const int n = nb * kW4BN + 2 * tid;
+    const int n = nb * kW4BN + 4 * tid;
+    const int worker = static_cast<int>(rank) * 2 + g;
 #pragma unroll 1
-    for (int c = static_cast<int>(rank); c < kChunks; c += S) {
-      float ve[16], vo[16];
+    for (int c = worker; c < kChunks; c += 2 * S) {
+      float v[kW4Regions][8];
       if (S == 1) {
-        uint32_t re[16], ro[16];
-        tmem_ld16(tb + Cfg::kColDE + c * 16, re);
-        tmem_ld16(tb + Cfg::kColDO + c * 16, ro);
-        tmem_wait_ld();
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          ve[jj] = have ? __uint_as_float(re[jj]) : 0.0f;
-          vo[jj] = have ? __uint_as_float(ro[jj]) : 0.0f;
+        for (int r = 0; r < kW4Regions; ++r) {
+          uint32_t u[8];
+          tmem_ld8(tb + r * MPAD + c * 8, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[r][j] = have ? __uint_as_float(u[j]) : 0.0f;
         }
       } else {
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) ve[jj] = vo[jj] = 0.0f;
+        for (int r = 0; r < kW4Regions; ++r)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[r][j] = 0.0f;
         for (int p = 0; p < S; ++p) {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            float4 fe, fo;
-            float4* pe = &red[(c * 4 + w) * 128 + tid];
-            float4* po = &red[((kChunks + c) * 4 + w) * 128 + tid];
-            if (p == static_cast<int>(rank)) {
-              fe = *pe;
-              fo = *po;
-            } else {
-              fe = ld_dsmem_f4(mapa_shared(smem_u32(pe), static_cast<uint32_t>(p)));
-              fo = ld_dsmem_f4(mapa_shared(smem_u32(po), static_cast<uint32_t>(p)));
+          for (int r = 0; r < kW4Regions; ++r) {
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              float4* src = &red[((r * (MPAD / 4)) + c * 2 + w) * 128 + tid];
+              const float4 f = p == static_cast<int>(rank)
+                                   ? *src
+                                   : ld_dsmem_f4(mapa_shared(smem_u32(src),
+                                                             static_cast<uint32_t>(p)));
+              v[r][4 * w] += f.x;
+              v[r][4 * w + 1] += f.y;
+              v[r][4 * w + 2] += f.z;
+              v[r][4 * w + 3] += f.w;
             }
-            ve[4 * w] += fe.x; ve[4 * w + 1] += fe.y; ve[4 * w + 2] += fe.z; ve[4 * w + 3] += fe.w;
-            vo[4 * w] += fo.x; vo[4 * w + 1] += fo.y; vo[4 * w + 2] += fo.z; vo[4 * w + 3] += fo.w;
           }
         }
       }
-      const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;
+      const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 8;
       switch (a.ep.act) {
-        case kActRelu: epi_pair16<kActRelu>(ve, vo, m0, n, a.M, a.N, a.ep); break;
-        case kActSilu: epi_pair16<kActSilu>(ve, vo, m0, n, a.M, a.N, a.ep); break;
-        case kActGeluTanh: epi_pair16<kActGeluTanh>(ve, vo, m0, n, a.M, a.N, a.ep); break;
-        default: epi_pair16<kActIdentity>(ve, vo, m0, n, a.M, a.N, a.ep); break;
+        case kActRelu: epi_quad8<kActRelu>(v, m0, n, a.M, a.N, a.ep); break;
+        case kActSilu: epi_quad8<kActSilu>(v, m0, n, a.M, a.N, a.ep); break;
+        case kActGeluTanh: epi_quad8<kActGeluTanh>(v, m0, n, a.M, a.N, a.ep); break;
+        default: epi_quad8<kActIdentity>(v, m0, n, a.M, a.N, a.ep); break;
       }
     }
   }
@@ -404,7 +461,6 @@ cudaError_t launch_w4a16(const GemmPlan& plan, const CUtensorMap& tmA, const CUt
   switch (plan.mpad) {
     case 16: return run_w4<16>(plan, tmA, tmQ, tmS, args, group, stream);
     case 32: return run_w4<32>(plan, tmA, tmQ, tmS, args, group, stream);
-    case 64: return run_w4<64>(plan, tmA, tmQ, tmS, args, group, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -58,10 +58,12 @@ def test_workspace_sizes(lib):
 
 
 def test_kernel_path_planning(lib):
-    assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096) == ("persistent", 1)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096) == ("pair", 1)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096) == ("persistent", 1)
     path, splits = gbf.gbf_kernel_path("gemm_epilogue", 16, 8192, 8192, "kn")
     assert path == "swap_splitk" and 1 <= splits <= 8
-    assert gbf.gbf_kernel_path("swiglu", 2048, 14336, 4096)[0] == "persistent"
+    assert gbf.gbf_kernel_path("swiglu", 2048, 14336, 4096)[0] == "pair"
+    assert gbf.gbf_kernel_path("swiglu", 200, 14336, 4096)[0] == "persistent"
     path, splits = gbf.gbf_kernel_path("w4a16", 16, 28672, 8192)
     assert path == "w4a16" and 1 <= splits <= 8
     assert gbf.gbf_kernel_path("gemm_epilogue", 0, 8, 8)[0] == "none"

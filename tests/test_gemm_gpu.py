@@ -62,22 +62,30 @@ def test_small_m_swapped_kernel(cuda_lib, layout, M):
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-@pytest.mark.parametrize("M,N,K", [(129, 136, 72), (300, 520, 1000), (515, 264, 256),
-                                   (256, 512, 64), (1030, 1048, 136)])
+@pytest.mark.parametrize("M,N,K", [(129, 136, 72), (300, 520, 1000), (256, 512, 64),
+                                   (511, 264, 128)])
 def test_persistent_kernel(cuda_lib, layout, M, N, K):
     run_and_check(cuda_lib, M, N, K, layout, "silu", 0.5, 1.5, seed=M + N + K,
                   expect_path="persistent")
 
 
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,N,K", [(512, 256, 64), (515, 264, 256), (1030, 1048, 136),
+                                   (777, 520, 328), (2048, 1024, 512)])
+def test_cta_pair_kernel(cuda_lib, layout, M, N, K):
+    run_and_check(cuda_lib, M, N, K, layout, "gelu_tanh", 0.75, -0.25, seed=M + 3 * N + K,
+                  expect_path="pair")
+
+
 @pytest.mark.parametrize("act", ["identity", "relu", "silu", "gelu_tanh"])
-@pytest.mark.parametrize("M", [48, 260])
+@pytest.mark.parametrize("M", [48, 260, 600])
 def test_every_activation(cuda_lib, act, M):
     run_and_check(cuda_lib, M, 392, 200, "nk", act, 1.25, -0.5, seed=7 + M)
 
 
 @pytest.mark.parametrize("opts", [(False, False, False), (True, False, False),
                                   (False, True, False), (False, False, True)])
-@pytest.mark.parametrize("M", [20, 200])
+@pytest.mark.parametrize("M", [20, 200, 700])
 def test_optional_operands(cuda_lib, opts, M):
     c, b, r = opts
     run_and_check(cuda_lib, M, 256, 128, "kn", "relu", 1.0, 2.0, seed=11 + M, c=c, bias=b, res=r)
@@ -98,7 +106,7 @@ def test_plain_product_matches_torch_matmul(cuda_lib, M):
     assert_parity(down(out), down(t), "plain product vs torch")
 
 
-@pytest.mark.parametrize("M", [5, 300])
+@pytest.mark.parametrize("M", [5, 300, 520])
 def test_in_place_residual(cuda_lib, M):
     N, K = 264, 128
     A, B, C, bi, r = case(M, N, K, "nk", 400 + M)

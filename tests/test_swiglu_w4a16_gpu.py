@@ -21,7 +21,7 @@ def rand_bf16(seed, shape, std=1.0):
 
 @pytest.mark.parametrize("layout", ["nk", "kn"])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (130, 264, 328), (300, 128, 1000),
-                                   (513, 392, 256)])
+                                   (513, 392, 256), (1024, 264, 328), (1500, 512, 200)])
 def test_swiglu_dual_gemm(cuda_lib, layout, M, N, K):
     x = rand_bf16(M + 1, (M, K))
     shp = (N, K) if layout == "nk" else (K, N)
@@ -74,7 +74,8 @@ def w4_case(M, N, K, G, seed):
 
 @pytest.mark.parametrize("M,N,K,G", [(1, 256, 128, 128), (16, 544, 1024, 128),
                                      (20, 256, 512, 64), (64, 32, 256, 128),
-                                     (100, 512, 384, 128), (3, 1056, 2048, 256)])
+                                     (100, 512, 384, 128), (3, 1056, 2048, 256),
+                                     (32, 1536, 640, 64), (7, 2080, 8192, 128)])
 def test_w4a16_full_output(cuda_lib, M, N, K, G):
     A, Wq, s = w4_case(M, N, K, G, seed=M * 7 + N)
     out = poison_bf16(M, N)
