@@ -159,15 +159,17 @@ gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, 
     }
     return cuda_status(launch_pointwise_epilogue(nullptr, ep, M, N, dev.sms, stream));
   }
-  const GemmPlan plan = plan_gemm(M, N, K, dual, dev);
   const bool kn = layout == GBF_B_KN;
+  const GemmPlan plan = plan_gemm(M, N, K, dual, kn, dev);
   CUtensorMap tmA, tmW, tmW2;
   const uint32_t a_rows = plan.path == kPathSwap ? plan.mpad : kBM;
   const bool pair = plan.path == kPathPair;
   if (!tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, kBK, a_rows,
                CU_TENSOR_MAP_SWIZZLE_128B))
     return GBF_ERR_CUDA;
-  uint32_t w_rows = (plan.path == kPathSwap || pair) ? 128 : (dual ? 128 : kPersistBN);
+  uint32_t w_rows = plan.path == kPathSwap ? 128
+                    : pair                  ? (dual ? 128 : plan.bn / 2)
+                                            : (dual ? 128 : kPersistBN);
   const void* ws[2] = {W, dual ? W2 : W};
   CUtensorMap* maps[2] = {&tmW, &tmW2};
   for (int i = 0; i < 2; ++i) {
@@ -215,7 +217,7 @@ gbf_status_t check_w4(int64_t M, int64_t N, int64_t K, int group, int act) {
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo& dev) {
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const DeviceInfo& dev) {
   GemmPlan p;
   if (M == 0 || N == 0 || K == 0) return p;
   p.num_kb = ceil_div(K, kBK);
@@ -229,6 +231,20 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo&
     p.path = kPathPair;
     p.m_tiles = ceil_div(M, 2 * kBM);
     p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
+    p.bn = 256;
+    if (!dual && !kn) {
+      // A 224-wide tile when it wastes less of the last round of tiles:
+      // compare useful area / (rounds * pairs * tile area).
+      auto eff = [&](int bn) {
+        const int64_t tiles = static_cast<int64_t>(p.m_tiles) * ceil_div(N, bn);
+        const int64_t rounds = (tiles + dev.pairs - 1) / dev.pairs;
+        return static_cast<double>(M) * N / (static_cast<double>(rounds) * dev.pairs * 256 * bn);
+      };
+      if (eff(224) > eff(256) * 1.02) {
+        p.bn = 224;
+        p.n_tiles = ceil_div(N, 224);
+      }
+    }
     p.grid = 2 * std::min(p.m_tiles * p.n_tiles, dev.pairs);
   } else {
     p.path = kPathPersistent;
@@ -459,7 +475,7 @@ int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int* 
     case GBF_OP_SWIGLU:
       if (check_common(M, N, K, 0) != GBF_OK || (b_layout != GBF_B_KN && b_layout != GBF_B_NK))
         return -1;
-      p = plan_gemm(M, N, K, op == GBF_OP_SWIGLU, dev);
+      p = plan_gemm(M, N, K, op == GBF_OP_SWIGLU, b_layout == GBF_B_KN, dev);
       break;
     case GBF_OP_W4A16:
       if (check_w4(M, N, K, 128, 0) != GBF_OK) return -1;

@@ -68,10 +68,12 @@ __device__ __forceinline__ float act_apply(float v) {
   if constexpr (ACT == kActRelu) {
     return fmaxf(v, 0.0f);
   } else if constexpr (ACT == kActSilu) {
-    return v / (1.0f + __expf(-v));
+    // approximate reciprocal (a few ulp of fp32, far below bf16's rounding);
+    // 1/inf = 0 keeps large negative v at -0
+    return v * __fdividef(1.0f, 1.0f + __expf(-v));
   } else if constexpr (ACT == kActGeluTanh) {
     const float z = 0.7978845608028654f * fmaf(0.044715f * v, v * v, v);
-    return v / (1.0f + __expf(-2.0f * z));
+    return v * __fdividef(1.0f, 1.0f + __expf(-2.0f * z));
   } else {
     return v;
   }
@@ -107,6 +109,43 @@ __device__ __forceinline__ uint4 ld_u4(const void* p) {
 }
 __device__ __forceinline__ void st_u4(void* p, const uint4& v) {
   *reinterpret_cast<uint4*>(p) = v;
+}
+
+// Streaming accesses of the ending's operands and results: they are touched
+// once, so they are marked evict-first in L2 and do not push the GEMM's
+// operand panels out.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_stream_u4(const void* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_stream_u4(void* ptr, const uint4& v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(ptr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* ptr, uint64_t pol) {
+  uint16_t v;
+  asm volatile("ld.global.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_stream_u16(void* ptr, uint16_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.u16 [%0], %1, %2;" ::"l"(ptr), "h"(v), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ float bf16bits_to_f(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+__device__ __forceinline__ uint16_t f_to_bf16bits(float x) {
+  __nv_bfloat16 b = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&b);
 }
 
 __device__ __forceinline__ float ld_bf16f(const __nv_bfloat16* p) {

@@ -28,7 +28,7 @@ struct RowLoads {
 };
 
 __device__ __forceinline__ void epi_row_prefetch(RowLoads& L, int64_t row, int col0, int M,
-                                                 int N, const EpiParams& e) {
+                                                 int N, const EpiParams& e, uint64_t pol) {
   const bool rok = row < M;
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
@@ -36,9 +36,9 @@ __device__ __forceinline__ void epi_row_prefetch(RowLoads& L, int64_t row, int c
     const bool ok = rok && col < N;
     const int64_t off = row * N + col;
     const uint4 z = make_uint4(0, 0, 0, 0);
-    L.c[v] = (ok && e.C) ? ldg_u4(e.C + off) : z;
+    L.c[v] = (ok && e.C) ? ld_stream_u4(e.C + off, pol) : z;
     L.b[v] = (ok && e.bias) ? ldg_u4(e.bias + col) : z;
-    L.r[v] = (ok && e.residual) ? ld_u4(e.residual + off) : z;  // may alias out
+    L.r[v] = (ok && e.residual) ? ld_stream_u4(e.residual + off, pol) : z;  // may alias out
   }
 }
 
@@ -48,7 +48,7 @@ __device__ __forceinline__ void epi_row_prefetch(RowLoads& L, int64_t row, int c
 template <int ACT, bool DUAL>
 __device__ __forceinline__ void epi_row32(const uint32_t (&acc)[32], const uint32_t (&up)[32],
                                           const RowLoads& L, int64_t row, int col0, int N,
-                                          const EpiParams& e) {
+                                          const EpiParams& e, uint64_t pol) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const int col = col0 + v * 8;
@@ -77,7 +77,7 @@ __device__ __forceinline__ void epi_row32(const uint32_t (&acc)[32], const uint3
         x[i] = act_apply<ACT>(fmaf(beta, c[i], e.alpha * __uint_as_float(acc[v * 8 + i])) + b[i]) +
                r[i];
     }
-    st_u4(e.out + off, pack8(x));
+    st_stream_u4(e.out + off, pack8(x), pol);
   }
 }
 
@@ -96,29 +96,43 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
   mb = first_m + local % gm;
 }
 
-// Epilogue of one output column n for 16 consecutive rows m0..m0+15.  All
-// operand loads are issued first (independent, so they overlap), then the
-// math and the stores.
-template <int ACT>
-__device__ __forceinline__ void epi_col16(const float (&v)[16], int64_t m0, int n, int M,
-                                          int N, const EpiParams& e) {
-  if (n >= N) return;
-  const float b = e.bias ? __bfloat162float(e.bias[n]) : 0.0f;
-  float c[16], r[16];
+// Epilogue of one output column n for 16 consecutive rows m0..m0+15 (the
+// swapped kernels): the operands are fetched first (col16_prefetch, which can
+// run before the accumulator is ready), then the math and the stores.
+struct ColLoads {
+  float c[16];
+  float r[16];
+  float b;
+};
+
+__device__ __forceinline__ void col16_prefetch(ColLoads& L, int64_t m0, int n, int M, int N,
+                                               const EpiParams& e, uint64_t pol) {
+  const bool nok = n < N;
+  L.b = (nok && e.bias) ? __bfloat162float(e.bias[n]) : 0.0f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int64_t m = m0 + j;
-    const bool ok = m < M;
+    const bool ok = nok && m < M;
     const int64_t off = m * N + n;
-    c[j] = (ok && e.C) ? __bfloat162float(e.C[off]) : 0.0f;
-    r[j] = (ok && e.residual) ? __bfloat162float(e.residual[off]) : 0.0f;
+    L.c[j] = (ok && e.C) ? bf16bits_to_f(ld_stream_u16(e.C + off, pol)) : 0.0f;
+    L.r[j] = (ok && e.residual) ? bf16bits_to_f(ld_stream_u16(e.residual + off, pol)) : 0.0f;
   }
+}
+
+template <int ACT>
+__device__ __forceinline__ void epi_col16(const float (&v)[16], const ColLoads& L, int64_t m0,
+                                          int n, int M, int N, const EpiParams& e,
+                                          uint64_t pol) {
+  if (n >= N) return;
   const float beta = e.C ? e.beta : 0.0f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int64_t m = m0 + j;
     if (m < M)
-      e.out[m * N + n] = __float2bfloat16_rn(act_apply<ACT>(fmaf(beta, c[j], e.alpha * v[j]) + b) + r[j]);
+      st_stream_u16(e.out + m * N + n,
+                    f_to_bf16bits(act_apply<ACT>(fmaf(beta, L.c[j], e.alpha * v[j]) + L.b) +
+                                  L.r[j]),
+                    pol);
   }
 }
 

@@ -36,11 +36,22 @@ namespace gbf {
 
 constexpr int kQStages = 6;
 constexpr int kQABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
-constexpr int kQBBytes = 128 * kBK * 2;        // 16 KB: this CTA's half of the B tile
-constexpr int kQStageBytes = kQABytes + kQBBytes;
 constexpr int kQThreads = 384;                 // warps 0-3 roles, 4-11 epilogue
-constexpr int kQSmem = 1024 + kQStages * kQStageBytes + 256;
 constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
+
+// Tile width BN (MMA N) of the pair: 256, or 224 when that fills the last
+// round of tiles better (the planner picks it for K-contiguous weights).
+// Each CTA holds BN/2 rows of the B tile.
+template <int BN>
+struct PairCfg {
+  static constexpr int kBBytes = (BN / 2) * kBK * 2;
+  static constexpr int kStageBytes = kQABytes + kBBytes;
+  static constexpr int kSmem = 1024 + kQStages * kStageBytes + 256;
+  static constexpr int kChunks = BN / 32;             // 32-column epilogue chunks
+  static constexpr int kHalf0 = (kChunks + 1) / 2;    // chunks of the first warpgroup
+  static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+  static_assert(BN % 32 == 0 && BN <= 256, "tile width");
+};
 
 struct PairArgs {
   int M, N, K;
@@ -55,14 +66,16 @@ __device__ __forceinline__ void settle_after_abort() {
   while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
 }
 
-template <bool W_KN, bool DUAL>
+template <bool W_KN, bool DUAL, int BN>
 __global__ void __launch_bounds__(kQThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmW2, const PairArgs a) {
+  using Cfg = PairCfg<BN>;
+  static_assert(!(W_KN || DUAL) || BN == 256, "narrow tiles only for K-contiguous single B");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQStages * kQStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQStages * Cfg::kStageBytes);
   uint64_t* empty = full + kQStages;
   uint64_t* tfull = empty + kQStages;
   uint64_t* tempty = tfull + 2;
@@ -105,7 +118,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag};
   const int num_tiles = a.m_tiles * a.n_tiles;
   const int num_kb = a.num_kb;
-  const int out_bn = DUAL ? 128 : 256;
+  const int out_bn = DUAL ? 128 : BN;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -124,13 +137,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
             ok = false;
             break;
           }
-          uint8_t* sa = stages + s * kQStageBytes;
+          uint8_t* sa = stages + s * Cfg::kStageBytes;
           uint8_t* sb = sa + kQABytes;
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
-          if (leader) mbar_arrive_expect_tx(&full[s], 2 * kQStageBytes);
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * Cfg::kStageBytes);
           tma_load_2d_pair(sa, &tmA, bar, kb * kBK, mb * kQTileM + static_cast<int>(rank) * kBM);
           const CUtensorMap* wmap = (DUAL && rank) ? &tmW2 : &tmW;
-          const int n0 = DUAL ? nb * 128 : nb * 256 + static_cast<int>(rank) * 128;
+          const int n0 = DUAL ? nb * 128 : nb * BN + static_cast<int>(rank) * (BN / 2);
           if constexpr (W_KN) {
             tma_load_2d_pair(sb, wmap, bar, n0, kb * kBK);
             tma_load_2d_pair(sb + 8192, wmap, bar, n0 + 64, kb * kBK);
@@ -156,7 +169,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_bf16(kQTileM, 256, false, W_KN);
+      constexpr uint32_t idesc = idesc_bf16(kQTileM, BN, false, W_KN);
       int s = 0;
       uint32_t ph = 0;
       int local = 0;
@@ -173,7 +186,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(stages + s * kQStageBytes);
+          const uint32_t a0 = smem_u32(stages + s * Cfg::kStageBytes);
           const uint32_t b0 = a0 + kQABytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
@@ -199,8 +212,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;
-    constexpr int kChunks = (DUAL ? 128 : 256) / 32;
-    constexpr int kMine = kChunks / 2;
+    const uint64_t pol = l2_evict_first_policy();
+    constexpr int kChunks = DUAL ? 4 : Cfg::kChunks;
+    constexpr int kFirst = DUAL ? 2 : Cfg::kHalf0;  // chunks of warpgroup 0; the rest go to 1
+    const int c_begin = half == 0 ? 0 : kFirst;
+    const int c_end = half == 0 ? kFirst : kChunks;
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
                                        mapa_shared(smem_u32(&tempty[1]), 0)};
     int local = 0;
@@ -212,19 +228,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const int64_t row =
           static_cast<int64_t>(mb) * kQTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
       RowLoads L;
-      epi_row_prefetch(L, row, nb * out_bn + half * kMine * 32, a.M, a.N, a.ep);
+      epi_row_prefetch(L, row, nb * out_bn + c_begin * 32, a.M, a.N, a.ep, pol);
       if (!wait_bar(&tfull[buf], aph, ctl, kSiteEpiAccFull)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + buf * 256 + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-      for (int cc = 0; cc < kMine; ++cc) {
-        const int c = half * kMine + cc;
+      for (int c = c_begin; c < c_end; ++c) {
         const int col0 = nb * out_bn + c * 32;
         uint32_t acc[32], up[32];
         tmem_ld32(tb + c * 32, acc);
         if constexpr (DUAL) tmem_ld32(tb + 128 + c * 32, up);
         tmem_wait_ld();
-        if (cc == kMine - 1) {
+        if (c == c_end - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -233,15 +248,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
         }
         const RowLoads cur = L;
-        if (cc + 1 < kMine) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep);
+        if (c + 1 < c_end) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep, pol);
         if (row < a.M) {
           switch (a.ep.act) {
-            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
-            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
+            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
+            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
             case kActGeluTanh:
-              epi_row32<kActGeluTanh, DUAL>(acc, up, cur, row, col0, a.N, a.ep);
+              epi_row32<kActGeluTanh, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol);
               break;
-            default: epi_row32<kActIdentity, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
+            default: epi_row32<kActIdentity, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
           }
         }
       }
@@ -259,11 +274,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 namespace {
 
-template <bool W_KN, bool DUAL>
+template <bool W_KN, bool DUAL, int BN>
 cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
                      const CUtensorMap& tmW2, const PairArgs& args, cudaStream_t stream) {
   static std::atomic<uint64_t> mask{0};
-  auto kernel = gemm_pair_kernel<W_KN, DUAL>;
+  auto kernel = gemm_pair_kernel<W_KN, DUAL, BN>;
+  constexpr int kQSmem = PairCfg<BN>::kSmem;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -293,6 +309,7 @@ cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMa
 int max_active_pairs() {
   // Clusters of two 1-SM CTAs that fit on the device at once.
   cudaLaunchConfig_t cfg = {};
+  constexpr int kQSmem = PairCfg<256>::kSmem;
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kQThreads, 1, 1);
   cfg.dynamicSmemBytes = kQSmem;
@@ -303,7 +320,7 @@ int max_active_pairs() {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto kernel = gemm_pair_kernel<false, false>;
+  auto kernel = gemm_pair_kernel<false, false, 256>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return 0;
@@ -318,10 +335,11 @@ cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const C
                              cudaStream_t stream) {
   PairArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
   if (w_kn)
-    return dual ? run_pair<true, true>(plan, tmA, tmW, tmW2, args, stream)
-                : run_pair<true, false>(plan, tmA, tmW, tmW2, args, stream);
-  return dual ? run_pair<false, true>(plan, tmA, tmW, tmW2, args, stream)
-              : run_pair<false, false>(plan, tmA, tmW, tmW2, args, stream);
+    return dual ? run_pair<true, true, 256>(plan, tmA, tmW, tmW2, args, stream)
+                : run_pair<true, false, 256>(plan, tmA, tmW, tmW2, args, stream);
+  if (dual) return run_pair<false, true, 256>(plan, tmA, tmW, tmW2, args, stream);
+  return plan.bn == 224 ? run_pair<false, false, 224>(plan, tmA, tmW, tmW2, args, stream)
+                        : run_pair<false, false, 256>(plan, tmA, tmW, tmW2, args, stream);
 }
 
 }  // namespace gbf

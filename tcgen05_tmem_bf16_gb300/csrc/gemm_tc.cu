@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // columns, the second the right half.
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;
+    const uint64_t pol = l2_evict_first_policy();
     constexpr int kChunks = (DUAL ? 128 : 256) / 32;
     constexpr int kMine = kChunks / 2;
     int local = 0;
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint32_t aph = (local >> 1) & 1;
       const int64_t row = static_cast<int64_t>(mb) * kBM + q * 32 + lane;
       RowLoads L;
-      epi_row_prefetch(L, row, nb * out_bn + half * kMine * 32, a.M, a.N, a.ep);
+      epi_row_prefetch(L, row, nb * out_bn + half * kMine * 32, a.M, a.N, a.ep, pol);
       if (!wait_bar(&tfull[buf], aph, ctl, kSiteEpiAccFull)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + buf * 256 + (static_cast<uint32_t>(q * 32) << 16);
@@ -233,15 +234,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (lane == 0) mbar_arrive(&tempty[buf]);
         }
         const RowLoads cur = L;
-        if (cc + 1 < kMine) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep);
+        if (cc + 1 < kMine) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep, pol);
         if (row < a.M) {
           switch (a.ep.act) {
-            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
-            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
+            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
+            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
             case kActGeluTanh:
-              epi_row32<kActGeluTanh, DUAL>(acc, up, cur, row, col0, a.N, a.ep);
+              epi_row32<kActGeluTanh, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol);
               break;
-            default: epi_row32<kActIdentity, DUAL>(acc, up, cur, row, col0, a.N, a.ep); break;
+            default: epi_row32<kActIdentity, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
           }
         }
       }
@@ -399,6 +400,12 @@ __global__ void __launch_bounds__(256, 2)
   float4* red = reinterpret_cast<float4*>(stages);
   constexpr int kChunks = MPAD / 16;
   bool have = false;
+  const uint64_t pol = l2_evict_first_policy();
+  const int n = nb * kSwapBN + tid;
+  ColLoads L;
+  if (epi && static_cast<int>(rank) < kChunks)  // this rank's first chunk: operands early
+    col16_prefetch(L, static_cast<int64_t>(mb) * MPAD + static_cast<int>(rank) * 16, n, a.M,
+                   a.N, a.ep, pol);
   if (epi) {
     have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
     tc_fence_after();
@@ -418,9 +425,10 @@ __global__ void __launch_bounds__(256, 2)
   }
   if (S > 1) cluster_sync_all();
   if (epi) {
-    const int n = nb * kSwapBN + tid;
 #pragma unroll 1
     for (int c = static_cast<int>(rank); c < kChunks; c += S) {
+      if (c != static_cast<int>(rank))
+        col16_prefetch(L, static_cast<int64_t>(mb) * MPAD + c * 16, n, a.M, a.N, a.ep, pol);
       float v[16];
       if (S == 1) {
         uint32_t r[16];
@@ -450,10 +458,10 @@ __global__ void __launch_bounds__(256, 2)
       }
       const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;
       switch (a.ep.act) {
-        case kActRelu: epi_col16<kActRelu>(v, m0, n, a.M, a.N, a.ep); break;
-        case kActSilu: epi_col16<kActSilu>(v, m0, n, a.M, a.N, a.ep); break;
-        case kActGeluTanh: epi_col16<kActGeluTanh>(v, m0, n, a.M, a.N, a.ep); break;
-        default: epi_col16<kActIdentity>(v, m0, n, a.M, a.N, a.ep); break;
+        case kActRelu: epi_col16<kActRelu>(v, L, m0, n, a.M, a.N, a.ep, pol); break;
+        case kActSilu: epi_col16<kActSilu>(v, L, m0, n, a.M, a.N, a.ep, pol); break;
+        case kActGeluTanh: epi_col16<kActGeluTanh>(v, L, m0, n, a.M, a.N, a.ep, pol); break;
+        default: epi_col16<kActIdentity>(v, L, m0, n, a.M, a.N, a.ep, pol); break;
       }
     }
   }

@@ -39,7 +39,8 @@ struct GemmPlan {
   int m_tiles = 0;
   int n_tiles = 0;
   int num_kb = 0;    // 64-wide K blocks
-  int grid = 0;      // persistent kernel: CTAs
+  int grid = 0;      // persistent kernels: CTAs
+  int bn = 256;      // pair kernel: tile width (MMA N)
 };
 
 struct DeviceInfo {
@@ -50,7 +51,7 @@ struct DeviceInfo {
 };
 
 // ---- planning (api.cu) -------------------------------------------------------
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo& dev);
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const DeviceInfo& dev);
 GemmPlan plan_w4a16(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 
 // ---- launchers ---------------------------------------------------------------
