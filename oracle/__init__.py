@@ -13,6 +13,7 @@ Every function here follows the passage cited in ``gbf_oracle.c``:
                       "Kernel fusion" guide, Concept.
   * swiglu         -- "Fusion Thinking", Pattern 2 (Fused SwiGLU).
   * w4a16 / dequant_int4 -- "Fusion Thinking", Pattern 3 (Dequant + GEMM).
+  * add_rmsnorm    -- "Fusion Thinking", Pattern 1 (Fused RMSNorm + residual).
   * unfused modes  -- "kernel fusion" wiki, the activation-after-matmul case.
 """
 from __future__ import annotations
@@ -82,6 +83,8 @@ def _load():
         lib.oracle_pointwise_epilogue.restype = I
         lib.oracle_swiglu_pointwise.argtypes = [P, P, P, I64, I64, D, D, I, P]
         lib.oracle_swiglu_pointwise.restype = I
+        lib.oracle_add_rmsnorm.argtypes = [P, P, P, I64, I64, D, I, P, P]
+        lib.oracle_add_rmsnorm.restype = I
         _lib = lib
         return lib
 
@@ -220,3 +223,16 @@ def swiglu_pointwise(g, u, C=None, *, M, N, alpha=1.0, beta=0.0, act="silu"):
                                    float(beta), ACT[act], _ptr(out)) != 0:
         raise ValueError("oracle rejected its arguments")
     return out
+
+
+def add_rmsnorm(a, x, w, *, M, N, eps=1e-5, unfused=False):
+    """(norm, resid): resid = bf16(a + x); norm = bf16((a + x) * rsqrt(mean((a + x)^2) + eps) * w)
+    per row (unfused: the norm is taken of the bf16-rounded residual)."""
+    lib = _load()
+    a, x, w = map(_u16, (a, x, w))
+    norm = np.empty((M, N), dtype=np.uint16)
+    resid = np.empty((M, N), dtype=np.uint16)
+    if lib.oracle_add_rmsnorm(_ptr(a), _ptr(x), _ptr(w), M, N, float(eps), int(bool(unfused)),
+                              _ptr(norm), _ptr(resid)) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return norm, resid

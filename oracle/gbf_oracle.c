@@ -24,6 +24,11 @@
  *       "Fusion Thinking", Pattern 3 (Dequant + GEMM): packed 2 x int4 per
  *       byte along N, high nibble first (interleave(w_hi, w_lo)), zero point
  *       8, per-group bf16 scales, result fed to the matrix product.
+ *   add_rmsnorm     r = a + x;  resid = bf16(r);
+ *                   n = bf16( r / sqrt(mean_j(r_j^2) + eps) * w )   (per row)
+ *       "Fusion Thinking", Pattern 1 (Fused RMSNorm + residual): one pass
+ *       computes the residual sum, writes it for the next residual add, and
+ *       normalises the (unrounded) sum with the row's root mean square.
  *   unfused modes   the same results with the intermediate written as bf16
  *       between the product and the pointwise pass ("kernel fusion",
  *       infraphysics.net: "the activation-after-matmul case"; "Fusion
@@ -328,5 +333,38 @@ int oracle_swiglu_pointwise(const uint16_t *g, const uint16_t *u,
                 h += beta * oracle_bf16_to_f64(C[m * N + n]);
             out_bf16[m * N + n] = oracle_bf16_from_f64(h);
         }
+    return 0;
+}
+
+/* Fused residual add + RMSNorm ("Fusion Thinking", Pattern 1): per row m,
+ * r_j = a[m][j] + x[m][j] (exact in fp64), out_resid = bf16(r),
+ * out_norm = bf16(r_j / sqrt(sum_j r_j^2 / N + eps) * w[j]).  unfused != 0
+ * normalises the bf16-rounded residual instead, as a separate RMSNorm kernel
+ * reading the stored residual would ("x = x + a; rmsnorm(x)"). */
+int oracle_add_rmsnorm(const uint16_t *a, const uint16_t *x, const uint16_t *w, int64_t M,
+                       int64_t N, double eps, int unfused, uint16_t *out_norm,
+                       uint16_t *out_resid)
+{
+    if (M < 0 || N <= 0 || eps < 0.0)
+        return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double r = oracle_bf16_to_f64(a[m * N + j]) + oracle_bf16_to_f64(x[m * N + j]);
+            uint16_t rb = oracle_bf16_from_f64(r);
+            if (out_resid)
+                out_resid[m * N + j] = rb;
+            if (unfused)
+                r = oracle_bf16_to_f64(rb);
+            ss += r * r;
+        }
+        double rrms = 1.0 / sqrt(ss / (double)N + eps);
+        for (int64_t j = 0; j < N; ++j) {
+            double r = oracle_bf16_to_f64(a[m * N + j]) + oracle_bf16_to_f64(x[m * N + j]);
+            if (unfused)
+                r = oracle_bf16_to_f64(oracle_bf16_from_f64(r));
+            out_norm[m * N + j] = oracle_bf16_from_f64(r * rrms * oracle_bf16_to_f64(w[j]));
+        }
+    }
     return 0;
 }

@@ -363,3 +363,55 @@ def test_oracle_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.gemm_epilogue(A, np.zeros((4, 2), np.uint16), "kn", M=2, N=2, K=4,
                              rows=np.array([2]), cols=np.array([0]))
+
+
+# ---------------------------------------------------------------- add + RMSNorm
+
+def test_add_rmsnorm_hand_worked_example():
+    g = _golden("add_rmsnorm_hand.json")
+    a, x, w = bits(g["a"]), bits(g["x"]), bits(g["w"])
+    norm, resid = oracle.add_rmsnorm(a, x, w, M=3, N=4, eps=0.0)
+    assert np.array_equal(resid, bits(g["resid"]))
+    want = workloads_bf16(np.array(g["norm"], dtype=np.float64))
+    # compared as values: 0 * w with w < 0 is -0, equal to the fixture's 0
+    assert np.array_equal(oracle.bf16_bits_to_f64(norm), oracle.bf16_bits_to_f64(want))
+
+
+def workloads_bf16(v64):
+    # one RNE rounding of exact float64 values (1.2 and 3.2 are not bf16-exact)
+    return np.array([oracle.bf16_from_f64(float(t)) for t in v64.ravel()],
+                    dtype=np.uint16).reshape(v64.shape)
+
+
+def test_add_rmsnorm_matches_torch_rms_norm():
+    rng = np.random.Generator(np.random.PCG64(31))
+    M, N, eps = 7, 96, 1e-5
+    a = to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    x = to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    w = to_bf16_bits(rng.uniform(0.5, 1.5, N).astype(np.float32))
+    f = oracle.bf16_bits_to_f64
+    r = torch.from_numpy(f(a) + f(x))
+    want = torch.nn.functional.rms_norm(r, (N,), torch.from_numpy(f(w)), eps)
+    want_bits = want.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    norm, resid = oracle.add_rmsnorm(a, x, w, M=M, N=N, eps=eps)
+    assert np.array_equal(resid, r.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    # float64 torch vs fp64 oracle: equal after one bf16 rounding except at exact ties
+    assert np.mean(norm == want_bits) > 0.999
+    np.testing.assert_allclose(f(norm), want.numpy(), rtol=2 ** -8, atol=0)
+
+
+def test_add_rmsnorm_scale_invariance_and_unfused_mode():
+    rng = np.random.Generator(np.random.PCG64(32))
+    M, N = 4, 64
+    a = to_bf16_bits(rng.standard_normal((M, N)).astype(np.float32))
+    zero = np.zeros_like(a)
+    w = to_bf16_bits(np.ones(N, dtype=np.float32))
+    # eps = 0: normalising 4*a gives the same as normalising a (power-of-two scale is exact)
+    a4 = to_bf16_bits(oracle.bf16_bits_to_f64(a).astype(np.float32) * 4)
+    n1, _ = oracle.add_rmsnorm(a, zero, w, M=M, N=N, eps=0.0)
+    n4, _ = oracle.add_rmsnorm(a4, zero, w, M=M, N=N, eps=0.0)
+    assert np.array_equal(n1, n4)
+    # unfused normalises the stored bf16 residual: equal to fused when r is bf16-exact
+    nf, rf = oracle.add_rmsnorm(a, zero, w, M=M, N=N)
+    nu, ru = oracle.add_rmsnorm(a, zero, w, M=M, N=N, unfused=True)
+    assert np.array_equal(rf, ru) and np.array_equal(nf, nu)
