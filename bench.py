@@ -12,10 +12,11 @@ tiny case.
 Prints ONE JSON line.  ``value`` is whole-job TFLOP/s (FLOPs of every rank's
 steps / max over ranks of the timed region).  Inputs are resident in HBM;
 rotating input sets (>= 2x L2 in total) keep consecutive steps from reading
-each other's data out of L2.  Each launch is bracketed by CUDA events on the
-launching stream, which give the kernel's average duration for the roofline
-fraction.  Extra keys: roofline, cpu_baseline (the fp64 oracle timed on a
-bounded sample on the host cores), e2e (the same metric with host buffers and
+each other's data out of L2.  CUDA events on the launching stream bracket the
+timed region; a step is one kernel launch, so region / steps is the kernel's
+average launch duration used for the roofline fraction.  Extra keys:
+roofline, cpu_baseline (the fp64 oracle timed on a bounded sample on the host
+cores), e2e (the same metric with host buffers and
 host<->device copies inside the timed region), clocks (nvidia-smi samples taken
 during the timed region), the unfused composition's time and the
 fused-vs-unfused speedup.
@@ -491,7 +492,12 @@ def main(argv=None):
     sampler.start()
     barrier(world)
     torch.cuda.synchronize()
-    region, per_launch = time_loop(wl.fused, args.steps, stream, per_launch=True)
+    # One event pair around the region; a step is exactly one kernel launch, so
+    # the kernel's average launch duration is region / steps (conservative:
+    # gaps between launches count against it).  The unfused leg is timed the
+    # same way, so the speedup compares like with like.
+    region, _ = time_loop(wl.fused, args.steps, stream, per_launch=False)
+    per_launch = region / args.steps
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()

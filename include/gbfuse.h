@@ -125,6 +125,20 @@ GBF_API gbf_status_t w4a16_gemm(const void *A, const uint8_t *Wq, const void *sc
                         void *workspace, size_t workspace_bytes, gbf_stream_t stream);
 
 /*
+ * swiglu_pointwise -- the level-1 fused gated ending on its own:
+ *   h[M][N] = bf16( act(alpha*g) * (alpha*u) + beta*C ) from bf16 g, u, C
+ *   ("Fusion Thinking", Pattern 2, level 1: one elementwise kernel replaces
+ *   the separate sigmoid, multiply and multiply of an eager framework; SiLU
+ *   computed in fp32).  Unlike the page's snippet, silu(g) is not rounded to
+ *   bf16 before the product (one rounding at the end, as everywhere here).
+ *   g, u, C (nullable), h: [M][N] bf16, 16-byte aligned, N % 8 == 0.
+ *   HBM-bound: reads g and u (and C) once, writes h once.
+ */
+GBF_API gbf_status_t swiglu_pointwise(const void *g, const void *u, const void *C, void *h,
+                                      int64_t M, int64_t N, float alpha, float beta, int act,
+                                      gbf_stream_t stream);
+
+/*
  * Unfused reference compositions: the same results as above, computed the
  * way an eager framework does it, with the intermediate written to HBM and
  * read back by a second kernel ("kernel fusion" wiki: unfused, the product
@@ -200,6 +214,20 @@ GBF_API gbf_status_t gbf_set_wait_timeout_ns(uint64_t ns);
  * bounded wait runs out; the kernel then records GBF_ERR_TIMEOUT and exits
  * cleanly.  Off by default. */
 GBF_API gbf_status_t gbf_debug_inject_timeout(int on);
+
+/* Profiling hook: with a zeroed device buffer of `bytes` registered, each CTA
+ * of later launches (if the buffer has room for 32 counters per CTA) adds,
+ * per wait site i of its pipeline, the cycles spent waiting to counter 2i and
+ * the number of waits to counter 2i+1, and its total cycles to counter 31
+ * (unsigned 64-bit, CTA b at offset 32*b, b = linear block index).  NULL
+ * turns it off (the default).  The caller owns and clears the buffer. */
+GBF_API gbf_status_t gbf_debug_set_profile(void *counters, size_t bytes);
+
+/* Tuning hook: the split-K cluster size of the swapped small-M and W4A16
+ * kernels (1..8) for later launches, or 0 (default) for the automatic choice
+ * (about two CTAs per SM).  Changes the partition of the work, not its
+ * result beyond the order of the fp32 partial sums. */
+GBF_API gbf_status_t gbf_debug_force_splits(int splits);
 
 /* Which kernel family a call with these arguments runs (for tests and the
  * benchmark's roofline attribution): 1 = persistent 128x256-tile kernel,

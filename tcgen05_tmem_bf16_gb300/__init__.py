@@ -31,7 +31,8 @@ EXPORTS = ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unf
            "swiglu_dual_gemm_unfused", "w4a16_gemm_unfused", "gbf_workspace_size",
            "gbf_check_device_error", "gbf_status_string", "gbf_set_wait_timeout_ns",
            "gbf_debug_inject_timeout", "gbf_kernel_path", "gbf_version",
-           "gemm_epilogue_unfused_noalloc")
+           "gemm_epilogue_unfused_noalloc", "gbf_debug_force_splits", "gbf_debug_set_profile",
+           "swiglu_pointwise")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,8 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = I
+        lib.swiglu_pointwise.argtypes = [V, V, V, V, I64, I64, F, F, I, V]
+        lib.swiglu_pointwise.restype = I
         lib.gemm_epilogue_unfused_noalloc.argtypes = [V, V, I, V, V, V, V, I64, I64, I64, F, F,
                                                       I, V]
         lib.gemm_epilogue_unfused_noalloc.restype = I
@@ -83,6 +86,10 @@ def load(path: str | None = None):
         lib.gbf_set_wait_timeout_ns.restype = I
         lib.gbf_debug_inject_timeout.argtypes = [I]
         lib.gbf_debug_inject_timeout.restype = I
+        lib.gbf_debug_set_profile.argtypes = [V, SZ]
+        lib.gbf_debug_set_profile.restype = I
+        lib.gbf_debug_force_splits.argtypes = [I]
+        lib.gbf_debug_force_splits.restype = I
         lib.gbf_kernel_path.argtypes = [I, I64, I64, I64, I, ctypes.POINTER(I)]
         lib.gbf_kernel_path.restype = I
         lib.gbf_version.argtypes = []
@@ -167,6 +174,13 @@ def swiglu_dual_gemm_unfused(x, w_gate, w_up, w_layout, h, M, N, K, alpha=1.0, b
     return _check(st, "swiglu_dual_gemm_unfused", raise_on_error)
 
 
+def swiglu_pointwise(g, u, C, h, M, N, alpha=1.0, beta=0.0, act="silu", stream=None,
+                     raise_on_error=True):
+    st = load().swiglu_pointwise(_p(g), _p(u), _p(C), _p(h), M, N, alpha, beta,
+                                 _code(act, ACT), _s(stream))
+    return _check(st, "swiglu_pointwise", raise_on_error)
+
+
 def w4a16_gemm(A, Wq, scales, group_size, C, bias, residual, out, M, N, K, alpha=1.0,
                beta=0.0, act="identity", workspace=None, workspace_bytes=0, stream=None,
                raise_on_error=True):
@@ -203,6 +217,17 @@ def gbf_set_wait_timeout_ns(ns: int) -> int:
 
 def gbf_debug_inject_timeout(on: bool) -> int:
     return int(load().gbf_debug_inject_timeout(int(bool(on))))
+
+
+def gbf_debug_set_profile(counters, nbytes: int = 0) -> int:
+    """Register a zeroed device buffer for per-CTA wait-time counters (None: off)."""
+    if counters is not None and not nbytes:
+        nbytes = counters.numel() * counters.element_size()
+    return int(load().gbf_debug_set_profile(_p(counters), int(nbytes)))
+
+
+def gbf_debug_force_splits(splits: int) -> int:
+    return int(load().gbf_debug_force_splits(int(splits)))
 
 
 def gbf_kernel_path(op, M, N, K, b_layout="nk"):

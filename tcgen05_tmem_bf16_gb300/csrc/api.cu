@@ -24,6 +24,9 @@ namespace {
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject{0};
+std::atomic<int> g_force_splits{0};
+std::atomic<unsigned long long*> g_prof{nullptr};
+std::atomic<size_t> g_prof_bytes{0};
 
 constexpr int kMaxDevices = 64;
 
@@ -119,8 +122,19 @@ gbf_status_t check_ptrs(std::initializer_list<const void*> required,
   return GBF_OK;
 }
 
-KernelCtl make_ctl(unsigned* err) {
-  return KernelCtl{err, static_cast<unsigned long long>(g_timeout_ns.load()), g_inject.load()};
+// Launch control; the wait-time counters are passed only when the
+// registered buffer has room for every CTA of the launch.
+KernelCtl make_ctl(unsigned* err, int64_t ctas) {
+  unsigned long long* prof = g_prof.load();
+  if (prof && static_cast<size_t>(ctas) * kProfSlots * 8 > g_prof_bytes.load()) prof = nullptr;
+  return KernelCtl{err, static_cast<unsigned long long>(g_timeout_ns.load()), g_inject.load(),
+                   prof};
+}
+
+int64_t plan_ctas(const GemmPlan& p) {
+  if (p.path == kPathSwap || p.path == kPathW4)
+    return static_cast<int64_t>(p.splits) * p.n_tiles * p.m_tiles;
+  return p.grid;
 }
 
 gbf_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? GBF_OK : GBF_ERR_CUDA; }
@@ -137,6 +151,7 @@ int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 int choose_splits(int tiles, int num_kb, const DeviceInfo& dev) {
   const int slots = dev.sms * 2;  // the swapped kernels fit two CTAs per SM
   int s = tiles > 0 ? slots / tiles : 1;
+  if (const int f = g_force_splits.load()) s = f;
   s = std::max(1, std::min(s, kMaxSplits));
   s = std::min(s, std::max(1, num_kb));
   return s;
@@ -181,11 +196,11 @@ gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, 
   }
   if (pair)
     return cuda_status(launch_gemm_pair(plan, kn, dual, tmA, tmW, tmW2, ep, static_cast<int>(M),
-                                        static_cast<int>(N), static_cast<int>(K), make_ctl(err),
-                                        stream));
+                                        static_cast<int>(N), static_cast<int>(K),
+                                        make_ctl(err, plan_ctas(plan)), stream));
   return cuda_status(launch_gemm(plan, kn, dual, tmA, tmW, tmW2, ep, static_cast<int>(M),
-                                 static_cast<int>(N), static_cast<int>(K), make_ctl(err),
-                                 stream));
+                                 static_cast<int>(N), static_cast<int>(K),
+                                 make_ctl(err, plan_ctas(plan)), stream));
 }
 
 gbf_status_t run_w4(const void* A, const uint8_t* Wq, const void* scales, int group,
@@ -203,8 +218,8 @@ gbf_status_t run_w4(const void* A, const uint8_t* Wq, const void* scales, int gr
                CU_TENSOR_MAP_SWIZZLE_NONE))
     return GBF_ERR_CUDA;
   return cuda_status(launch_w4a16(plan, tmA, tmQ, tmS, ep, static_cast<int>(M),
-                                  static_cast<int>(N), static_cast<int>(K), group, make_ctl(err),
-                                  stream));
+                                  static_cast<int>(N), static_cast<int>(K), group,
+                                  make_ctl(err, plan_ctas(plan)), stream));
 }
 
 gbf_status_t check_w4(int64_t M, int64_t N, int64_t K, int group, int act) {
@@ -322,6 +337,21 @@ gbf_status_t w4a16_gemm(const void* A, const uint8_t* Wq, const void* scales, in
   if ((st = current_device(&dev, &err)) != GBF_OK) return st;
   return run_w4(A, Wq, scales, group_size, make_ep(C, bias, residual, out, alpha, beta, act), M,
                 N, K, *dev, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gbf_status_t swiglu_pointwise(const void* g, const void* u, const void* C, void* h, int64_t M,
+                              int64_t N, float alpha, float beta, int act, gbf_stream_t stream) {
+  gbf_status_t st = check_common(M, N, 8, act);
+  if (st != GBF_OK) return st;
+  if ((st = check_ptrs({g, u, h}, {C})) != GBF_OK) return st;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || N == 0) return GBF_OK;
+  return cuda_status(launch_swiglu_pointwise(
+      static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(u),
+      make_ep(C, nullptr, nullptr, h, alpha, beta, act), M, N, dev->sms,
+      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t gbf_workspace_size(int op, int64_t M, int64_t N, int64_t K, int fused) {
@@ -455,6 +485,18 @@ gbf_status_t gbf_set_wait_timeout_ns(uint64_t ns) {
 
 gbf_status_t gbf_debug_inject_timeout(int on) {
   g_inject.store(on ? 1 : 0);
+  return GBF_OK;
+}
+
+gbf_status_t gbf_debug_set_profile(void* counters, size_t bytes) {
+  g_prof_bytes.store(counters ? bytes : 0);
+  g_prof.store(static_cast<unsigned long long*>(counters));
+  return GBF_OK;
+}
+
+gbf_status_t gbf_debug_force_splits(int splits) {
+  if (splits < 0 || splits > kMaxSplits) return GBF_ERR_INVALID_ARG;
+  g_force_splits.store(splits);
   return GBF_OK;
 }
 

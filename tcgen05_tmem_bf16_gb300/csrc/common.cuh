@@ -30,14 +30,23 @@ struct WaitCtl {
   unsigned* err;          // device error word (global)
   uint64_t timeout_ns;    // limit of one wait
   volatile int* abort;    // shared flag: some role of this CTA gave up
+  unsigned long long* prof = nullptr;  // this CTA's wait counters, or null
 };
+
+// Wait-time profiling (off unless a buffer is registered): lane 0 of each
+// waiting warp adds the cycles it spent in a wait to its site's counter.
+__device__ __forceinline__ unsigned long long* prof_slots(unsigned long long* prof) {
+  if (!prof) return nullptr;
+  const unsigned bid = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  return prof + static_cast<size_t>(bid) * 32;
+}
 
 // Wait until phase `parity` of `bar` has completed, for at most
 // ctl.timeout_ns.  On expiry, records the site in the error word, raises the
 // CTA's abort flag and returns false.  With honor_abort, returns false as
 // soon as another role of the CTA has given up.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
-                                         unsigned site, bool honor_abort = true) {
+__device__ __forceinline__ bool wait_bar_impl(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
+                                              unsigned site, bool honor_abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   // The clock and the abort flag are checked every 64 polls only, so that a
@@ -54,6 +63,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const W
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const WaitCtl& ctl,
+                                         unsigned site, bool honor_abort = true) {
+  if (!ctl.prof) return wait_bar_impl(bar, parity, ctl, site, honor_abort);
+  const long long c0 = clock64();
+  const bool ok = wait_bar_impl(bar, parity, ctl, site, honor_abort);
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&ctl.prof[2 * site], static_cast<unsigned long long>(clock64() - c0));
+    atomicAdd(&ctl.prof[2 * site + 1], 1ull);
+  }
+  return ok;
 }
 
 // ---------------------------------------------------------------- epilogue math

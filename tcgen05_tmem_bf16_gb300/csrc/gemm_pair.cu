@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag};
+  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
+  const long long t_start = clock64();
   const int num_tiles = a.m_tiles * a.n_tiles;
   const int num_kb = a.num_kb;
   const int out_bn = DUAL ? 128 : BN;
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
   }
 
+  if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no CTA leaves while its peer may still signal it or read its memory

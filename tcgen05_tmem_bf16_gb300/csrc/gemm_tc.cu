@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag};
+  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
+  const long long t_start = clock64();
   const int num_tiles = a.m_tiles * a.n_tiles;
   const int num_kb = a.num_kb;
   const int out_bn = DUAL ? 128 : 256;
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
   }
 
+  if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
@@ -259,13 +261,36 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 // ============================================================ swapped small-M kernel
 
+// Sum of the NACC accumulators (spaced MPAD columns apart) for 16 columns of
+// this thread's lane, accumulator 0 first.
+template <int NACC, int MPAD>
+__device__ __forceinline__ void acc_sum16(uint32_t taddr, float (&out)[16]) {
+  uint32_t r[16];
+  tmem_ld16(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) out[j] = __uint_as_float(r[j]);
+#pragma unroll
+  for (int a = 1; a < NACC; ++a) {
+    tmem_ld16(taddr + a * MPAD, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) out[j] += __uint_as_float(r[j]);
+  }
+}
+
 template <int MPAD>
 struct SwapCfg {
   static constexpr int kWBytes = kSwapBN * kBK * 2;          // 16 KB weight tile
   static constexpr int kXBytes = MPAD * kBK * 2;             // activation tile
   static constexpr int kStageBytes = kWBytes + kXBytes;
   static constexpr int kStages = MPAD <= 32 ? 5 : (MPAD <= 64 ? 4 : 3);
-  static constexpr uint32_t kTmemCols = MPAD < 32 ? 32 : MPAD;
+  // Consecutive 16-deep K steps go to kAcc accumulators in turn: with a
+  // narrow MMA (N = MPAD) the time per MMA is set by the accumulator's
+  // read-after-write chain, not by its arithmetic, so independent chains
+  // multiply the MMA rate; the epilogue sums them in a fixed order.
+  static constexpr int kAcc = MPAD <= 32 ? 4 : 2;
+  static constexpr uint32_t kTmemCols = kAcc * MPAD <= 64 ? 64 : (kAcc * MPAD <= 128 ? 128 : 256);
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
   static_assert(kStages * kStageBytes >= 128 * MPAD * 4, "reduction buffer must fit");
 };
@@ -322,7 +347,8 @@ __global__ void __launch_bounds__(256, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag};
+  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
+  const long long t_start = clock64();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -372,7 +398,8 @@ __global__ void __launch_bounds__(256, 2)
           const uint64_t ad = W_KN ? sdesc_sw128(w0 + k * 2048, 8192, 1024)
                                    : sdesc_sw128(w0 + k * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(x0 + k * 32, 16, 1024);
-          mma_ss(tmem_base, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+          const int j = (kb - kb0) * (kBK / kUK) + k;  // K step within this CTA's range
+          mma_ss(tmem_base + (j % Cfg::kAcc) * MPAD, ad, bd, idesc, j >= Cfg::kAcc ? 1u : 0u);
         }
         mma_commit(&empty[s]);
         if (++s == Cfg::kStages) {
@@ -412,14 +439,11 @@ __global__ void __launch_bounds__(256, 2)
     if (S > 1) {
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
-        uint32_t r[16];
-        tmem_ld16(tb + c * 16, r);
-        tmem_wait_ld();
+        float r[16];
+        acc_sum16<Cfg::kAcc, MPAD>(tb + c * 16, r);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-          red[(c * 4 + v) * 128 + tid] =
-              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          red[(c * 4 + v) * 128 + tid] = make_float4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
       }
     }
   }
@@ -431,11 +455,10 @@ __global__ void __launch_bounds__(256, 2)
         col16_prefetch(L, static_cast<int64_t>(mb) * MPAD + c * 16, n, a.M, a.N, a.ep, pol);
       float v[16];
       if (S == 1) {
-        uint32_t r[16];
-        tmem_ld16(tb + c * 16, r);
-        tmem_wait_ld();
+        float r[16];
+        acc_sum16<Cfg::kAcc, MPAD>(tb + c * 16, r);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = have ? __uint_as_float(r[j]) : 0.0f;
+        for (int j = 0; j < 16; ++j) v[j] = have ? r[j] : 0.0f;
       } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = 0.0f;
@@ -467,6 +490,7 @@ __global__ void __launch_bounds__(256, 2)
   }
   if (S > 1) cluster_sync_all();
 
+  if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {

@@ -27,7 +27,9 @@ struct KernelCtl {
   unsigned* err;
   unsigned long long timeout_ns;
   int inject;
+  unsigned long long* prof;  // per-CTA wait-time counters (kProfSlots each) or null
 };
+constexpr int kProfSlots = 32;  // [2*site] cycles waited, [2*site+1] waits; [31] CTA cycles
 
 // Kernel families (gbf_kernel_path codes).
 enum Path { kPathNone = 0, kPathPersistent = 1, kPathSwap = 2, kPathW4 = 3, kPathPair = 4 };

@@ -62,7 +62,12 @@ struct W4Cfg {
   static constexpr int kStages = MPAD <= 16 ? 5 : 4;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
   static constexpr uint32_t kTmemCols = 256;
-  static constexpr uint32_t kColA = kW4Regions * MPAD;  // D region r at r*MPAD
+  // Accumulator sets: the 16-deep K steps alternate between kSets copies of
+  // the four region accumulators, so that 4*kSets independent accumulation
+  // chains are in flight (a narrow MMA's time is set by its accumulator's
+  // read-after-write chain); the epilogue adds the sets, set 0 first.
+  static constexpr int kSets = MPAD <= 16 ? 2 : 1;
+  static constexpr uint32_t kColA = kSets * kW4Regions * MPAD;  // D(set e, region r) at (4e+r)*MPAD
   // A buffer of group g at kColA + 64g; region r at +16r (16 columns = 32 k).
   static_assert(kColA + 128 <= kTmemCols, "TMEM budget");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
@@ -203,7 +208,8 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag};
+  const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
+  const long long t_start = clock64();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -259,10 +265,13 @@ __global__ void __launch_bounds__(kW4Threads, 2)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const uint64_t bd = sdesc_sw128(x0 + (2 * g + k) * 32, 16, 1024);
-            const uint32_t accum = (kb != kb0 || g != 0 || k != 0) ? 1u : 0u;
+            const int j = (kb - kb0) * 4 + 2 * g + k;  // K step within this CTA's range
+            const int e = j % Cfg::kSets;
+            const uint32_t accum = j >= Cfg::kSets ? 1u : 0u;
 #pragma unroll
             for (int r = 0; r < kW4Regions; ++r)
-              mma_ts(tmem_base + r * MPAD, abuf + 16 * r + 8 * k, bd, idesc, accum);
+              mma_ts(tmem_base + (e * kW4Regions + r) * MPAD, abuf + 16 * r + 8 * k, bd, idesc,
+                     accum);
           }
           mma_commit(&aempty[g]);
         }
@@ -350,14 +359,21 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       for (int r = 0; r < kW4Regions; ++r) {
 #pragma unroll 1
         for (int c = 0; c < MPAD / 16; ++c) {
-          uint32_t v[16];
-          tmem_ld16(tb + r * MPAD + c * 16, v);
-          tmem_wait_ld();
+          float v[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) v[jj] = 0.0f;
+#pragma unroll
+          for (int e = 0; e < Cfg::kSets; ++e) {
+            uint32_t u[16];
+            tmem_ld16(tb + (e * kW4Regions + r) * MPAD + c * 16, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) v[jj] += __uint_as_float(u[jj]);
+          }
 #pragma unroll
           for (int w = 0; w < 4; ++w)
             red[((r * (MPAD / 4)) + c * 4 + w) * 128 + tid] =
-                make_float4(__uint_as_float(v[4 * w]), __uint_as_float(v[4 * w + 1]),
-                            __uint_as_float(v[4 * w + 2]), __uint_as_float(v[4 * w + 3]));
+                make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
         }
       }
     }
@@ -372,11 +388,16 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       if (S == 1) {
 #pragma unroll
         for (int r = 0; r < kW4Regions; ++r) {
-          uint32_t u[8];
-          tmem_ld8(tb + r * MPAD + c * 8, u);
-          tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[r][j] = have ? __uint_as_float(u[j]) : 0.0f;
+          for (int j = 0; j < 8; ++j) v[r][j] = 0.0f;
+#pragma unroll
+          for (int e = 0; e < Cfg::kSets; ++e) {
+            uint32_t u[8];
+            tmem_ld8(tb + (e * kW4Regions + r) * MPAD + c * 8, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[r][j] += have ? __uint_as_float(u[j]) : 0.0f;
+          }
         }
       } else {
 #pragma unroll
@@ -412,6 +433,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   }
   if (S > 1) cluster_sync_all();
 
+  if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
