@@ -51,6 +51,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1024 * 1024
 
 WORKLOAD_TEXT = {
+    "add_rmsnorm": "fused residual add + RMSNorm, a,x[4096x4096] bf16, eps 1e-5",
+    "swiglu_pointwise": "level-1 fused SwiGLU ending, g,u[2048x14336] bf16 (vs eager sigmoid/mul/mul)",
     "prefill": "prefill projection A[4096x4096] x W[4096x4096]^T + bias + residual, bf16",
     "swiglu": "gate/up SwiGLU dual GEMM x[2048x4096], Wg,Wu[14336x4096], bf16",
     "w4a16": "W4A16 decode GEMM A[16x8192] x int4 W[8192x28672], group 128",
@@ -188,6 +190,8 @@ class ClockSampler:
 
 def describe(w: dict) -> dict:
     d = {"M": w["M"], "N": w["N"], "K": w["K"], "op": w["op"]}
+    if "eps" in w:
+        d["eps"] = w["eps"]
     if "layout" in w:
         d["b_layout"] = w["layout"]
     if w["op"] == "w4a16":
@@ -225,7 +229,8 @@ class Workload:
         self.M, self.N, self.K = w["M"], w["N"], w["K"]
         self.counts = roofline.counts_for(w)
         host = {}
-        for key in ("A", "B", "C", "bias", "residual", "x", "w_gate", "w_up", "Wq", "scales"):
+        for key in ("A", "B", "C", "bias", "residual", "x", "w_gate", "w_up", "Wq", "scales",
+                    "a", "weight", "g", "u"):
             if w.get(key) is not None:
                 host[key] = w[key]
         self.host_np = host
@@ -242,10 +247,11 @@ class Workload:
         for _ in range(self.n_sets):
             d = {k: up(v) for k, v in host.items()}
             d["out"] = torch.empty(self.M, self.N, dtype=torch.bfloat16, device=dev)
+            if self.op == "add_rmsnorm":
+                d["resid"] = torch.empty(self.M, self.N, dtype=torch.bfloat16, device=dev)
             self.sets.append(d)
-        ws = gbf.gbf_workspace_size(
-            {"gemm": "gemm_epilogue", "swiglu": "swiglu", "w4a16": "w4a16"}[self.op],
-            self.M, self.N, self.K, False)
+        gemm_op = {"gemm": "gemm_epilogue", "swiglu": "swiglu", "w4a16": "w4a16"}.get(self.op)
+        ws = gbf.gbf_workspace_size(gemm_op, self.M, self.N, self.K, False) if gemm_op else 0
         self.ws_bytes = ws
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
         # pinned host buffers for the end-to-end leg
@@ -253,9 +259,11 @@ class Workload:
         self.pinned_out = torch.empty(self.M * self.N * 2, dtype=torch.uint8).pin_memory()
         self.h2d_bytes = sum(v.nbytes for v in host.values())
         self.d2h_bytes = self.M * self.N * 2
-        self.path, self.splits = gbf.gbf_kernel_path(
-            {"gemm": "gemm_epilogue", "swiglu": "swiglu", "w4a16": "w4a16"}[self.op],
-            self.M, self.N, self.K, w.get("layout", "kn"))
+        if gemm_op:
+            self.path, self.splits = gbf.gbf_kernel_path(gemm_op, self.M, self.N, self.K,
+                                                         w.get("layout", "kn"))
+        else:
+            self.path, self.splits = self.op, 1
 
     def describe(self) -> dict:
         return describe(self.w)
@@ -271,10 +279,16 @@ class Workload:
             gbf.swiglu_dual_gemm(s["x"], s["w_gate"], s["w_up"], w["layout"], s["out"], self.M,
                                  self.N, self.K, w["alpha"], w["beta"], s.get("C"), w["act"],
                                  stream=stream)
-        else:
+        elif self.op == "w4a16":
             gbf.w4a16_gemm(s["A"], s["Wq"], s["scales"], w["group"], s.get("C"), s.get("bias"),
                            s.get("residual"), s["out"], self.M, self.N, self.K, w["alpha"],
                            w["beta"], w["act"], stream=stream)
+        elif self.op == "add_rmsnorm":
+            gbf.add_rmsnorm(s["a"], s["x"], s["weight"], s["out"], s["resid"], self.M, self.N,
+                            w["eps"], stream=stream)
+        else:
+            gbf.swiglu_pointwise(s["g"], s["u"], None, s["out"], self.M, self.N, w["alpha"],
+                                 w["beta"], w["act"], stream=stream)
 
     def unfused(self, i: int, stream=None):
         s = self.sets[i % self.n_sets]
@@ -288,13 +302,26 @@ class Workload:
             gbf.swiglu_dual_gemm_unfused(s["x"], s["w_gate"], s["w_up"], w["layout"], s["out"],
                                          self.M, self.N, self.K, w["alpha"], w["beta"],
                                          s.get("C"), w["act"], **kw)
-        else:
+        elif self.op == "w4a16":
             gbf.w4a16_gemm_unfused(s["A"], s["Wq"], s["scales"], w["group"], s.get("C"),
                                    s.get("bias"), s.get("residual"), s["out"], self.M, self.N,
                                    self.K, w["alpha"], w["beta"], w["act"], **kw)
+        elif self.op == "add_rmsnorm":
+            gbf.add_rmsnorm_unfused(s["a"], s["x"], s["weight"], s["out"], s["resid"], self.M,
+                                    self.N, w["eps"], stream=stream)
+        else:
+            # the eager composition the level-1 kernel replaces: sigmoid, mul, mul
+            g, u = s["g"], s["u"]
+            torch = self.torch
+            torch.mul(torch.mul(g, torch.sigmoid(g)), u, out=s["out"])
 
-    def unfused_launches(self) -> int:
-        return 2 if self.op != "swiglu" else 3
+    def unfused_kind(self) -> str:
+        if self.op == "swiglu_pointwise":
+            return "eager torch: sigmoid, mul, mul (3 kernels)"
+        return {"gemm": "GEMM -> bf16 D in HBM -> pointwise kernel",
+                "swiglu": "two GEMMs -> bf16 g, u in HBM -> GLU pointwise kernel",
+                "w4a16": "dequantise kernel -> bf16 W in HBM -> bf16 GEMM",
+                "add_rmsnorm": "residual-add kernel -> bf16 r in HBM -> RMSNorm kernel"}[self.op]
 
     def e2e_step(self, stream):
         """Host->device copy of the step's inputs, the call, device->host copy
@@ -338,24 +365,46 @@ def time_loop(fn, steps: int, stream, per_launch: bool):
 # ---------------------------------------------------------------- CPU (oracle) legs
 
 def oracle_elements(w: dict, rows, cols):
+    """The oracle on the given output positions (row-wise ops: on the rows
+    they belong to).  Returns the number of output elements computed."""
+    import numpy as np
     import oracle
     op = w["op"]
     M, N, K = w["M"], w["N"], w["K"]
+    if op in ("add_rmsnorm", "swiglu_pointwise"):
+        r = np.unique(np.asarray(rows) % M)
+        if op == "add_rmsnorm":
+            oracle.add_rmsnorm(w["a"][r], w["x"][r], w["weight"], M=r.size, N=N, eps=w["eps"])
+        else:
+            oracle.swiglu_pointwise(w["g"][r], w["u"][r], M=r.size, N=N, alpha=w["alpha"],
+                                    beta=w["beta"], act=w["act"])
+        return r.size * N
     if op == "gemm":
-        return oracle.gemm_epilogue(w["A"], w["B"], w["layout"], w.get("C"), w.get("bias"),
-                                    w.get("residual"), M=M, N=N, K=K, alpha=w["alpha"],
-                                    beta=w["beta"], act=w["act"], rows=rows, cols=cols)
-    if op == "swiglu":
-        return oracle.swiglu(w["x"], w["w_gate"], w["w_up"], w["layout"], w.get("C"), M=M, N=N,
-                             K=K, alpha=w["alpha"], beta=w["beta"], act=w["act"], rows=rows,
-                             cols=cols)
-    return oracle.w4a16(w["A"], w["Wq"], w["scales"], w["group"], w.get("C"), w.get("bias"),
-                        w.get("residual"), M=M, N=N, K=K, alpha=w["alpha"], beta=w["beta"],
-                        act=w["act"], rows=rows, cols=cols)
+        oracle.gemm_epilogue(w["A"], w["B"], w["layout"], w.get("C"), w.get("bias"),
+                             w.get("residual"), M=M, N=N, K=K, alpha=w["alpha"],
+                             beta=w["beta"], act=w["act"], rows=rows, cols=cols)
+    elif op == "swiglu":
+        oracle.swiglu(w["x"], w["w_gate"], w["w_up"], w["layout"], w.get("C"), M=M, N=N,
+                      K=K, alpha=w["alpha"], beta=w["beta"], act=w["act"], rows=rows,
+                      cols=cols)
+    else:
+        oracle.w4a16(w["A"], w["Wq"], w["scales"], w["group"], w.get("C"), w.get("bias"),
+                     w.get("residual"), M=M, N=N, K=K, alpha=w["alpha"], beta=w["beta"],
+                     act=w["act"], rows=rows, cols=cols)
+    return len(rows)
 
 
-def flops_per_element(w: dict) -> float:
-    return (4.0 if w["op"] == "swiglu" else 2.0) * w["K"]
+def metric_per_element(w: dict):
+    """(units of the workload's metric per output element, unit): algorithmic
+    FLOPs (TFLOP/s) for tensor-bound workloads, algorithmic bytes (GB/s) for
+    HBM-bound ones, spread evenly over the M*N outputs."""
+    from tcgen05_tmem_bf16_gb300 import roofline as rf
+    peaks, _ = load_peaks()
+    c = rf.counts_for(w)
+    per = 1.0 / (w["M"] * w["N"])
+    if rf.bound(c, peaks["bf16_tflops"], peaks["hbm_gbs"]) == "tensor":
+        return c.flops * per / 1e12, "TFLOP/s"
+    return c.fused_bytes * per / 1e9, "GB/s"
 
 
 def cpu_baseline(w: dict, seconds: float = 12.0) -> dict:
@@ -364,18 +413,18 @@ def cpu_baseline(w: dict, seconds: float = 12.0) -> dict:
     import numpy as np
     import workloads
     rows, cols = workloads.sample_indices(w["M"], w["N"], 1 << 20, seed=0xBEEF)
-    done, t0, batch = 0, time.perf_counter(), 64
+    pos, done, t0, batch = 0, 0, time.perf_counter(), 64
     while True:
-        oracle_elements(w, rows[done:done + batch], cols[done:done + batch])
-        done += batch
+        done += oracle_elements(w, rows[pos:pos + batch], cols[pos:pos + batch])
+        pos += batch
         el = time.perf_counter() - t0
-        if el >= seconds or done + batch > rows.size:
+        if el >= seconds or pos + batch > rows.size:
             break
         batch = min(batch * 2, 4096)
-    tflops = done * flops_per_element(w) / el / 1e12
-    return {"value": tflops, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} seeded output elements of the {w['M']}x{w['N']}x{w['K']} "
-                      f"workload ({el:.1f} s, single-threaded fp64 C oracle)"}
+    per, unit = metric_per_element(w)
+    return {"value": done * per / el, "unit": unit, "cores": 1, "kind": "oracle",
+            "sample": f"{done} output elements of the {w['M']}x{w['N']}x{w['K']} workload at "
+                      f"seeded positions ({el:.1f} s, single-threaded fp64 C oracle)"}
 
 
 def run_reference(args, workload_name):
@@ -390,37 +439,40 @@ def run_reference(args, workload_name):
          if workload_name.startswith("sweep-") else workloads.make(workload_name))
     rows, cols = workloads.sample_indices(w["M"], w["N"], 1 << 16, seed=0xFACE)
     t0 = time.perf_counter()
-    oracle_elements(w, rows[:32], cols[:32])
-    per_elem = max((time.perf_counter() - t0) / 32, 1e-7)
+    n0 = oracle_elements(w, rows[:32], cols[:32])
+    per_elem = max((time.perf_counter() - t0) / n0, 1e-9)
     budget = 90.0 / max(1, args.steps + args.warmup)
     per_step = int(max(1, min(rows.size // 2, budget / per_elem)))
-    pos = 0
+    if w["op"] in ("add_rmsnorm", "swiglu_pointwise"):
+        per_step = max(1, per_step // w["N"])  # rows per step
+    pos, done = 0, 0
 
     def step():
-        nonlocal pos
+        nonlocal pos, done
         if pos + per_step > rows.size:
             pos = 0
-        oracle_elements(w, rows[pos:pos + per_step], cols[pos:pos + per_step])
+        done += oracle_elements(w, rows[pos:pos + per_step], cols[pos:pos + per_step])
         pos += per_step
 
     for _ in range(args.warmup):
         step()
+    done = 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    flops = args.steps * per_step * flops_per_element(w)
-    value = flops / el / 1e12
-    sample = (f"{per_step} seeded output elements per step of the {w['M']}x{w['N']}x{w['K']} "
-              f"workload, single-threaded fp64 C oracle")
-    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+    per, unit = metric_per_element(w)
+    value = done * per / el
+    sample = (f"{done // args.steps} output elements per step at seeded positions of the "
+              f"{w['M']}x{w['N']}x{w['K']} workload, single-threaded fp64 C oracle")
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
             "config": config_of(workload_name, w, max(1, args.gpus)),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -501,10 +553,16 @@ def main(argv=None):
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
-    max_region, total_flops = aggregate(region, wl.counts.flops * args.steps, world)
+    from tcgen05_tmem_bf16_gb300 import roofline as rf
+    bnd = rf.bound(wl.counts, peaks["bf16_tflops"], peaks["hbm_gbs"])
+    # the workload's metric: TFLOP/s when tensor-bound, GB/s of algorithmic
+    # bytes when HBM-bound
+    per_step, vscale, vunit = ((wl.counts.flops, 1e12, "TFLOP/s") if bnd == "tensor"
+                               else (wl.counts.fused_bytes, 1e9, "GB/s"))
+    max_region, total_units = aggregate(region, per_step * args.steps, world)
     if gbf.gbf_check_device_error() != 0:
         raise SystemExit("kernel reported a timeout in the timed region")
-    value = total_flops / max_region / 1e12
+    value = total_units / max_region / vscale
 
     # unfused composition, same workload, same rotation of input sets
     for i in range(3):
@@ -520,11 +578,9 @@ def main(argv=None):
     torch.cuda.synchronize()
     e2e_region, _ = time_loop(lambda i: wl.e2e_step(stream), args.e2e_steps, stream,
                               per_launch=False)
-    e2e_max, e2e_flops = aggregate(e2e_region, wl.counts.flops * args.e2e_steps, world)
+    e2e_max, e2e_units = aggregate(e2e_region, per_step * args.e2e_steps, world)
 
     # roofline of the dominant (only) kernel of the step
-    from tcgen05_tmem_bf16_gb300 import roofline as rf
-    bnd = rf.bound(wl.counts, peaks["bf16_tflops"], peaks["hbm_gbs"])
     long_loop = region > 0.5
     if bnd == "tensor":
         achieved = wl.counts.flops / per_launch / 1e12
@@ -551,7 +607,7 @@ def main(argv=None):
         roof["frac_of_burst_peak"] = achieved / peaks["bf16_tflops"]
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": vunit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": fu_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
@@ -561,8 +617,9 @@ def main(argv=None):
         "impl": "gbfuse",
         "roofline": roof,
         "unfused_ms_per_step": un_ms,
+        "unfused_kind": wl.unfused_kind(),
         "speedup_vs_unfused": un_ms / fu_ms,
-        "e2e": {"value": e2e_flops / e2e_max / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": e2e_units / e2e_max / vscale, "unit": vunit,
                 "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
         "gpu_launches": args.steps,
         "clocks": clocks,

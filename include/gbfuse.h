@@ -139,6 +139,27 @@ GBF_API gbf_status_t swiglu_pointwise(const void *g, const void *u, const void *
                                       gbf_stream_t stream);
 
 /*
+ * add_rmsnorm -- fused residual add + RMSNorm, per row m:
+ *   r = a + x (fp32);  out_resid = bf16(r);
+ *   out_norm = bf16( r * rsqrt(mean_j(r_j^2) + eps) * weight )
+ *   ("Fusion Thinking", Pattern 1, Fused RMSNorm + residual: one pass reads
+ *   attn_out and x once, writes the residual for the next add and the
+ *   normalised tensor).  The norm uses the unrounded fp32 sum.
+ *   a, x: [M][N] bf16; weight: [N] bf16; out_norm, out_resid: [M][N] bf16
+ *   (out_resid may be NULL: not written).  N % 8 == 0 and N <= 16384; eps >= 0.
+ *   HBM-bound: reads a and x once, writes each result once.
+ * add_rmsnorm_unfused -- the same as two kernels: bf16(a + x) written to
+ *   out_resid (required), then an RMSNorm kernel that reads it back
+ *   ("x = x + a; rmsnorm(x)"); the norm is then taken of the bf16 residual.
+ */
+GBF_API gbf_status_t add_rmsnorm(const void *a, const void *x, const void *weight, void *out_norm,
+                                 void *out_resid, int64_t M, int64_t N, float eps,
+                                 gbf_stream_t stream);
+GBF_API gbf_status_t add_rmsnorm_unfused(const void *a, const void *x, const void *weight,
+                                         void *out_norm, void *out_resid, int64_t M, int64_t N,
+                                         float eps, gbf_stream_t stream);
+
+/*
  * Unfused reference compositions: the same results as above, computed the
  * way an eager framework does it, with the intermediate written to HBM and
  * read back by a second kernel ("kernel fusion" wiki: unfused, the product

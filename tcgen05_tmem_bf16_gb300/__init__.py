@@ -32,7 +32,7 @@ EXPORTS = ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unf
            "gbf_check_device_error", "gbf_status_string", "gbf_set_wait_timeout_ns",
            "gbf_debug_inject_timeout", "gbf_kernel_path", "gbf_version",
            "gemm_epilogue_unfused_noalloc", "gbf_debug_force_splits", "gbf_debug_set_profile",
-           "swiglu_pointwise")
+           "swiglu_pointwise", "add_rmsnorm", "add_rmsnorm_unfused")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +70,10 @@ def load(path: str | None = None):
                            ("w4a16_gemm", w4_args), ("w4a16_gemm_unfused", w4_args)):
             fn = getattr(lib, name)
             fn.argtypes = args
+            fn.restype = I
+        for name in ("add_rmsnorm", "add_rmsnorm_unfused"):
+            fn = getattr(lib, name)
+            fn.argtypes = [V, V, V, V, V, I64, I64, F, V]
             fn.restype = I
         lib.swiglu_pointwise.argtypes = [V, V, V, V, I64, I64, F, F, I, V]
         lib.swiglu_pointwise.restype = I
@@ -179,6 +183,20 @@ def swiglu_pointwise(g, u, C, h, M, N, alpha=1.0, beta=0.0, act="silu", stream=N
     st = load().swiglu_pointwise(_p(g), _p(u), _p(C), _p(h), M, N, alpha, beta,
                                  _code(act, ACT), _s(stream))
     return _check(st, "swiglu_pointwise", raise_on_error)
+
+
+def add_rmsnorm(a, x, weight, out_norm, out_resid, M, N, eps=1e-5, stream=None,
+                raise_on_error=True):
+    st = load().add_rmsnorm(_p(a), _p(x), _p(weight), _p(out_norm), _p(out_resid), M, N, eps,
+                            _s(stream))
+    return _check(st, "add_rmsnorm", raise_on_error)
+
+
+def add_rmsnorm_unfused(a, x, weight, out_norm, out_resid, M, N, eps=1e-5, stream=None,
+                        raise_on_error=True):
+    st = load().add_rmsnorm_unfused(_p(a), _p(x), _p(weight), _p(out_norm), _p(out_resid), M, N,
+                                    eps, _s(stream))
+    return _check(st, "add_rmsnorm_unfused", raise_on_error)
 
 
 def w4a16_gemm(A, Wq, scales, group_size, C, bias, residual, out, M, N, K, alpha=1.0,

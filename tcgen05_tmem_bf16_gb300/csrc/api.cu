@@ -354,6 +354,55 @@ gbf_status_t swiglu_pointwise(const void* g, const void* u, const void* C, void*
       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+gbf_status_t check_rms(const void* a, const void* x, const void* w, const void* norm,
+                       const void* resid, int64_t M, int64_t N, float eps, bool need_resid) {
+  if (M < 0 || N < 0 || !(eps >= 0.0f)) return GBF_ERR_INVALID_ARG;
+  if (need_resid && !resid) return GBF_ERR_INVALID_ARG;
+  gbf_status_t st = check_ptrs({a, x, w, norm}, {resid});
+  if (st != GBF_OK) return st;
+  if (N % 8 != 0 || N > kRmsMaxN || M > kMaxDim) return GBF_ERR_UNSUPPORTED_SHAPE;
+  return GBF_OK;
+}
+}  // namespace
+
+gbf_status_t add_rmsnorm(const void* a, const void* x, const void* weight, void* out_norm,
+                         void* out_resid, int64_t M, int64_t N, float eps, gbf_stream_t stream) {
+  gbf_status_t st = check_rms(a, x, weight, out_norm, out_resid, M, N, eps, false);
+  if (st != GBF_OK) return st;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || N == 0) return GBF_OK;
+  return cuda_status(launch_add_rmsnorm(
+      static_cast<const __nv_bfloat16*>(a), static_cast<const __nv_bfloat16*>(x),
+      static_cast<const __nv_bfloat16*>(weight), static_cast<__nv_bfloat16*>(out_norm),
+      static_cast<__nv_bfloat16*>(out_resid), M, static_cast<int>(N), eps, dev->sms,
+      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gbf_status_t add_rmsnorm_unfused(const void* a, const void* x, const void* weight,
+                                 void* out_norm, void* out_resid, int64_t M, int64_t N,
+                                 float eps, gbf_stream_t stream) {
+  gbf_status_t st = check_rms(a, x, weight, out_norm, out_resid, M, N, eps, true);
+  if (st != GBF_OK) return st;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || N == 0) return GBF_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // kernel 1: the residual add, bf16(a + x) written to out_resid
+  const EpiParams add = make_ep(nullptr, nullptr, x, out_resid, 1.0f, 0.0f, GBF_ACT_IDENTITY);
+  if ((st = cuda_status(launch_pointwise_epilogue(static_cast<const __nv_bfloat16*>(a), add, M,
+                                                  N, dev->sms, s))) != GBF_OK)
+    return st;
+  // kernel 2: RMSNorm of the stored residual
+  return cuda_status(launch_add_rmsnorm(static_cast<const __nv_bfloat16*>(out_resid), nullptr,
+                                        static_cast<const __nv_bfloat16*>(weight),
+                                        static_cast<__nv_bfloat16*>(out_norm), nullptr, M,
+                                        static_cast<int>(N), eps, dev->sms, s));
+}
+
 size_t gbf_workspace_size(int op, int64_t M, int64_t N, int64_t K, int fused) {
   if (fused || M < 0 || N < 0 || K < 0) return 0;
   switch (op) {

@@ -88,6 +88,14 @@ cudaError_t launch_dequant_int4(const uint8_t* Wq, const __nv_bfloat16* scales, 
                                 int64_t K, int64_t N, __nv_bfloat16* w, int sms,
                                 cudaStream_t stream);
 
+// Fused residual add + RMSNorm (rmsnorm.cu).  x == null: no add (plain
+// RMSNorm of a); resid == null: the residual is not written.  N <= 16384.
+cudaError_t launch_add_rmsnorm(const __nv_bfloat16* a, const __nv_bfloat16* x,
+                               const __nv_bfloat16* w, __nv_bfloat16* norm,
+                               __nv_bfloat16* resid, int64_t M, int N, float eps, int sms,
+                               cudaStream_t stream);
+constexpr int kRmsMaxN = 16384;
+
 // Tile geometry shared by the planner and the kernels.
 constexpr int kBM = 128;        // MMA M: rows of TMEM / output tile height
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)

@@ -65,6 +65,22 @@ def bf16_weight_bytes(K, N) -> int:
     return K * N * BF16
 
 
+def add_rmsnorm_counts(M, N) -> Counts:
+    """Fused: read a and x, write the residual and the norm (4 passes of
+    M*N bf16) plus the weight row.  Unfused: the add kernel reads a, x and
+    writes r; the RMSNorm kernel reads r back and writes the norm (5 passes)."""
+    t = M * N * BF16
+    return Counts(5.0 * M * N, 4 * t + N * BF16, 5 * t + N * BF16)
+
+
+def swiglu_pointwise_counts(M, N) -> Counts:
+    """Fused: read g and u, write h (3 passes).  Eager (sigmoid, mul, mul):
+    s = sigmoid(g) reads g writes s; t = g*s reads g, s writes t; h = t*u reads
+    t, u writes h (8 passes)."""
+    t = M * N * BF16
+    return Counts(6.0 * M * N, 3 * t, 8 * t)
+
+
 def roofline_seconds(c: Counts, peak_tflops: float, peak_gbs: float, fused=True) -> float:
     b = c.fused_bytes if fused else c.unfused_bytes
     return max(c.flops / (peak_tflops * 1e12), b / (peak_gbs * 1e9))
@@ -87,4 +103,8 @@ def counts_for(cfg: dict) -> Counts:
     if op == "w4a16":
         return w4a16_counts(M, N, K, cfg["group"], cfg.get("has_c", False),
                             cfg.get("has_bias", False), cfg.get("has_res", False))
+    if op == "add_rmsnorm":
+        return add_rmsnorm_counts(M, N)
+    if op == "swiglu_pointwise":
+        return swiglu_pointwise_counts(M, N)
     raise KeyError(op)

@@ -16,6 +16,9 @@ Workloads are the five configurations of the fused-GEMM study:
                                   scales uniform [0.005,0.02], group 128
   sweep      N=K=8192, M in {1,16,128,1024,8192}, A,B~N(0,1/sqrt(K)),
              C~N(0,1), bias~N(0,0.1), out=gelu_tanh(0.75AB+0.25C+bias)
+  add_rmsnorm  M=N=4096 (the prefill projection's output), a,x~N(0,1),
+               weight~N(1,0.01), eps=1e-5
+  swiglu_pointwise  M=2048 N=14336 (the gate/up outputs), g,u~N(0,64)
 
 N(0, x) is read as mean 0 and VARIANCE x (std = sqrt(x)); ``sigma_is_std``
 switches to reading x as the standard deviation.
@@ -43,6 +46,11 @@ CONFIGS = {
                   beta=0.0, act="identity", has_c=False, has_bias=False, has_res=False),
     "sweep": dict(id=5, op="gemm", M=None, N=8192, K=8192, layout="kn", alpha=0.75,
                   beta=0.25, act="gelu_tanh", has_c=True, has_bias=True, has_res=False),
+    # rows after the core path
+    "add_rmsnorm": dict(id=6, op="add_rmsnorm", M=4096, N=4096, K=0, eps=1e-5, alpha=1.0,
+                        beta=0.0, act="identity"),
+    "swiglu_pointwise": dict(id=7, op="swiglu_pointwise", M=2048, N=14336, K=0, alpha=1.0,
+                             beta=0.0, act="silu", has_c=False),
 }
 
 
@@ -109,6 +117,15 @@ def make(name: str, M: int | None = None, sigma_is_std: bool = False,
         out["Wq"] = int4_packed(rng_for(cid, 1), Kv, Nv)
         out["scales"] = bf16_uniform(rng_for(cid, 2), (Kv // cfg["group"], Nv), 0.005, 0.02)
         out["C"] = out["bias"] = out["residual"] = None
+    elif name == "add_rmsnorm":
+        out["a"] = bf16_normal(rng_for(cid, 0), (Mv, Nv), 1.0, s)
+        out["x"] = bf16_normal(rng_for(cid, 1), (Mv, Nv), 1.0, s)
+        out["weight"] = to_bf16_bits(rng_for(cid, 2).standard_normal(Nv).astype(np.float32)
+                                     * np.float32(0.1) + np.float32(1.0))
+    elif name == "swiglu_pointwise":
+        out["g"] = bf16_normal(rng_for(cid, 0), (Mv, Nv), 64.0, s)
+        out["u"] = bf16_normal(rng_for(cid, 1), (Mv, Nv), 64.0, s)
+        out["C"] = None
     elif name == "sweep":
         var = 1.0 / math.sqrt(Kv)
         out["A"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), var, s)
