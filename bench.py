@@ -57,6 +57,8 @@ WORKLOAD_TEXT = {
     "swiglu": "gate/up SwiGLU dual GEMM x[2048x4096], Wg,Wu[14336x4096], bf16",
     "w4a16": "W4A16 decode GEMM A[16x8192] x int4 W[8192x28672], group 128",
     "tiny": "tiny fused GEMM 64x256x128, SiLU(0.5AB + C + bias)",
+    "mlp_decode": "gated MLP block + residual at decode, x[16x4096], Wg,Wu[14336x4096], "
+                  "Wd[4096x14336], bf16, replayed from one CUDA graph",
 }
 
 
@@ -189,6 +191,8 @@ class ClockSampler:
 # ---------------------------------------------------------------- workloads
 
 def describe(w: dict) -> dict:
+    if w["op"] == "mlp":
+        return {"M": w["M"], "D": w["D"], "F": w["F"], "op": "mlp", "act": "silu"}
     d = {"M": w["M"], "N": w["N"], "K": w["K"], "op": w["op"]}
     if "eps" in w:
         d["eps"] = w["eps"]
@@ -229,8 +233,8 @@ class Workload:
         self.M, self.N, self.K = w["M"], w["N"], w["K"]
         self.counts = roofline.counts_for(w)
         host = {}
-        for key in ("A", "B", "C", "bias", "residual", "x", "w_gate", "w_up", "Wq", "scales",
-                    "a", "weight", "g", "u"):
+        for key in ("A", "B", "C", "bias", "residual", "x", "w_gate", "w_up", "w_down", "Wq",
+                    "scales", "a", "weight", "g", "u"):
             if w.get(key) is not None:
                 host[key] = w[key]
         self.host_np = host
@@ -250,16 +254,26 @@ class Workload:
             if self.op == "add_rmsnorm":
                 d["resid"] = torch.empty(self.M, self.N, dtype=torch.bfloat16, device=dev)
             self.sets.append(d)
-        gemm_op = {"gemm": "gemm_epilogue", "swiglu": "swiglu", "w4a16": "w4a16"}.get(self.op)
-        ws = gbf.gbf_workspace_size(gemm_op, self.M, self.N, self.K, False) if gemm_op else 0
+        gemm_op = {"gemm": "gemm_epilogue", "swiglu": "swiglu", "w4a16": "w4a16",
+                   "mlp": "mlp"}.get(self.op)
+        wK = w["F"] if self.op == "mlp" else self.K
+        ws = gbf.gbf_workspace_size(gemm_op, self.M, self.N, wK, False) if gemm_op else 0
         self.ws_bytes = ws
-        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
-        # pinned host buffers for the end-to-end leg
-        self.pinned = {k: torch.from_numpy(v.copy()).pin_memory() for k, v in host.items()}
+        self.ws_fused_bytes = gbf.gbf_workspace_size(gemm_op, self.M, self.N, wK, True) \
+            if gemm_op else 0
+        self.ws = torch.empty(max(ws, self.ws_fused_bytes, 16), dtype=torch.uint8, device=dev)
+        # pinned host buffers for the end-to-end leg: every operand, except for
+        # the MLP block, whose per-step inputs are its activations (x and the
+        # residual) while its weights stay resident like a model's parameters
+        step_keys = ("x", "residual") if self.op == "mlp" else tuple(host)
+        self.pinned = {k: torch.from_numpy(host[k].copy()).pin_memory() for k in step_keys}
         self.pinned_out = torch.empty(self.M * self.N * 2, dtype=torch.uint8).pin_memory()
-        self.h2d_bytes = sum(v.nbytes for v in host.values())
+        self.h2d_bytes = sum(host[k].nbytes for k in step_keys)
         self.d2h_bytes = self.M * self.N * 2
-        if gemm_op:
+        self.graphs = None
+        if self.op == "mlp":
+            self.path, self.splits = gbf.gbf_kernel_path("swiglu", self.M, w["F"], w["D"], "nk")
+        elif gemm_op:
             self.path, self.splits = gbf.gbf_kernel_path(gemm_op, self.M, self.N, self.K,
                                                          w.get("layout", "kn"))
         else:
@@ -268,10 +282,33 @@ class Workload:
     def describe(self) -> dict:
         return describe(self.w)
 
+    def mlp_direct(self, i: int, stream=None, fused: bool = True):
+        s = self.sets[i % self.n_sets]
+        w, gbf = self.w, self.gbf
+        fn = gbf.mlp_swiglu_down if fused else gbf.mlp_swiglu_down_unfused
+        fn(s["x"], s["w_gate"], s["w_up"], s["w_down"], s["residual"], s["out"], self.M, w["D"],
+           w["F"], self.ws, self.ws_fused_bytes if fused else self.ws_bytes, stream=stream)
+
+    def capture(self):
+        """MLP block: one CUDA graph per input set, fused and unfused chains."""
+        from tcgen05_tmem_bf16_gb300.graphs import CapturedChain
+        self.graphs = [CapturedChain(lambda st, i=i: self.mlp_direct(i, st))
+                       for i in range(self.n_sets)]
+        self.graphs_unfused = [CapturedChain(lambda st, i=i: self.mlp_direct(i, st, False))
+                               for i in range(self.n_sets)]
+
+    def launches_per_step(self) -> int:
+        return 2 if self.op == "mlp" else 1
+
     def fused(self, i: int, stream=None):
         s = self.sets[i % self.n_sets]
         w, gbf = self.w, self.gbf
-        if self.op == "gemm":
+        if self.op == "mlp":
+            if self.graphs is None:
+                self.mlp_direct(i, stream)
+            else:
+                self.graphs[i % self.n_sets].replay()
+        elif self.op == "gemm":
             gbf.gemm_epilogue(s["A"], s["B"], w["layout"], s.get("C"), s.get("bias"),
                               s.get("residual"), s["out"], self.M, self.N, self.K, w["alpha"],
                               w["beta"], w["act"], stream=stream)
@@ -294,7 +331,12 @@ class Workload:
         s = self.sets[i % self.n_sets]
         w, gbf = self.w, self.gbf
         kw = dict(workspace=self.ws, workspace_bytes=self.ws_bytes, stream=stream)
-        if self.op == "gemm":
+        if self.op == "mlp":
+            if self.graphs is None:
+                self.mlp_direct(i, stream, fused=False)
+            else:
+                self.graphs_unfused[i % self.n_sets].replay()
+        elif self.op == "gemm":
             gbf.gemm_epilogue_unfused(s["A"], s["B"], w["layout"], s.get("C"), s.get("bias"),
                                       s.get("residual"), s["out"], self.M, self.N, self.K,
                                       w["alpha"], w["beta"], w["act"], **kw)
@@ -318,6 +360,9 @@ class Workload:
     def unfused_kind(self) -> str:
         if self.op == "swiglu_pointwise":
             return "eager torch: sigmoid, mul, mul (3 kernels)"
+        if self.op == "mlp":
+            return ("two GEMMs -> bf16 g, u -> GLU pointwise -> bf16 h -> GEMM -> bf16 D -> "
+                    "residual-add pass (5 kernels, one CUDA graph)")
         return {"gemm": "GEMM -> bf16 D in HBM -> pointwise kernel",
                 "swiglu": "two GEMMs -> bf16 g, u in HBM -> GLU pointwise kernel",
                 "w4a16": "dequantise kernel -> bf16 W in HBM -> bf16 GEMM",
@@ -371,9 +416,12 @@ def oracle_elements(w: dict, rows, cols):
     import oracle
     op = w["op"]
     M, N, K = w["M"], w["N"], w["K"]
-    if op in ("add_rmsnorm", "swiglu_pointwise"):
+    if op in ("add_rmsnorm", "swiglu_pointwise", "mlp"):
         r = np.unique(np.asarray(rows) % M)
-        if op == "add_rmsnorm":
+        if op == "mlp":
+            oracle.mlp_swiglu_down(w["x"], w["w_gate"], w["w_up"], w["w_down"], w["residual"],
+                                   M=M, D=w["D"], F=w["F"], rows=r)
+        elif op == "add_rmsnorm":
             oracle.add_rmsnorm(w["a"][r], w["x"][r], w["weight"], M=r.size, N=N, eps=w["eps"])
         else:
             oracle.swiglu_pointwise(w["g"][r], w["u"][r], M=r.size, N=N, alpha=w["alpha"],
@@ -423,8 +471,11 @@ def cpu_baseline(w: dict, seconds: float = 12.0) -> dict:
         batch = min(batch * 2, 4096)
     per, unit = metric_per_element(w)
     return {"value": done * per / el, "unit": unit, "cores": 1, "kind": "oracle",
-            "sample": f"{done} output elements of the {w['M']}x{w['N']}x{w['K']} workload at "
-                      f"seeded positions ({el:.1f} s, single-threaded fp64 C oracle)"}
+            "sample": f"{done} output elements of the "
+                      + (f"{w['M']}x{w['D']}x{w['F']}" if w["op"] == "mlp"
+                         else f"{w['M']}x{w['N']}x{w['K']}")
+                      + f" workload at seeded positions ({el:.1f} s, single-threaded fp64 C "
+                        f"oracle)"}
 
 
 def run_reference(args, workload_name):
@@ -443,7 +494,7 @@ def run_reference(args, workload_name):
     per_elem = max((time.perf_counter() - t0) / n0, 1e-9)
     budget = 90.0 / max(1, args.steps + args.warmup)
     per_step = int(max(1, min(rows.size // 2, budget / per_elem)))
-    if w["op"] in ("add_rmsnorm", "swiglu_pointwise"):
+    if w["op"] in ("add_rmsnorm", "swiglu_pointwise", "mlp"):
         per_step = max(1, per_step // w["N"])  # rows per step
     pos, done = 0, 0
 
@@ -463,8 +514,10 @@ def run_reference(args, workload_name):
     el = time.perf_counter() - t0
     per, unit = metric_per_element(w)
     value = done * per / el
+    shape = (f"{w['M']}x{w['D']}x{w['F']}" if w["op"] == "mlp"
+             else f"{w['M']}x{w['N']}x{w['K']}")
     sample = (f"{done // args.steps} output elements per step at seeded positions of the "
-              f"{w['M']}x{w['N']}x{w['K']} workload, single-threaded fp64 C oracle")
+              f"{shape} workload, single-threaded fp64 C oracle")
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -476,6 +529,65 @@ def run_reference(args, workload_name):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------- MLP block legs
+
+def mlp_latency(wl, stream, reps: int = 200) -> dict:
+    """Median host wall time (us) of one synchronous MLP block step -- issue,
+    then wait for it -- for each way of issuing it: fused chain replayed from
+    a CUDA graph, fused chain launched directly (two C-ABI launches), the
+    unfused composition (graph and direct), and PyTorch eager (cuBLAS GEMMs
+    plus elementwise kernels) as the outside point of comparison."""
+    import torch
+    import torch.nn.functional as Fn
+
+    def eager(i):
+        s = wl.sets[i % wl.n_sets]
+        g = Fn.linear(s["x"], s["w_gate"])
+        u = Fn.linear(s["x"], s["w_up"])
+        torch.add(Fn.linear(Fn.silu(g) * u, s["w_down"]), s["residual"], out=s["out"])
+
+    legs = {
+        "fused_graph": lambda i: wl.graphs[i % wl.n_sets].replay(),
+        "fused_direct": lambda i: wl.mlp_direct(i, stream),
+        "unfused_graph": lambda i: wl.graphs_unfused[i % wl.n_sets].replay(),
+        "unfused_direct": lambda i: wl.mlp_direct(i, stream, fused=False),
+        "torch_eager": eager,
+    }
+    out = {}
+    for name, fn in legs.items():
+        for i in range(5):
+            fn(i)
+        torch.cuda.synchronize()
+        t = []
+        for i in range(reps):
+            t0 = time.perf_counter()
+            fn(i)
+            stream.synchronize()
+            t.append(time.perf_counter() - t0)
+        out[name] = statistics.median(t) * 1e6
+    out["note"] = ("median host wall time of one step issued and synchronised alone, weights "
+                   "cold in L2 (two rotating weight sets of 352 MB)")
+    return out
+
+
+def mlp_gate_up_kernel_time(wl, stream, steps: int):
+    """Average launch duration of the block's gate/up GEMM alone (CUDA events
+    around a back-to-back loop on the launching stream), and its counts."""
+    from tcgen05_tmem_bf16_gb300 import roofline as rf
+    w, gbf = wl.w, wl.gbf
+    M, D, F = w["M"], w["D"], w["F"]
+
+    def gate_up(i):
+        s = wl.sets[i % wl.n_sets]
+        gbf.swiglu_dual_gemm(s["x"], s["w_gate"], s["w_up"], "nk", wl.ws, M, F, D, 1.0, 0.0,
+                             None, "silu", stream=stream)
+
+    for i in range(5):
+        gate_up(i)
+    region, _ = time_loop(gate_up, steps, stream, per_launch=False)
+    return region / steps, rf.swiglu_counts(M, F, D)
 
 
 # ---------------------------------------------------------------- main
@@ -529,6 +641,11 @@ def main(argv=None):
     for i in range(args.warmup):
         wl.fused(i)
     torch.cuda.synchronize()
+    if wl.op == "mlp":
+        wl.capture()  # the block is replayed from CUDA graphs from here on
+        for i in range(args.warmup):
+            wl.fused(i)
+        torch.cuda.synchronize()
     if args.steps is None:
         t_cal, _ = time_loop(wl.fused, 20, stream, per_launch=False)
         args.steps = int(min(50000, max(200, 1.5 / max(t_cal / 20, 1e-6))))
@@ -580,14 +697,23 @@ def main(argv=None):
                               per_launch=False)
     e2e_max, e2e_units = aggregate(e2e_region, per_step * args.e2e_steps, world)
 
-    # roofline of the dominant (only) kernel of the step
+    # MLP block: per-step latency of each way of issuing it, and the
+    # dominant kernel (the gate/up GEMM) timed on its own
+    extra = {}
+    per_launch_dom = per_launch
+    dom_counts = wl.counts
+    if wl.op == "mlp":
+        extra["latency_us"] = mlp_latency(wl, stream)
+        per_launch_dom, dom_counts = mlp_gate_up_kernel_time(wl, stream, args.steps)
+
+    # roofline of the dominant kernel of the step
     long_loop = region > 0.5
     if bnd == "tensor":
-        achieved = wl.counts.flops / per_launch / 1e12
+        achieved = dom_counts.flops / per_launch_dom / 1e12
         peak = peaks["bf16_tflops_sustained"] if long_loop else peaks["bf16_tflops"]
         unit = "TFLOP/s"
     else:
-        achieved = wl.counts.fused_bytes / per_launch / 1e9
+        achieved = dom_counts.fused_bytes / per_launch_dom / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     roof = {"bound": bnd, "achieved": achieved, "peak": peak, "unit": unit,
@@ -599,12 +725,17 @@ def main(argv=None):
             "kernel": {"persistent": "gemm_persistent_kernel", "swap_splitk": "gemm_swap_kernel",
                        "w4a16": "w4a16_kernel", "pair": "gemm_pair_kernel"}.get(wl.path, wl.path),
             "splits": wl.splits,
-            "kernel_ms": per_launch * 1e3,
-            "algorithmic_flops": wl.counts.flops, "algorithmic_bytes": wl.counts.fused_bytes,
+            "kernel_ms": per_launch_dom * 1e3,
+            "algorithmic_flops": dom_counts.flops, "algorithmic_bytes": dom_counts.fused_bytes,
             "roofline_ms": rf.roofline_seconds(wl.counts, peaks["bf16_tflops"],
                                                peaks["hbm_gbs"]) * 1e3}
     if bnd == "tensor":
         roof["frac_of_burst_peak"] = achieved / peaks["bf16_tflops"]
+    if wl.op == "mlp":
+        chain_gbs = wl.counts.fused_bytes / per_launch / 1e9
+        roof["kernel"] = f"{roof['kernel']} (gate/up GEMM, the larger of the block's two)"
+        roof["chain"] = {"achieved": chain_gbs, "unit": "GB/s", "frac": chain_gbs / peak,
+                         "ms": per_launch * 1e3, "algorithmic_bytes": wl.counts.fused_bytes}
 
     line = {
         "metric": METRIC, "value": value, "unit": vunit, "n_gpus": world,
@@ -621,8 +752,9 @@ def main(argv=None):
         "speedup_vs_unfused": un_ms / fu_ms,
         "e2e": {"value": e2e_units / e2e_max / vscale, "unit": vunit,
                 "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * wl.launches_per_step(),
         "clocks": clocks,
+        **extra,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl.w, args.cpu_seconds)

@@ -76,6 +76,7 @@ typedef int gbf_status_t;
 #define GBF_OP_GEMM_EPILOGUE 0
 #define GBF_OP_SWIGLU 1
 #define GBF_OP_W4A16 2
+#define GBF_OP_MLP 3 /* gbf_workspace_size(GBF_OP_MLP, M, D, F, fused) */
 
 /*
  * gemm_epilogue -- out[M][N] = bf16( act(alpha * A*B~ + beta*C + bias) + residual )
@@ -158,6 +159,31 @@ GBF_API gbf_status_t add_rmsnorm(const void *a, const void *x, const void *weigh
 GBF_API gbf_status_t add_rmsnorm_unfused(const void *a, const void *x, const void *weight,
                                          void *out_norm, void *out_resid, int64_t M, int64_t N,
                                          float eps, gbf_stream_t stream);
+
+/*
+ * mlp_swiglu_down -- one gated MLP block with its residual add:
+ *   h   = bf16( silu(x*Wg^T) * (x*Wu^T) )     [M][F]   (the fused gate/up GEMM)
+ *   out = bf16( h*Wd^T + residual )            [M][D]   (GEMM with the residual fused)
+ *   ("Fusion Thinking", Pattern 2: gate = W_gate x, up = W_up x,
+ *   h = silu(gate)*up, out = W_down h; with Pattern 1's "h = mlp(h) + h").
+ *   x [M][D]; w_gate, w_up [F][D]; w_down [D][F] (all K-contiguous); residual
+ *   [M][D] or NULL (may equal out); out [M][D].  h lives in the workspace
+ *   (gbf_workspace_size(GBF_OP_MLP, M, D, F, 1) bytes) and is left there.
+ *   Two kernel launches on `stream`, no host synchronisation between them.
+ * mlp_swiglu_down_unfused -- the same block the eager way: two GEMMs writing
+ *   g and u, the GLU pointwise pass, the down GEMM writing bf16 D, the
+ *   residual pointwise pass (workspace: gbf_workspace_size(GBF_OP_MLP, M, D,
+ *   F, 0) bytes: g, u, h, D in 256-byte aligned sections).
+ */
+GBF_API gbf_status_t mlp_swiglu_down(const void *x, const void *w_gate, const void *w_up,
+                                     const void *w_down, const void *residual, void *out,
+                                     int64_t M, int64_t D, int64_t F, void *workspace,
+                                     size_t workspace_bytes, gbf_stream_t stream);
+GBF_API gbf_status_t mlp_swiglu_down_unfused(const void *x, const void *w_gate,
+                                             const void *w_up, const void *w_down,
+                                             const void *residual, void *out, int64_t M,
+                                             int64_t D, int64_t F, void *workspace,
+                                             size_t workspace_bytes, gbf_stream_t stream);
 
 /*
  * Unfused reference compositions: the same results as above, computed the

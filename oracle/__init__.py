@@ -14,6 +14,9 @@ Every function here follows the passage cited in ``gbf_oracle.c``:
   * swiglu         -- "Fusion Thinking", Pattern 2 (Fused SwiGLU).
   * w4a16 / dequant_int4 -- "Fusion Thinking", Pattern 3 (Dequant + GEMM).
   * add_rmsnorm    -- "Fusion Thinking", Pattern 1 (Fused RMSNorm + residual).
+  * mlp_swiglu_down -- "Fusion Thinking", Pattern 2 (out = W_down h) with
+                      Pattern 1's residual add after the MLP: the two calls
+                      above composed, h rounded to bf16 in between.
   * unfused modes  -- "kernel fusion" wiki, the activation-after-matmul case.
 """
 from __future__ import annotations
@@ -223,6 +226,27 @@ def swiglu_pointwise(g, u, C=None, *, M, N, alpha=1.0, beta=0.0, act="silu"):
                                    float(beta), ACT[act], _ptr(out)) != 0:
         raise ValueError("oracle rejected its arguments")
     return out
+
+
+def mlp_swiglu_down(x, w_gate, w_up, w_down, residual=None, *, M, D, F, unfused=False,
+                    rows=None, want_f64=False):
+    """(out, h) of one gated MLP block with its residual add:
+    h = swiglu(x, Wg, Wu) rounded to bf16 ([M][F]), out = bf16(h*Wd^T +
+    residual) ([M][D]).  x [M][D]; w_gate, w_up [F][D]; w_down [D][F].
+    With ``rows`` only those rows are computed (h rows depend on x rows
+    alone).  ``unfused`` rounds g, u and the down product to bf16 first."""
+    x = _u16(x)
+    residual = _u16(residual)
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        x = np.ascontiguousarray(x.reshape(M, D)[rows])
+        if residual is not None:
+            residual = np.ascontiguousarray(residual.reshape(M, D)[rows])
+        M = int(rows.size)
+    h = swiglu(x, w_gate, w_up, "nk", M=M, N=F, K=D, act="silu", unfused=unfused)
+    out = gemm_epilogue(h, w_down, "nk", residual=residual, M=M, N=D, K=F, unfused=unfused,
+                        want_f64=want_f64)
+    return out, h
 
 
 def add_rmsnorm(a, x, w, *, M, N, eps=1e-5, unfused=False):

@@ -21,7 +21,7 @@ from . import build as _build
 
 ACT = {"identity": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
 LAYOUT = {"kn": 0, "nk": 1}
-OP = {"gemm_epilogue": 0, "swiglu": 1, "w4a16": 2}
+OP = {"gemm_epilogue": 0, "swiglu": 1, "w4a16": 2, "mlp": 3}
 STATUS = {0: "GBF_OK", 1: "GBF_ERR_INVALID_ARG", 2: "GBF_ERR_MISALIGNED",
           3: "GBF_ERR_UNSUPPORTED_SHAPE", 4: "GBF_ERR_WORKSPACE", 5: "GBF_ERR_CUDA",
           6: "GBF_ERR_TIMEOUT", 7: "GBF_ERR_NO_DEVICE"}
@@ -32,7 +32,8 @@ EXPORTS = ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unf
            "gbf_check_device_error", "gbf_status_string", "gbf_set_wait_timeout_ns",
            "gbf_debug_inject_timeout", "gbf_kernel_path", "gbf_version",
            "gemm_epilogue_unfused_noalloc", "gbf_debug_force_splits", "gbf_debug_set_profile",
-           "swiglu_pointwise", "add_rmsnorm", "add_rmsnorm_unfused")
+           "swiglu_pointwise", "add_rmsnorm", "add_rmsnorm_unfused", "mlp_swiglu_down",
+           "mlp_swiglu_down_unfused")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,10 @@ def load(path: str | None = None):
                            ("w4a16_gemm", w4_args), ("w4a16_gemm_unfused", w4_args)):
             fn = getattr(lib, name)
             fn.argtypes = args
+            fn.restype = I
+        for name in ("mlp_swiglu_down", "mlp_swiglu_down_unfused"):
+            fn = getattr(lib, name)
+            fn.argtypes = [V, V, V, V, V, V, I64, I64, I64, V, SZ, V]
             fn.restype = I
         for name in ("add_rmsnorm", "add_rmsnorm_unfused"):
             fn = getattr(lib, name)
@@ -197,6 +202,21 @@ def add_rmsnorm_unfused(a, x, weight, out_norm, out_resid, M, N, eps=1e-5, strea
     st = load().add_rmsnorm_unfused(_p(a), _p(x), _p(weight), _p(out_norm), _p(out_resid), M, N,
                                     eps, _s(stream))
     return _check(st, "add_rmsnorm_unfused", raise_on_error)
+
+
+def mlp_swiglu_down(x, w_gate, w_up, w_down, residual, out, M, D, F, workspace=None,
+                    workspace_bytes=0, stream=None, raise_on_error=True):
+    st = load().mlp_swiglu_down(_p(x), _p(w_gate), _p(w_up), _p(w_down), _p(residual), _p(out),
+                                M, D, F, _p(workspace), workspace_bytes, _s(stream))
+    return _check(st, "mlp_swiglu_down", raise_on_error)
+
+
+def mlp_swiglu_down_unfused(x, w_gate, w_up, w_down, residual, out, M, D, F, workspace=None,
+                            workspace_bytes=0, stream=None, raise_on_error=True):
+    st = load().mlp_swiglu_down_unfused(_p(x), _p(w_gate), _p(w_up), _p(w_down), _p(residual),
+                                        _p(out), M, D, F, _p(workspace), workspace_bytes,
+                                        _s(stream))
+    return _check(st, "mlp_swiglu_down_unfused", raise_on_error)
 
 
 def w4a16_gemm(A, Wq, scales, group_size, C, bias, residual, out, M, N, K, alpha=1.0,

@@ -404,7 +404,13 @@ gbf_status_t add_rmsnorm_unfused(const void* a, const void* x, const void* weigh
 }
 
 size_t gbf_workspace_size(int op, int64_t M, int64_t N, int64_t K, int fused) {
-  if (fused || M < 0 || N < 0 || K < 0) return 0;
+  if (M < 0 || N < 0 || K < 0) return 0;
+  if (op == GBF_OP_MLP) {
+    const size_t h = align256(static_cast<size_t>(M * K) * 2);
+    if (fused) return h;
+    return 4 * h + align256(static_cast<size_t>(M * N) * 2);  // g, u (2h), h, D
+  }
+  if (fused) return 0;
   switch (op) {
     case GBF_OP_GEMM_EPILOGUE: return align256(static_cast<size_t>(M * N) * 2);
     case GBF_OP_SWIGLU: return 2 * align256(static_cast<size_t>(M * N) * 2);
@@ -412,6 +418,12 @@ size_t gbf_workspace_size(int op, int64_t M, int64_t N, int64_t K, int fused) {
     default: return 0;
   }
 }
+
+namespace {
+// MLP workspace sections (N = D, K = F): h first; the unfused chain adds
+// g, u and the down GEMM's bf16 product.
+size_t mlp_h_bytes(int64_t M, int64_t F) { return align256(static_cast<size_t>(M * F) * 2); }
+}  // namespace
 
 gbf_status_t gemm_epilogue_unfused(const void* A, const void* B, int b_layout, const void* C,
                                    const void* bias, const void* residual, void* out, int64_t M,
@@ -493,6 +505,57 @@ gbf_status_t w4a16_gemm_unfused(const void* A, const uint8_t* Wq, const void* sc
                                             group_size, K, N, w, dev->sms, s))) != GBF_OK)
     return st;
   return run_gemm(A, w, nullptr, GBF_B_KN, false, ep, M, N, K, *dev, err, s);
+}
+
+gbf_status_t mlp_swiglu_down(const void* x, const void* w_gate, const void* w_up,
+                             const void* w_down, const void* residual, void* out, int64_t M,
+                             int64_t D, int64_t F, void* workspace, size_t workspace_bytes,
+                             gbf_stream_t stream) {
+  gbf_status_t st = check_common(M, F, D, GBF_ACT_SILU);
+  if (st != GBF_OK) return st;
+  if ((st = check_common(M, D, F, GBF_ACT_IDENTITY)) != GBF_OK) return st;
+  if ((st = check_ptrs({x, w_gate, w_up, w_down, out}, {residual, workspace})) != GBF_OK)
+    return st;
+  const size_t need = gbf_workspace_size(GBF_OP_MLP, M, D, F, 1);
+  if (need && (!workspace || workspace_bytes < need)) return GBF_ERR_WORKSPACE;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || D == 0) return GBF_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* h = workspace;
+  if ((st = run_gemm(x, w_gate, w_up, GBF_B_NK, true,
+                     make_ep(nullptr, nullptr, nullptr, h, 1.0f, 0.0f, GBF_ACT_SILU), M, F, D,
+                     *dev, err, s)) != GBF_OK)
+    return st;
+  return run_gemm(h, w_down, nullptr, GBF_B_NK, false,
+                  make_ep(nullptr, nullptr, residual, out, 1.0f, 0.0f, GBF_ACT_IDENTITY), M, D, F,
+                  *dev, err, s);
+}
+
+gbf_status_t mlp_swiglu_down_unfused(const void* x, const void* w_gate, const void* w_up,
+                                     const void* w_down, const void* residual, void* out,
+                                     int64_t M, int64_t D, int64_t F, void* workspace,
+                                     size_t workspace_bytes, gbf_stream_t stream) {
+  gbf_status_t st = check_common(M, F, D, GBF_ACT_SILU);
+  if (st != GBF_OK) return st;
+  if ((st = check_common(M, D, F, GBF_ACT_IDENTITY)) != GBF_OK) return st;
+  if ((st = check_ptrs({x, w_gate, w_up, w_down, out}, {residual, workspace})) != GBF_OK)
+    return st;
+  const size_t need = gbf_workspace_size(GBF_OP_MLP, M, D, F, 0);
+  if (need && (!workspace || workspace_bytes < need)) return GBF_ERR_WORKSPACE;
+  if (M == 0 || D == 0) return GBF_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t hb = mlp_h_bytes(M, F);
+  // [g | u] (what swiglu_dual_gemm_unfused expects), then h, then the down GEMM's D
+  uint8_t* gu = ws;
+  uint8_t* h = ws + 2 * hb;
+  uint8_t* d = ws + 3 * hb;
+  if ((st = swiglu_dual_gemm_unfused(x, w_gate, w_up, GBF_B_NK, h, M, F, D, 1.0f, 0.0f, nullptr,
+                                     GBF_ACT_SILU, gu, 2 * hb, stream)) != GBF_OK)
+    return st;
+  return gemm_epilogue_unfused(h, w_down, GBF_B_NK, nullptr, nullptr, residual, out, M, D, F,
+                               1.0f, 0.0f, GBF_ACT_IDENTITY, d, need - 3 * hb, stream);
 }
 
 gbf_status_t gbf_check_device_error(gbf_stream_t stream) {

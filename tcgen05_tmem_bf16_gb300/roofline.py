@@ -81,6 +81,21 @@ def swiglu_pointwise_counts(M, N) -> Counts:
     return Counts(6.0 * M * N, 3 * t, 8 * t)
 
 
+def mlp_counts(M, D, F) -> Counts:
+    """One gated MLP block with its residual.  FLOPs: the gate and up products
+    (2*M*F*D each) and the down product (2*M*D*F).  Fused chain: x, the three
+    weights, the residual and out cross HBM once, and h (M x F bf16) is
+    written by the gate/up GEMM and read back by the down GEMM.  Unfused: x is
+    read twice, g and u are written and read back, h likewise, and the down
+    product D is written and read back by the residual-add pass."""
+    x = M * D * BF16
+    w = 3 * F * D * BF16
+    h = M * F * BF16
+    fused = x + w + 2 * h + 2 * x  # + residual read, out written
+    unfused = fused + x + 2 * (2 * h) + 2 * x
+    return Counts(6.0 * M * D * F, fused, unfused)
+
+
 def roofline_seconds(c: Counts, peak_tflops: float, peak_gbs: float, fused=True) -> float:
     b = c.fused_bytes if fused else c.unfused_bytes
     return max(c.flops / (peak_tflops * 1e12), b / (peak_gbs * 1e9))
@@ -107,4 +122,6 @@ def counts_for(cfg: dict) -> Counts:
         return add_rmsnorm_counts(M, N)
     if op == "swiglu_pointwise":
         return swiglu_pointwise_counts(M, N)
+    if op == "mlp":
+        return mlp_counts(M, cfg["D"], cfg["F"])
     raise KeyError(op)

@@ -415,3 +415,72 @@ def test_add_rmsnorm_scale_invariance_and_unfused_mode():
     nf, rf = oracle.add_rmsnorm(a, zero, w, M=M, N=N)
     nu, ru = oracle.add_rmsnorm(a, zero, w, M=M, N=N, unfused=True)
     assert np.array_equal(rf, ru) and np.array_equal(nf, nu)
+
+
+# ---------------------------------------------------------------- MLP block chain
+
+def _bf16_from_f64_torch(v):
+    return torch.from_numpy(np.asarray(v, dtype=np.float64)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def test_mlp_chain_matches_library_composition():
+    # h = bf16(silu(x Wg^T) * (x Wu^T)) from numpy matmuls and torch's SiLU;
+    # out = h Wd^T + residual in float64 before the final rounding.
+    rng = np.random.Generator(np.random.PCG64(21))
+    M, D, F = 5, 24, 40
+    x = to_bf16_bits(rng.standard_normal((M, D)).astype(np.float32))
+    wg = to_bf16_bits((rng.standard_normal((F, D)) / 5).astype(np.float32))
+    wu = to_bf16_bits((rng.standard_normal((F, D)) / 5).astype(np.float32))
+    wd = to_bf16_bits((rng.standard_normal((D, F)) / 6).astype(np.float32))
+    r = to_bf16_bits(rng.standard_normal((M, D)).astype(np.float32))
+    f = oracle.bf16_bits_to_f64
+    gm, um = f(x) @ f(wg).T, f(x) @ f(wu).T
+    h_want = _bf16_from_f64_torch(torch.nn.functional.silu(torch.from_numpy(gm)).numpy() * um)
+    (_, out64), h = oracle.mlp_swiglu_down(x, wg, wu, wd, r, M=M, D=D, F=F, want_f64=True)
+    assert np.array_equal(h, h_want)
+    np.testing.assert_allclose(out64, f(h_want) @ f(wd).T + f(r), rtol=1e-12, atol=1e-14)
+    # without a residual the block is the bare down projection of h
+    (_, bare), _ = oracle.mlp_swiglu_down(x, wg, wu, wd, None, M=M, D=D, F=F, want_f64=True)
+    np.testing.assert_allclose(bare, f(h_want) @ f(wd).T, rtol=1e-12, atol=1e-14)
+    # a row subset equals the same rows of the full result
+    full, _ = oracle.mlp_swiglu_down(x, wg, wu, wd, r, M=M, D=D, F=F)
+    sub, hs = oracle.mlp_swiglu_down(x, wg, wu, wd, r, M=M, D=D, F=F, rows=[4, 1])
+    assert np.array_equal(sub, full[[4, 1]]) and np.array_equal(hs, h[[4, 1]])
+
+
+def test_mlp_chain_identity_down_projection_adds_residual_to_h():
+    # D == F and W_down = I: out = bf16(h + residual), with h, residual
+    # small dyadic values so the sum is exact and the rounding is the only step.
+    rng = np.random.Generator(np.random.PCG64(22))
+    M, D = 3, 16
+    x = bits(rng.integers(-4, 5, size=(M, D)) / 4.0)
+    wg = bits(rng.integers(-2, 3, size=(D, D)) / 8.0)
+    wu = bits(rng.integers(-2, 3, size=(D, D)) / 8.0)
+    wd = bits(np.eye(D))
+    r = bits(rng.integers(-8, 9, size=(M, D)) / 2.0)
+    out, h = oracle.mlp_swiglu_down(x, wg, wu, wd, r, M=M, D=D, F=D)
+    f = oracle.bf16_bits_to_f64
+    want = np.array([[oracle.bf16_from_f64(v) for v in row] for row in f(h) + f(r)],
+                    dtype=np.uint16)
+    assert np.array_equal(out, want)
+    assert not np.array_equal(out, h)  # the residual is really added
+    out0, h0 = oracle.mlp_swiglu_down(x, wg, wu, wd, None, M=M, D=D, F=D)
+    assert np.array_equal(out0, h0)
+
+
+def test_mlp_chain_unfused_mode_rounds_every_intermediate():
+    rng = np.random.Generator(np.random.PCG64(23))
+    M, D, F = 4, 16, 32
+    x = to_bf16_bits(rng.standard_normal((M, D)).astype(np.float32))
+    wg = to_bf16_bits((rng.standard_normal((F, D)) / 4).astype(np.float32))
+    wu = to_bf16_bits((rng.standard_normal((F, D)) / 4).astype(np.float32))
+    wd = to_bf16_bits((rng.standard_normal((D, F)) / 6).astype(np.float32))
+    r = to_bf16_bits(rng.standard_normal((M, D)).astype(np.float32))
+    out, h = oracle.mlp_swiglu_down(x, wg, wu, wd, r, M=M, D=D, F=F, unfused=True)
+    f = oracle.bf16_bits_to_f64
+    gb = _bf16_from_f64_torch(f(x) @ f(wg).T)
+    ub = _bf16_from_f64_torch(f(x) @ f(wu).T)
+    assert np.array_equal(h, oracle.swiglu_pointwise(gb, ub, M=M, N=F))
+    db = _bf16_from_f64_torch(f(h) @ f(wd).T)
+    assert np.array_equal(out, oracle.pointwise_epilogue(db, residual=r, M=M, N=D))

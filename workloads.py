@@ -51,6 +51,11 @@ CONFIGS = {
                         beta=0.0, act="identity"),
     "swiglu_pointwise": dict(id=7, op="swiglu_pointwise", M=2048, N=14336, K=0, alpha=1.0,
                              beta=0.0, act="silu", has_c=False),
+    # one gated MLP block with its residual at a decode step of 16 sequences:
+    # x[16x4096], Wg, Wu [14336x4096], Wd [4096x14336]; out = M x D (N = D),
+    # the input width K = D, the hidden width F.
+    "mlp_decode": dict(id=8, op="mlp", M=16, N=4096, K=4096, D=4096, F=14336, alpha=1.0,
+                       beta=0.0, act="silu"),
 }
 
 
@@ -126,6 +131,15 @@ def make(name: str, M: int | None = None, sigma_is_std: bool = False,
         out["g"] = bf16_normal(rng_for(cid, 0), (Mv, Nv), 64.0, s)
         out["u"] = bf16_normal(rng_for(cid, 1), (Mv, Nv), 64.0, s)
         out["C"] = None
+    elif name == "mlp_decode":
+        D, F = cfg["D"], cfg["F"]
+        out["x"] = bf16_normal(rng_for(cid, 0), (Mv, D), 1.0, s)
+        # fan-in scaled weights (variance 1/fan_in), so g, u ~ N(0, 1) and the
+        # block output is of the same order as the residual it is added to
+        out["w_gate"] = bf16_normal(rng_for(cid, 1), (F, D), 1.0 / D, s)
+        out["w_up"] = bf16_normal(rng_for(cid, 2), (F, D), 1.0 / D, s)
+        out["w_down"] = bf16_normal(rng_for(cid, 3), (D, F), 1.0 / F, s)
+        out["residual"] = bf16_normal(rng_for(cid, 4), (Mv, D), 1.0, s)
     elif name == "sweep":
         var = 1.0 / math.sqrt(Kv)
         out["A"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), var, s)
