@@ -25,17 +25,38 @@ def block_inputs(M, D, F, seed=0):
     return w
 
 
-def check_stagewise(w, h_gpu, out_gpu, M, D, F, residual=True, unfused=False, what=""):
+def check_stagewise(w, h_gpu, out_gpu, M, D, F, residual=True, what=""):
     _, h_want = oracle.mlp_swiglu_down(w["x"], w["w_gate"], w["w_up"], w["w_down"], None,
-                                       M=M, D=D, F=F, unfused=unfused)
+                                       M=M, D=D, F=F)
     assert_parity(h_gpu, h_want, f"{what} h")
     out_want = oracle.gemm_epilogue(h_gpu, w["w_down"], "nk",
                                     residual=w["residual"] if residual else None,
-                                    M=M, N=D, K=F, unfused=unfused)
+                                    M=M, N=D, K=F)
     assert_parity(out_gpu, out_want, f"{what} out")
 
 
-def run_block(cuda_lib, w, M, D, F, fused=True, residual=True, inplace=False):
+def check_unfused_stagewise(w, ws, out_gpu, M, D, F, what=""):
+    """The unfused chain stores g, u, h and the down product D in bf16; each
+    stored tensor is a rounding decision, so every kernel is checked on the
+    GPU's own inputs: g, u against the oracle's products of x, h against the
+    oracle's GLU of the GPU's g and u, D against the oracle's product of the
+    GPU's h, out against the oracle's residual add of the GPU's D."""
+    hb = (M * F * 2 + 255) // 256 * 256
+
+    def sect(off, rows, cols):
+        return down(ws[off:off + rows * cols * 2].view(torch.bfloat16).view(rows, cols))
+
+    g, u, h, d = sect(0, M, F), sect(hb, M, F), sect(2 * hb, M, F), sect(3 * hb, M, D)
+    for name, wt, got in (("g", w["w_gate"], g), ("u", w["w_up"], u)):
+        assert_parity(got, oracle.gemm_epilogue(w["x"], wt, "nk", M=M, N=F, K=D),
+                      f"{what} {name}")
+    assert_parity(h, oracle.swiglu_pointwise(g, u, M=M, N=F), f"{what} h")
+    assert_parity(d, oracle.gemm_epilogue(h, w["w_down"], "nk", M=M, N=D, K=F), f"{what} D")
+    assert_parity(out_gpu, oracle.pointwise_epilogue(d, residual=w["residual"], M=M, N=D),
+                  f"{what} out")
+
+
+def run_block(cuda_lib, w, M, D, F, fused=True, residual=True, inplace=False, keep_ws=False):
     ws_bytes = cuda_lib.gbf_workspace_size("mlp", M, D, F, fused)
     ws = torch.full((max(ws_bytes, 256),), 0xFF, dtype=torch.uint8, device="cuda")
     r = up(w["residual"]) if residual else None
@@ -47,6 +68,8 @@ def run_block(cuda_lib, w, M, D, F, fused=True, residual=True, inplace=False):
     hb = (M * F * 2 + 255) // 256 * 256
     off = 0 if fused else 2 * hb
     h = down(ws[off:off + M * F * 2].view(torch.bfloat16).view(M, F))
+    if keep_ws:
+        return ws, down(out)
     return h, down(out)
 
 
@@ -61,8 +84,8 @@ def test_mlp_chain_fused(cuda_lib, M, D, F):
 @pytest.mark.parametrize("M,D,F", [(16, 1024, 2816), (300, 512, 1024)])
 def test_mlp_chain_unfused(cuda_lib, M, D, F):
     w = block_inputs(M, D, F)
-    h, out = run_block(cuda_lib, w, M, D, F, fused=False)
-    check_stagewise(w, h, out, M, D, F, unfused=True, what=f"unfused {M}x{D}x{F}")
+    ws, out = run_block(cuda_lib, w, M, D, F, fused=False, keep_ws=True)
+    check_unfused_stagewise(w, ws, out, M, D, F, what=f"unfused {M}x{D}x{F}")
 
 
 def test_mlp_chain_decode_workload_full_output(cuda_lib):
@@ -139,7 +162,7 @@ def test_graph_replay_of_unfused_chain(cuda_lib):
     blk = MLPBlock(up(w["w_gate"]), up(w["w_up"]), up(w["w_down"]), M, fused=False)
     out = down(blk.run(up(w["x"]), up(w["residual"])))
     assert cuda_lib.gbf_check_device_error() == 0
-    check_stagewise(w, down(blk.h), out, M, D, F, unfused=True, what="unfused graph")
+    check_unfused_stagewise(w, blk.workspace, out, M, D, F, what="unfused graph")
 
 
 def test_graph_buckets_pad_rows(cuda_lib):
