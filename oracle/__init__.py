@@ -13,6 +13,9 @@ Every function here follows the passage cited in ``gbf_oracle.c``:
                       "Kernel fusion" guide, Concept.
   * swiglu         -- "Fusion Thinking", Pattern 2 (Fused SwiGLU).
   * w4a16 / dequant_int4 -- "Fusion Thinking", Pattern 3 (Dequant + GEMM).
+  * wq_gemm / dequant_wq -- the same with int4, FP8 (E4M3) or NVFP4 (E2M1 with
+                      E4M3 scales per 16 along K) weights; Pattern 3 names
+                      NVFP4 weight-only quantisation with BF16 activations.
   * add_rmsnorm    -- "Fusion Thinking", Pattern 1 (Fused RMSNorm + residual).
   * mlp_swiglu_down -- "Fusion Thinking", Pattern 2 (out = W_down h) with
                       Pattern 1's residual add after the MLP: the two calls
@@ -82,6 +85,15 @@ def _load():
         lib.oracle_w4a16.restype = I
         lib.oracle_dequant_int4.argtypes = [P, P, I64, I64, I64, P]
         lib.oracle_dequant_int4.restype = I
+        lib.oracle_wq_gemm.argtypes = [I, P, P, P, I64, P, P, P, I64, I64, I64, D, D, I,
+                                       P, P, I64, P, P]
+        lib.oracle_wq_gemm.restype = I
+        lib.oracle_wq_dequant.argtypes = [I, P, P, I64, I64, I64, P]
+        lib.oracle_wq_dequant.restype = I
+        lib.oracle_fp8_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_fp8_e4m3_to_f64.restype = D
+        lib.oracle_fp4_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_fp4_e2m1_to_f64.restype = D
         lib.oracle_pointwise_epilogue.argtypes = [P, P, P, P, I64, I64, D, D, I, P]
         lib.oracle_pointwise_epilogue.restype = I
         lib.oracle_swiglu_pointwise.argtypes = [P, P, P, I64, I64, D, D, I, P]
@@ -195,6 +207,55 @@ def w4a16(A, Wq, scales, group_size, C=None, bias=None, residual=None, *, M, N, 
                           _ptr(bias), _ptr(residual), M, N, K, float(alpha), float(beta),
                           ACT[act], _ptr(r), _ptr(c), count, _ptr(ob), _ptr(of))
     return _finish(rc, ob, of, M, N, rows, want_f64)
+
+
+WQ_KIND = {"int4": 0, "fp8": 1, "nvfp4": 2}
+
+
+def fp8_e4m3_to_f64(b: int) -> float:
+    return float(_load().oracle_fp8_e4m3_to_f64(int(b) & 0xFF))
+
+
+def fp4_e2m1_to_f64(b: int) -> float:
+    return float(_load().oracle_fp4_e2m1_to_f64(int(b) & 0xF))
+
+
+def _scales(kind, scales):
+    if scales is None:
+        return None
+    if kind == "nvfp4":
+        return np.ascontiguousarray(scales, dtype=np.uint8)
+    return _u16(scales)
+
+
+def wq_gemm(kind, A, Wq, scales, group_size=16, C=None, bias=None, residual=None, *, M, N, K,
+            alpha=1.0, beta=0.0, act="identity", rows=None, cols=None, want_f64=False):
+    """Weight-only GEMM: gemm_epilogue with B~ the dequantised weight of
+    format ``kind`` ("int4", "fp8" or "nvfp4"; see gbf_oracle.c).  For nvfp4
+    ``scales`` are E4M3 bytes [K/16][N] and alpha carries the per-tensor
+    factor; group_size is ignored."""
+    lib = _load()
+    A, C, bias, residual = map(_u16, (A, C, bias, residual))
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    sc = _scales(kind, scales)
+    r, c, count = _idx(M, N, rows, cols)
+    ob, of = _outputs(count, want_f64)
+    rc = lib.oracle_wq_gemm(WQ_KIND[kind], _ptr(A), _ptr(Wq), _ptr(sc), int(group_size),
+                            _ptr(C), _ptr(bias), _ptr(residual), M, N, K, float(alpha),
+                            float(beta), ACT[act], _ptr(r), _ptr(c), count, _ptr(ob), _ptr(of))
+    return _finish(rc, ob, of, M, N, rows, want_f64)
+
+
+def dequant_wq(kind, Wq, scales, group_size=16, *, K, N):
+    """The dequantised K x N bf16 weight of format ``kind``."""
+    lib = _load()
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    sc = _scales(kind, scales)
+    out = np.empty((K, N), dtype=np.uint16)
+    if lib.oracle_wq_dequant(WQ_KIND[kind], _ptr(Wq), _ptr(sc), int(group_size), K, N,
+                             _ptr(out)) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
 
 
 def dequant_int4(Wq, scales, group_size, *, K, N):

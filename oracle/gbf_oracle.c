@@ -24,6 +24,18 @@
  *       "Fusion Thinking", Pattern 3 (Dequant + GEMM): packed 2 x int4 per
  *       byte along N, high nibble first (interleave(w_hi, w_lo)), zero point
  *       8, per-group bf16 scales, result fed to the matrix product.
+ *   wq_gemm         the gemm_epilogue formula with B = a dequantised
+ *                   weight of one of three weight-only formats:
+ *                   int4:  bf16((q - 8) * s[k/G][n])       (as w4a16)
+ *                   fp8:   bf16(e4m3(q[k][n]) * s[k/G][n]) (bf16 group scales)
+ *                   nvfp4: bf16(e2m1(q[k][n]) * e4m3(S[k/16][n]))
+ *       "Fusion Thinking", Pattern 3 names INT4 / INT8 / NVFP4 weights with
+ *       BF16 activations; "Fusion and Epilogues" lists INT4 / FP8 / FP4
+ *       paths.  The element formats are the public OCP 8-bit (E4M3: bias 7,
+ *       subnormals, no infinity, S.1111.111 = NaN) and 4-bit (E2M1: bias 1,
+ *       values 0, 0.5, 1, 1.5, 2, 3, 4, 6) floating-point encodings; NVFP4
+ *       scales each run of 16 elements along K by an E4M3 factor, and its
+ *       per-tensor factor is the product's alpha.
  *   add_rmsnorm     r = a + x;  resid = bf16(r);
  *                   n = bf16( r / sqrt(mean_j(r_j^2) + eps) * w )   (per row)
  *       "Fusion Thinking", Pattern 1 (Fused RMSNorm + residual): one pass
@@ -166,6 +178,68 @@ static double w4_at(const uint8_t *Wq, const uint16_t *scales, int64_t G,
     return oracle_bf16_to_f64(oracle_bf16_from_f64(((double)q - 8.0) * s));
 }
 
+/* OCP FP8 E4M3 (bias 7, 3 mantissa bits, subnormals, no infinities; the
+ * two codes S.1111.111 are NaN), decoded from its definition. */
+double oracle_fp8_e4m3_to_f64(uint8_t b)
+{
+    int sign = (b >> 7) & 1, e = (b >> 3) & 0xF, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* OCP FP4 E2M1 (bias 1, 1 mantissa bit, subnormal 0.5), low 4 bits of b. */
+double oracle_fp4_e2m1_to_f64(uint8_t b)
+{
+    int sign = (b >> 3) & 1, e = (b >> 1) & 3, m = b & 1;
+    double v = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return sign ? -v : v;
+}
+
+enum { WQ_INT4 = 0, WQ_FP8 = 1, WQ_NVFP4 = 2 };
+
+/* Dequantised weight w[k][n] of format `kind` as a double (already rounded
+ * to bf16, the precision the product consumes).  int4 and nvfp4 codes are
+ * packed two per byte along N (column 2j in the high nibble of byte j, as
+ * the int4 weights); fp8 codes are one byte each.  Scales: int4 and fp8 take
+ * bf16 `scales` [K/G][N]; nvfp4 takes E4M3 bytes [K/16][N]. */
+static double wq_at(int kind, const uint8_t *Wq, const void *scales, int64_t G,
+                    int64_t N, int64_t k, int64_t n)
+{
+    double q, s;
+    if (kind == WQ_FP8) {
+        q = oracle_fp8_e4m3_to_f64(Wq[k * N + n]);
+        s = oracle_bf16_to_f64(((const uint16_t *)scales)[(k / G) * N + n]);
+    } else {
+        uint8_t byte = Wq[k * (N / 2) + n / 2];
+        int code = (n % 2 == 0) ? (byte >> 4) & 0xF : byte & 0xF;
+        if (kind == WQ_INT4) {
+            q = (double)code - 8.0;
+            s = oracle_bf16_to_f64(((const uint16_t *)scales)[(k / G) * N + n]);
+        } else {
+            q = oracle_fp4_e2m1_to_f64((uint8_t)code);
+            s = oracle_fp8_e4m3_to_f64(((const uint8_t *)scales)[(k / 16) * N + n]);
+        }
+    }
+    return oracle_bf16_to_f64(oracle_bf16_from_f64(q * s));
+}
+
+static int wq_args_ok(int kind, int64_t G, int64_t N, int64_t K)
+{
+    if (K < 0 || N < 0 || kind < WQ_INT4 || kind > WQ_NVFP4)
+        return 0;
+    if (kind == WQ_NVFP4)
+        return N % 2 == 0 && K % 16 == 0;
+    if (G <= 0 || K % G != 0)
+        return 0;
+    return kind == WQ_FP8 || N % 2 == 0;
+}
+
 /* Element iteration helper: idx_m/idx_n == NULL means all M x N in row-major
  * order (count must then be M*N); otherwise count explicit (m, n) pairs. */
 static void elem(const int64_t *idx_m, const int64_t *idx_n, int64_t N,
@@ -284,6 +358,46 @@ int oracle_w4a16(const uint16_t *A, const uint8_t *Wq, const uint16_t *scales,
         emit(i, epilogue(acc, C, bias, residual, N, m, n, alpha, beta, act),
              out_bf16, out_f64);
     }
+    return 0;
+}
+
+/* Weight-only GEMM of any of the three formats (wq_at): the gemm_epilogue
+ * formula with B~ = the dequantised weight ("Fusion Thinking", Pattern 3).
+ * G is ignored for nvfp4 (its blocks are 16 along K). */
+int oracle_wq_gemm(int kind, const uint16_t *A, const uint8_t *Wq, const void *scales,
+                   int64_t G, const uint16_t *C, const uint16_t *bias,
+                   const uint16_t *residual, int64_t M, int64_t N, int64_t K,
+                   double alpha, double beta, int act, const int64_t *idx_m,
+                   const int64_t *idx_n, int64_t count, uint16_t *out_bf16,
+                   double *out_f64)
+{
+    if (M < 0 || !wq_args_ok(kind, G, N, K))
+        return -1;
+    if (!idx_m && count != M * N)
+        return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t m, n;
+        elem(idx_m, idx_n, N, i, &m, &n);
+        if (m < 0 || m >= M || n < 0 || n >= N)
+            return -1;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += oracle_bf16_to_f64(A[m * K + k]) * wq_at(kind, Wq, scales, G, N, k, n);
+        emit(i, epilogue(acc, C, bias, residual, N, m, n, alpha, beta, act),
+             out_bf16, out_f64);
+    }
+    return 0;
+}
+
+/* The dequantised weight of any format on its own, K x N bf16. */
+int oracle_wq_dequant(int kind, const uint8_t *Wq, const void *scales, int64_t G,
+                      int64_t K, int64_t N, uint16_t *w_out)
+{
+    if (!wq_args_ok(kind, G, N, K))
+        return -1;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n)
+            w_out[k * N + n] = oracle_bf16_from_f64(wq_at(kind, Wq, scales, G, N, k, n));
     return 0;
 }
 

@@ -484,3 +484,96 @@ def test_mlp_chain_unfused_mode_rounds_every_intermediate():
     assert np.array_equal(h, oracle.swiglu_pointwise(gb, ub, M=M, N=F))
     db = _bf16_from_f64_torch(f(h) @ f(wd).T)
     assert np.array_equal(out, oracle.pointwise_epilogue(db, residual=r, M=M, N=D))
+
+
+# ---------------------------------------------------------------- FP8 / NVFP4 weights
+
+# FP4 E2M1 element values by code 0..7 (OCP Microscaling Formats v1.0, FP4
+# E2M1: sign bit, 2 exponent bits with bias 1, 1 mantissa bit; code 1 is the
+# subnormal 0.5); codes 8..15 are their negatives.
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_fp8_e4m3_decode_matches_torch_for_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.fp8_e4m3_to_f64(c) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.isnan(got).sum() == 2  # S.1111.111 only
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def test_fp4_e2m1_decode_table_and_symmetry():
+    got = [oracle.fp4_e2m1_to_f64(c) for c in range(16)]
+    assert got[:8] == E2M1
+    assert got[8:] == [-v for v in E2M1]
+    assert math.copysign(1.0, got[8]) == -1.0  # code 8 is -0
+    # every E2M1 value is an exact E4M3 value (the scale format holds them all)
+    e4 = {oracle.fp8_e4m3_to_f64(c) for c in range(256)}
+    assert all(v in e4 for v in got)
+
+
+def _wq_setup(seed, M, N, K):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    A = to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    return rng, A
+
+
+def test_wq_gemm_int4_kind_equals_w4a16():
+    rng, A = _wq_setup(31, 5, 32, 256)
+    Wq = rng.integers(0, 256, size=(256, 16), dtype=np.uint8)
+    s = to_bf16_bits(rng.uniform(0.01, 0.05, size=(2, 32)).astype(np.float32))
+    a = oracle.wq_gemm("int4", A, Wq, s, 128, M=5, N=32, K=256, act="silu", alpha=0.5)
+    b = oracle.w4a16(A, Wq, s, 128, M=5, N=32, K=256, act="silu", alpha=0.5)
+    assert np.array_equal(a, b)
+
+
+def test_fp8_weights_match_torch_decode_then_numpy_matmul():
+    M, N, K, G = 6, 24, 192, 64
+    rng, A = _wq_setup(32, M, N, K)
+    Wq = rng.integers(0, 256, size=(K, N), dtype=np.uint8)
+    Wq[(Wq & 0x7F) == 0x7F] = 0x3C  # no NaN codes in a weight
+    s = to_bf16_bits(rng.uniform(0.01, 0.1, size=(K // G, N)).astype(np.float32))
+    q = torch.from_numpy(Wq).view(torch.float8_e4m3fn).double()
+    sc = torch.from_numpy(oracle.bf16_bits_to_f64(s)).repeat_interleave(G, dim=0)
+    w = (q * sc).to(torch.bfloat16).double().numpy()  # 12 significant bits: one rounding
+    want = oracle.bf16_bits_to_f64(A) @ w
+    _, got = oracle.wq_gemm("fp8", A, Wq, s, G, M=M, N=N, K=K, want_f64=True)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(oracle.dequant_wq("fp8", Wq, s, G, K=K, N=N),
+                          workloads_bf16(w))
+
+
+@pytest.mark.parametrize("k0,n0,code", [(0, 0, 0x3), (17, 5, 0xE), (47, 30, 0x1), (63, 31, 0x9)])
+def test_nvfp4_single_code_probe_fixes_nibble_order_and_block_scale(k0, n0, code):
+    M, N, K = 3, 32, 64
+    _, A = _wq_setup(33, M, N, K)
+    Wq = np.zeros((K, N // 2), dtype=np.uint8)
+    Wq[k0, n0 // 2] = (code << 4) if n0 % 2 == 0 else code
+    # block scales 2^-1, 2^0, 2^1, 2^2 for k-blocks 0..3 (E4M3 codes 0x30, 0x38, 0x40, 0x48)
+    S = np.zeros((K // 16, N), dtype=np.uint8)
+    for b, c in enumerate((0x30, 0x38, 0x40, 0x48)):
+        S[b, :] = c
+    out = oracle.wq_gemm("nvfp4", A, Wq, S, M=M, N=N, K=K, want_f64=True)[1]
+    v = (E2M1[code & 7] * (-1 if code & 8 else 1)) * 2.0 ** (k0 // 16 - 1)
+    want = np.zeros((M, N))
+    want[:, n0] = oracle.bf16_bits_to_f64(A)[:, k0] * v
+    assert np.array_equal(out, want)
+
+
+def test_nvfp4_alpha_is_the_per_tensor_scale():
+    M, N, K = 4, 16, 32
+    rng, A = _wq_setup(34, M, N, K)
+    Wq = rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+    S = rng.integers(0x28, 0x50, size=(K // 16, N), dtype=np.uint8)
+    _, one = oracle.wq_gemm("nvfp4", A, Wq, S, M=M, N=N, K=K, want_f64=True)
+    _, quarter = oracle.wq_gemm("nvfp4", A, Wq, S, M=M, N=N, K=K, alpha=0.25, want_f64=True)
+    assert np.array_equal(quarter, one * 0.25)
+    # the weight is exact: E2M1 x E4M3 needs at most 6 significant bits
+    w = oracle.dequant_wq("nvfp4", Wq, S, K=K, N=N)
+    codes = np.stack([(Wq >> 4) & 0xF, Wq & 0xF], axis=-1).reshape(K, N)
+    vals = np.array([oracle.fp4_e2m1_to_f64(c) for c in range(16)])[codes]
+    sv = np.array([oracle.fp8_e4m3_to_f64(c) for c in range(256)])[S].repeat(16, axis=0)
+    assert np.array_equal(oracle.bf16_bits_to_f64(w), vals * sv)
