@@ -73,26 +73,36 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha() -> str:
+KERNEL_SOURCE = {"gemm_pair_kernel": "gemm_pair.cu", "gemm_persistent_kernel": "gemm_tc.cu",
+                 "gemm_swap_kernel": "gemm_tc.cu", "w4a16_kernel": "w4a16.cu",
+                 "add_rmsnorm_kernel": "rmsnorm.cu", "swiglu_pointwise_kernel": "pointwise.cu"}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the sources a kernel is built from: its own .cu file, the
+    shared headers and the launch planner."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tcgen05_tmem_bf16_gb300", "csrc")
+    own = KERNEL_SOURCE.get(kernel)
     for name in sorted(os.listdir(csrc)):
+        if name.endswith(".cu") and name not in (own, "api.cu"):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the dominant kernel from a committed ncu
-    capture, if it was taken on the current kernel sources."""
+    capture, if it was taken on the kernel's current sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("kernel") != kernel or e.get("source_sha") != kernel_source_sha(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -716,14 +726,17 @@ def main(argv=None):
         achieved = dom_counts.fused_bytes / per_launch_dom / 1e9
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
+    kname = {"persistent": "gemm_persistent_kernel", "swap_splitk": "gemm_swap_kernel",
+             "w4a16": "w4a16_kernel", "pair": "gemm_pair_kernel",
+             "add_rmsnorm": "add_rmsnorm_kernel",
+             "swiglu_pointwise": "swiglu_pointwise_kernel"}.get(wl.path, wl.path)
     roof = {"bound": bnd, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+            "frac": achieved / peak, "traffic": recorded_traffic(args.workload, kname),
             "peak_source": (f"{peak_src}: " + ("bf16_tflops_sustained (back-to-back loop)"
                                                if bnd == "tensor" and long_loop else
                                                ("bf16_tflops (burst)" if bnd == "tensor"
                                                 else "hbm_gbs"))),
-            "kernel": {"persistent": "gemm_persistent_kernel", "swap_splitk": "gemm_swap_kernel",
-                       "w4a16": "w4a16_kernel", "pair": "gemm_pair_kernel"}.get(wl.path, wl.path),
+            "kernel": kname,
             "splits": wl.splits,
             "kernel_ms": per_launch_dom * 1e3,
             "algorithmic_flops": dom_counts.flops, "algorithmic_bytes": dom_counts.fused_bytes,
