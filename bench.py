@@ -56,6 +56,9 @@ WORKLOAD_TEXT = {
     "prefill": "prefill projection A[4096x4096] x W[4096x4096]^T + bias + residual, bf16",
     "swiglu": "gate/up SwiGLU dual GEMM x[2048x4096], Wg,Wu[14336x4096], bf16",
     "w4a16": "W4A16 decode GEMM A[16x8192] x int4 W[8192x28672], group 128",
+    "w8a16_fp8": "FP8-weight decode GEMM A[16x8192] x E4M3 W[8192x28672], bf16 scales per 128",
+    "w4a16_nvfp4": "NVFP4-weight decode GEMM A[16x8192] x E2M1 W[8192x28672], E4M3 scales "
+                   "per 16, per-tensor factor 1/256",
     "tiny": "tiny fused GEMM 64x256x128, SiLU(0.5AB + C + bias)",
     "mlp_decode": "gated MLP block + residual at decode, x[16x4096], Wg,Wu[14336x4096], "
                   "Wd[4096x14336], bf16, replayed from one CUDA graph",
@@ -74,7 +77,7 @@ def load_peaks():
 
 
 KERNEL_SOURCE = {"gemm_pair_kernel": "gemm_pair.cu", "gemm_persistent_kernel": "gemm_tc.cu",
-                 "gemm_swap_kernel": "gemm_tc.cu", "w4a16_kernel": "w4a16.cu",
+                 "gemm_swap_kernel": "gemm_tc.cu", "wq_gemm_kernel": "wq_gemm.cu",
                  "add_rmsnorm_kernel": "rmsnorm.cu", "swiglu_pointwise_kernel": "pointwise.cu"}
 
 
@@ -208,7 +211,7 @@ def describe(w: dict) -> dict:
         d["eps"] = w["eps"]
     if "layout" in w:
         d["b_layout"] = w["layout"]
-    if w["op"] == "w4a16":
+    if w["op"] in ("w4a16", "w8a16_fp8", "w4a16_nvfp4"):
         d["group_size"] = w["group"]
     d.update(alpha=w["alpha"], beta=w["beta"], act=w["act"])
     return d
@@ -265,7 +268,8 @@ class Workload:
                 d["resid"] = torch.empty(self.M, self.N, dtype=torch.bfloat16, device=dev)
             self.sets.append(d)
         gemm_op = {"gemm": "gemm_epilogue", "swiglu": "swiglu", "w4a16": "w4a16",
-                   "mlp": "mlp"}.get(self.op)
+                   "mlp": "mlp", "w8a16_fp8": "w8a16_fp8",
+                   "w4a16_nvfp4": "w4a16_nvfp4"}.get(self.op)
         wK = w["F"] if self.op == "mlp" else self.K
         ws = gbf.gbf_workspace_size(gemm_op, self.M, self.N, wK, False) if gemm_op else 0
         self.ws_bytes = ws
@@ -330,6 +334,14 @@ class Workload:
             gbf.w4a16_gemm(s["A"], s["Wq"], s["scales"], w["group"], s.get("C"), s.get("bias"),
                            s.get("residual"), s["out"], self.M, self.N, self.K, w["alpha"],
                            w["beta"], w["act"], stream=stream)
+        elif self.op == "w8a16_fp8":
+            gbf.w8a16_fp8_gemm(s["A"], s["Wq"], s["scales"], w["group"], None, None, None,
+                               s["out"], self.M, self.N, self.K, w["alpha"], w["beta"],
+                               w["act"], stream=stream)
+        elif self.op == "w4a16_nvfp4":
+            gbf.w4a16_nvfp4_gemm(s["A"], s["Wq"], s["scales"], None, None, None, s["out"],
+                                 self.M, self.N, self.K, w["alpha"], w["beta"], w["act"],
+                                 stream=stream)
         elif self.op == "add_rmsnorm":
             gbf.add_rmsnorm(s["a"], s["x"], s["weight"], s["out"], s["resid"], self.M, self.N,
                             w["eps"], stream=stream)
@@ -358,6 +370,14 @@ class Workload:
             gbf.w4a16_gemm_unfused(s["A"], s["Wq"], s["scales"], w["group"], s.get("C"),
                                    s.get("bias"), s.get("residual"), s["out"], self.M, self.N,
                                    self.K, w["alpha"], w["beta"], w["act"], **kw)
+        elif self.op == "w8a16_fp8":
+            gbf.w8a16_fp8_gemm_unfused(s["A"], s["Wq"], s["scales"], w["group"], None, None,
+                                       None, s["out"], self.M, self.N, self.K, w["alpha"],
+                                       w["beta"], w["act"], **kw)
+        elif self.op == "w4a16_nvfp4":
+            gbf.w4a16_nvfp4_gemm_unfused(s["A"], s["Wq"], s["scales"], None, None, None,
+                                         s["out"], self.M, self.N, self.K, w["alpha"],
+                                         w["beta"], w["act"], **kw)
         elif self.op == "add_rmsnorm":
             gbf.add_rmsnorm_unfused(s["a"], s["x"], s["weight"], s["out"], s["resid"], self.M,
                                     self.N, w["eps"], stream=stream)
@@ -376,6 +396,8 @@ class Workload:
         return {"gemm": "GEMM -> bf16 D in HBM -> pointwise kernel",
                 "swiglu": "two GEMMs -> bf16 g, u in HBM -> GLU pointwise kernel",
                 "w4a16": "dequantise kernel -> bf16 W in HBM -> bf16 GEMM",
+                "w8a16_fp8": "dequantise kernel -> bf16 W in HBM -> bf16 GEMM",
+                "w4a16_nvfp4": "dequantise kernel -> bf16 W in HBM -> bf16 GEMM",
                 "add_rmsnorm": "residual-add kernel -> bf16 r in HBM -> RMSNorm kernel"}[self.op]
 
     def e2e_step(self, stream):
@@ -445,6 +467,10 @@ def oracle_elements(w: dict, rows, cols):
         oracle.swiglu(w["x"], w["w_gate"], w["w_up"], w["layout"], w.get("C"), M=M, N=N,
                       K=K, alpha=w["alpha"], beta=w["beta"], act=w["act"], rows=rows,
                       cols=cols)
+    elif op in ("w8a16_fp8", "w4a16_nvfp4"):
+        oracle.wq_gemm("fp8" if op == "w8a16_fp8" else "nvfp4", w["A"], w["Wq"], w["scales"],
+                       w["group"], M=M, N=N, K=K, alpha=w["alpha"], beta=w["beta"],
+                       act=w["act"], rows=rows, cols=cols)
     else:
         oracle.w4a16(w["A"], w["Wq"], w["scales"], w["group"], w.get("C"), w.get("bias"),
                      w.get("residual"), M=M, N=N, K=K, alpha=w["alpha"], beta=w["beta"],
@@ -727,7 +753,7 @@ def main(argv=None):
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     kname = {"persistent": "gemm_persistent_kernel", "swap_splitk": "gemm_swap_kernel",
-             "w4a16": "w4a16_kernel", "pair": "gemm_pair_kernel",
+             "w4a16": "wq_gemm_kernel", "pair": "gemm_pair_kernel",
              "add_rmsnorm": "add_rmsnorm_kernel",
              "swiglu_pointwise": "swiglu_pointwise_kernel"}.get(wl.path, wl.path)
     roof = {"bound": bnd, "achieved": achieved, "peak": peak, "unit": unit,

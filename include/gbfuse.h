@@ -77,6 +77,8 @@ typedef int gbf_status_t;
 #define GBF_OP_SWIGLU 1
 #define GBF_OP_W4A16 2
 #define GBF_OP_MLP 3 /* gbf_workspace_size(GBF_OP_MLP, M, D, F, fused) */
+#define GBF_OP_W8A16_FP8 4
+#define GBF_OP_W4A16_NVFP4 5
 
 /*
  * gemm_epilogue -- out[M][N] = bf16( act(alpha * A*B~ + beta*C + bias) + residual )
@@ -124,6 +126,41 @@ GBF_API gbf_status_t w4a16_gemm(const void *A, const uint8_t *Wq, const void *sc
                         const void *C, const void *bias, const void *residual, void *out,
                         int64_t M, int64_t N, int64_t K, float alpha, float beta, int act,
                         void *workspace, size_t workspace_bytes, gbf_stream_t stream);
+
+/*
+ * w8a16_fp8_gemm -- the gemm_epilogue result with
+ *   B~[k][n] = bf16( e4m3(Wq[k][n]) * s[k/G][n] ), dequantised on-chip: FP8
+ *   weight-only quantisation with bf16 activations ("Fusion Thinking",
+ *   Pattern 3 names INT8/FP8-class weight-only formats with BF16 activations;
+ *   "Fusion and Epilogues" lists FP8 GEMM paths).
+ *   Wq     [K][N] bytes, each an OCP FP8 E4M3 code (bias 7, subnormals,
+ *          S.1111.111 = NaN; NaN codes are not valid weights and give an
+ *          unspecified result).
+ *   scales [K/group_size][N] bf16; group_size a multiple of 64 dividing K
+ *          (group_size == K: one scale per output channel).
+ *   The one rounding is the product e4m3 * s to bf16 (round to nearest even).
+ *   Requires N % 32 == 0.  Workspace unused (NULL, 0).
+ *
+ * w4a16_nvfp4_gemm -- the gemm_epilogue result with
+ *   B~[k][n] = e2m1(q[k][n]) * e4m3(S[k/16][n])   (exact in bf16),
+ *   NVFP4 weight-only quantisation with bf16 activations ("Fusion Thinking",
+ *   Pattern 3: "INT4 / INT8 / NVFP4 weights, BF16 activations").
+ *   Wq     [K][N/2] bytes of OCP FP4 E2M1 codes, packed like w4a16_gemm's
+ *          (column 2j in the HIGH nibble of byte j).
+ *   scales [K/16][N] bytes, each an E4M3 factor for 16 consecutive k.
+ *   The format's per-tensor factor is alpha (it multiplies the product).
+ *   Requires K % 16 == 0 and N % 32 == 0.  Workspace unused (NULL, 0).
+ */
+GBF_API gbf_status_t w8a16_fp8_gemm(const void *A, const uint8_t *Wq, const void *scales,
+                                    int group_size, const void *C, const void *bias,
+                                    const void *residual, void *out, int64_t M, int64_t N,
+                                    int64_t K, float alpha, float beta, int act, void *workspace,
+                                    size_t workspace_bytes, gbf_stream_t stream);
+GBF_API gbf_status_t w4a16_nvfp4_gemm(const void *A, const uint8_t *Wq, const uint8_t *scales,
+                                      const void *C, const void *bias, const void *residual,
+                                      void *out, int64_t M, int64_t N, int64_t K, float alpha,
+                                      float beta, int act, void *workspace,
+                                      size_t workspace_bytes, gbf_stream_t stream);
 
 /*
  * swiglu_pointwise -- the level-1 fused gated ending on its own:
@@ -200,6 +237,8 @@ GBF_API gbf_status_t mlp_swiglu_down_unfused(const void *x, const void *w_gate,
  *                           [M][N] at align256(2*M*N), then the GLU pass.
  *   w4a16_gemm_unfused      w = bf16((q-8)*s) [K][N] at 0, then a bf16
  *                           GEMM with the fused ending (identical result).
+ *   w8a16_fp8_gemm_unfused, w4a16_nvfp4_gemm_unfused   the same with the
+ *                           FP8 / NVFP4 weight dequantised into [K][N] bf16.
  * The workspace contents are left in place after the call.
  */
 GBF_API gbf_status_t gemm_epilogue_unfused(const void *A, const void *B, int b_layout, const void *C,
@@ -217,6 +256,18 @@ GBF_API gbf_status_t w4a16_gemm_unfused(const void *A, const uint8_t *Wq, const 
                                 const void *residual, void *out, int64_t M, int64_t N,
                                 int64_t K, float alpha, float beta, int act, void *workspace,
                                 size_t workspace_bytes, gbf_stream_t stream);
+GBF_API gbf_status_t w8a16_fp8_gemm_unfused(const void *A, const uint8_t *Wq,
+                                            const void *scales, int group_size, const void *C,
+                                            const void *bias, const void *residual, void *out,
+                                            int64_t M, int64_t N, int64_t K, float alpha,
+                                            float beta, int act, void *workspace,
+                                            size_t workspace_bytes, gbf_stream_t stream);
+GBF_API gbf_status_t w4a16_nvfp4_gemm_unfused(const void *A, const uint8_t *Wq,
+                                              const uint8_t *scales, const void *C,
+                                              const void *bias, const void *residual, void *out,
+                                              int64_t M, int64_t N, int64_t K, float alpha,
+                                              float beta, int act, void *workspace,
+                                              size_t workspace_bytes, gbf_stream_t stream);
 
 /*
  * gemm_epilogue_unfused_noalloc -- the gemm_epilogue_unfused result for a

@@ -9,6 +9,10 @@ there is no CPU fallback, and a missing library is an error.
   gemm_epilogue      out = act(alpha*A*B + beta*C + bias) + residual
   swiglu_dual_gemm   h = act(alpha*x*Wg) * (alpha*x*Wu) + beta*C
   w4a16_gemm         gemm_epilogue with int4 weights dequantised on-chip
+  w8a16_fp8_gemm     the same with FP8 (E4M3) weights and bf16 group scales
+  w4a16_nvfp4_gemm   the same with NVFP4 (E2M1 + E4M3 block scales) weights
+  mlp_swiglu_down    gate/up GEMM -> bf16 h -> down GEMM + residual
+  add_rmsnorm        fused residual add + RMSNorm
   *_unfused          the same results as GEMM -> HBM -> pointwise kernel
 """
 from __future__ import annotations
@@ -21,7 +25,7 @@ from . import build as _build
 
 ACT = {"identity": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
 LAYOUT = {"kn": 0, "nk": 1}
-OP = {"gemm_epilogue": 0, "swiglu": 1, "w4a16": 2, "mlp": 3}
+OP = {"gemm_epilogue": 0, "swiglu": 1, "w4a16": 2, "mlp": 3, "w8a16_fp8": 4, "w4a16_nvfp4": 5}
 STATUS = {0: "GBF_OK", 1: "GBF_ERR_INVALID_ARG", 2: "GBF_ERR_MISALIGNED",
           3: "GBF_ERR_UNSUPPORTED_SHAPE", 4: "GBF_ERR_WORKSPACE", 5: "GBF_ERR_CUDA",
           6: "GBF_ERR_TIMEOUT", 7: "GBF_ERR_NO_DEVICE"}
@@ -33,7 +37,8 @@ EXPORTS = ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unf
            "gbf_debug_inject_timeout", "gbf_kernel_path", "gbf_version",
            "gemm_epilogue_unfused_noalloc", "gbf_debug_force_splits", "gbf_debug_set_profile",
            "swiglu_pointwise", "add_rmsnorm", "add_rmsnorm_unfused", "mlp_swiglu_down",
-           "mlp_swiglu_down_unfused")
+           "mlp_swiglu_down_unfused", "w8a16_fp8_gemm", "w8a16_fp8_gemm_unfused",
+           "w4a16_nvfp4_gemm", "w4a16_nvfp4_gemm_unfused")
 
 _lock = threading.Lock()
 _lib = None
@@ -68,7 +73,10 @@ def load(path: str | None = None):
         for name, args in (("gemm_epilogue", gemm_args), ("gemm_epilogue_unfused", gemm_args),
                            ("swiglu_dual_gemm", swiglu_args),
                            ("swiglu_dual_gemm_unfused", swiglu_args),
-                           ("w4a16_gemm", w4_args), ("w4a16_gemm_unfused", w4_args)):
+                           ("w4a16_gemm", w4_args), ("w4a16_gemm_unfused", w4_args),
+                           ("w8a16_fp8_gemm", w4_args), ("w8a16_fp8_gemm_unfused", w4_args),
+                           ("w4a16_nvfp4_gemm", w4_args[:3] + w4_args[4:]),
+                           ("w4a16_nvfp4_gemm_unfused", w4_args[:3] + w4_args[4:])):
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = I
@@ -235,6 +243,44 @@ def w4a16_gemm_unfused(A, Wq, scales, group_size, C, bias, residual, out, M, N, 
                                    _p(residual), _p(out), M, N, K, alpha, beta,
                                    _code(act, ACT), _p(workspace), workspace_bytes, _s(stream))
     return _check(st, "w4a16_gemm_unfused", raise_on_error)
+
+
+def w8a16_fp8_gemm(A, Wq, scales, group_size, C, bias, residual, out, M, N, K, alpha=1.0,
+                   beta=0.0, act="identity", workspace=None, workspace_bytes=0, stream=None,
+                   raise_on_error=True):
+    st = load().w8a16_fp8_gemm(_p(A), _p(Wq), _p(scales), group_size, _p(C), _p(bias),
+                               _p(residual), _p(out), M, N, K, alpha, beta, _code(act, ACT),
+                               _p(workspace), workspace_bytes, _s(stream))
+    return _check(st, "w8a16_fp8_gemm", raise_on_error)
+
+
+def w8a16_fp8_gemm_unfused(A, Wq, scales, group_size, C, bias, residual, out, M, N, K,
+                           alpha=1.0, beta=0.0, act="identity", workspace=None,
+                           workspace_bytes=0, stream=None, raise_on_error=True):
+    st = load().w8a16_fp8_gemm_unfused(_p(A), _p(Wq), _p(scales), group_size, _p(C), _p(bias),
+                                       _p(residual), _p(out), M, N, K, alpha, beta,
+                                       _code(act, ACT), _p(workspace), workspace_bytes,
+                                       _s(stream))
+    return _check(st, "w8a16_fp8_gemm_unfused", raise_on_error)
+
+
+def w4a16_nvfp4_gemm(A, Wq, scales, C, bias, residual, out, M, N, K, alpha=1.0, beta=0.0,
+                     act="identity", workspace=None, workspace_bytes=0, stream=None,
+                     raise_on_error=True):
+    st = load().w4a16_nvfp4_gemm(_p(A), _p(Wq), _p(scales), _p(C), _p(bias), _p(residual),
+                                 _p(out), M, N, K, alpha, beta, _code(act, ACT), _p(workspace),
+                                 workspace_bytes, _s(stream))
+    return _check(st, "w4a16_nvfp4_gemm", raise_on_error)
+
+
+def w4a16_nvfp4_gemm_unfused(A, Wq, scales, C, bias, residual, out, M, N, K, alpha=1.0,
+                             beta=0.0, act="identity", workspace=None, workspace_bytes=0,
+                             stream=None, raise_on_error=True):
+    st = load().w4a16_nvfp4_gemm_unfused(_p(A), _p(Wq), _p(scales), _p(C), _p(bias),
+                                         _p(residual), _p(out), M, N, K, alpha, beta,
+                                         _code(act, ACT), _p(workspace), workspace_bytes,
+                                         _s(stream))
+    return _check(st, "w4a16_nvfp4_gemm_unfused", raise_on_error)
 
 
 def gbf_workspace_size(op, M, N, K, fused) -> int:

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgbfuse.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_pair.cu", "w4a16.cu", "pointwise.cu", "rmsnorm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_pair.cu", "wq_gemm.cu", "pointwise.cu", "rmsnorm.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "common.cuh", "internal.h", "epilogue.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -203,23 +203,29 @@ gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, 
                                  make_ctl(err, plan_ctas(plan)), stream));
 }
 
-gbf_status_t run_w4(const void* A, const uint8_t* Wq, const void* scales, int group,
+// Weight-only quantised GEMM launch after validation (fmt: WqFmt).
+gbf_status_t run_w4(int fmt, const void* A, const uint8_t* Wq, const void* scales, int group,
                     const EpiParams& ep, int64_t M, int64_t N, int64_t K, const DeviceInfo& dev,
                     unsigned* err, cudaStream_t stream) {
   if (M == 0 || N == 0) return GBF_OK;
   if (K == 0) return cuda_status(launch_pointwise_epilogue(nullptr, ep, M, N, dev.sms, stream));
   const GemmPlan plan = plan_w4a16(M, N, K, dev);
   CUtensorMap tmA, tmQ, tmS;
-  if (!tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, kBK, plan.mpad,
-               CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tmap_2d(&tmQ, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, N / 2, K, N / 2, kW4BN / 2, kBK,
-               CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !tmap_2d(&tmS, scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, K / group, N * 2, 256, 1,
-               CU_TENSOR_MAP_SWIZZLE_NONE))
-    return GBF_ERR_CUDA;
-  return cuda_status(launch_w4a16(plan, tmA, tmQ, tmS, ep, static_cast<int>(M),
-                                  static_cast<int>(N), static_cast<int>(K), group,
-                                  make_ctl(err, plan_ctas(plan)), stream));
+  const bool fp8 = fmt == kWqFp8;
+  const bool nv = fmt == kWqNvfp4;
+  const int64_t qcols = fp8 ? N : N / 2;  // weight bytes per k-row
+  bool ok = tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, kBK, plan.mpad,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+            tmap_2d(&tmQ, Wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, qcols, K, qcols, 256, kBK,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && (nv ? tmap_2d(&tmS, scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, N, K / 16, N, 256,
+                           kBK / 16, CU_TENSOR_MAP_SWIZZLE_NONE)
+                 : tmap_2d(&tmS, scales, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, K / group, N * 2,
+                           256, 1, CU_TENSOR_MAP_SWIZZLE_NONE));
+  if (!ok) return GBF_ERR_CUDA;
+  return cuda_status(launch_wq_gemm(fmt, plan, tmA, tmQ, tmS, ep, static_cast<int>(M),
+                                    static_cast<int>(N), static_cast<int>(K), group,
+                                    make_ctl(err, plan_ctas(plan)), stream));
 }
 
 gbf_status_t check_w4(int64_t M, int64_t N, int64_t K, int group, int act) {
@@ -227,6 +233,14 @@ gbf_status_t check_w4(int64_t M, int64_t N, int64_t K, int group, int act) {
   if (st != GBF_OK) return st;
   if (group <= 0) return GBF_ERR_INVALID_ARG;
   if (group % kBK != 0 || K % group != 0 || N % 32 != 0) return GBF_ERR_UNSUPPORTED_SHAPE;
+  return GBF_OK;
+}
+
+// NVFP4: blocks of 16 along K; packed rows of N/2 bytes.
+gbf_status_t check_nvfp4(int64_t M, int64_t N, int64_t K, int act) {
+  gbf_status_t st = check_common(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if (K % 16 != 0 || N % 32 != 0) return GBF_ERR_UNSUPPORTED_SHAPE;
   return GBF_OK;
 }
 
@@ -335,8 +349,43 @@ gbf_status_t w4a16_gemm(const void* A, const uint8_t* Wq, const void* scales, in
   const DeviceInfo* dev;
   unsigned* err;
   if ((st = current_device(&dev, &err)) != GBF_OK) return st;
-  return run_w4(A, Wq, scales, group_size, make_ep(C, bias, residual, out, alpha, beta, act), M,
-                N, K, *dev, err, reinterpret_cast<cudaStream_t>(stream));
+  return run_w4(kWqInt4, A, Wq, scales, group_size,
+                make_ep(C, bias, residual, out, alpha, beta, act), M, N, K, *dev, err,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+gbf_status_t w8a16_fp8_gemm(const void* A, const uint8_t* Wq, const void* scales,
+                            int group_size, const void* C, const void* bias,
+                            const void* residual, void* out, int64_t M, int64_t N, int64_t K,
+                            float alpha, float beta, int act, void* workspace,
+                            size_t workspace_bytes, gbf_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  gbf_status_t st = check_w4(M, N, K, group_size, act);
+  if (st != GBF_OK) return st;
+  if ((st = check_ptrs({A, Wq, scales, out}, {C, bias, residual})) != GBF_OK) return st;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  return run_w4(kWqFp8, A, Wq, scales, group_size,
+                make_ep(C, bias, residual, out, alpha, beta, act), M, N, K, *dev, err,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+gbf_status_t w4a16_nvfp4_gemm(const void* A, const uint8_t* Wq, const uint8_t* scales,
+                              const void* C, const void* bias, const void* residual, void* out,
+                              int64_t M, int64_t N, int64_t K, float alpha, float beta, int act,
+                              void* workspace, size_t workspace_bytes, gbf_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  gbf_status_t st = check_nvfp4(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if ((st = check_ptrs({A, Wq, scales, out}, {C, bias, residual})) != GBF_OK) return st;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  return run_w4(kWqNvfp4, A, Wq, scales, 16, make_ep(C, bias, residual, out, alpha, beta, act),
+                M, N, K, *dev, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gbf_status_t swiglu_pointwise(const void* g, const void* u, const void* C, void* h, int64_t M,
@@ -414,7 +463,9 @@ size_t gbf_workspace_size(int op, int64_t M, int64_t N, int64_t K, int fused) {
   switch (op) {
     case GBF_OP_GEMM_EPILOGUE: return align256(static_cast<size_t>(M * N) * 2);
     case GBF_OP_SWIGLU: return 2 * align256(static_cast<size_t>(M * N) * 2);
-    case GBF_OP_W4A16: return align256(static_cast<size_t>(K * N) * 2);
+    case GBF_OP_W4A16:
+    case GBF_OP_W8A16_FP8:
+    case GBF_OP_W4A16_NVFP4: return align256(static_cast<size_t>(K * N) * 2);
     default: return 0;
   }
 }
@@ -503,6 +554,55 @@ gbf_status_t w4a16_gemm_unfused(const void* A, const uint8_t* Wq, const void* sc
   __nv_bfloat16* w = static_cast<__nv_bfloat16*>(workspace);
   if ((st = cuda_status(launch_dequant_int4(Wq, static_cast<const __nv_bfloat16*>(scales),
                                             group_size, K, N, w, dev->sms, s))) != GBF_OK)
+    return st;
+  return run_gemm(A, w, nullptr, GBF_B_KN, false, ep, M, N, K, *dev, err, s);
+}
+
+gbf_status_t w8a16_fp8_gemm_unfused(const void* A, const uint8_t* Wq, const void* scales,
+                                    int group_size, const void* C, const void* bias,
+                                    const void* residual, void* out, int64_t M, int64_t N,
+                                    int64_t K, float alpha, float beta, int act, void* workspace,
+                                    size_t workspace_bytes, gbf_stream_t stream) {
+  gbf_status_t st = check_w4(M, N, K, group_size, act);
+  if (st != GBF_OK) return st;
+  if ((st = check_ptrs({A, Wq, scales, out}, {C, bias, residual})) != GBF_OK) return st;
+  const size_t need = gbf_workspace_size(GBF_OP_W8A16_FP8, M, N, K, 0);
+  if (need && (!workspace || workspace_bytes < need)) return GBF_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return GBF_ERR_MISALIGNED;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || N == 0) return GBF_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const EpiParams ep = make_ep(C, bias, residual, out, alpha, beta, act);
+  if (K == 0) return cuda_status(launch_pointwise_epilogue(nullptr, ep, M, N, dev->sms, s));
+  __nv_bfloat16* w = static_cast<__nv_bfloat16*>(workspace);
+  if ((st = cuda_status(launch_dequant_fp8(Wq, static_cast<const __nv_bfloat16*>(scales),
+                                           group_size, K, N, w, dev->sms, s))) != GBF_OK)
+    return st;
+  return run_gemm(A, w, nullptr, GBF_B_KN, false, ep, M, N, K, *dev, err, s);
+}
+
+gbf_status_t w4a16_nvfp4_gemm_unfused(const void* A, const uint8_t* Wq, const uint8_t* scales,
+                                      const void* C, const void* bias, const void* residual,
+                                      void* out, int64_t M, int64_t N, int64_t K, float alpha,
+                                      float beta, int act, void* workspace,
+                                      size_t workspace_bytes, gbf_stream_t stream) {
+  gbf_status_t st = check_nvfp4(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if ((st = check_ptrs({A, Wq, scales, out}, {C, bias, residual})) != GBF_OK) return st;
+  const size_t need = gbf_workspace_size(GBF_OP_W4A16_NVFP4, M, N, K, 0);
+  if (need && (!workspace || workspace_bytes < need)) return GBF_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return GBF_ERR_MISALIGNED;
+  const DeviceInfo* dev;
+  unsigned* err;
+  if ((st = current_device(&dev, &err)) != GBF_OK) return st;
+  if (M == 0 || N == 0) return GBF_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const EpiParams ep = make_ep(C, bias, residual, out, alpha, beta, act);
+  if (K == 0) return cuda_status(launch_pointwise_epilogue(nullptr, ep, M, N, dev->sms, s));
+  __nv_bfloat16* w = static_cast<__nv_bfloat16*>(workspace);
+  if ((st = cuda_status(launch_dequant_nvfp4(Wq, scales, K, N, w, dev->sms, s))) != GBF_OK)
     return st;
   return run_gemm(A, w, nullptr, GBF_B_KN, false, ep, M, N, K, *dev, err, s);
 }
@@ -632,7 +732,12 @@ int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int* 
       p = plan_gemm(M, N, K, op == GBF_OP_SWIGLU, b_layout == GBF_B_KN, dev);
       break;
     case GBF_OP_W4A16:
-      if (check_w4(M, N, K, 128, 0) != GBF_OK) return -1;
+    case GBF_OP_W8A16_FP8:
+      if (check_w4(M, N, K, 64, 0) != GBF_OK) return -1;
+      p = plan_w4a16(M, N, K, dev);
+      break;
+    case GBF_OP_W4A16_NVFP4:
+      if (check_nvfp4(M, N, K, 0) != GBF_OK) return -1;
       p = plan_w4a16(M, N, K, dev);
       break;
     default: return -1;

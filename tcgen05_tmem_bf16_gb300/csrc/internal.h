@@ -71,11 +71,14 @@ cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const C
                              cudaStream_t stream);
 int max_active_pairs();
 
-// Weight-only int4 GEMM (w4a16.cu).  tmA: activations; tmQ: packed bytes
-// [K][N/2]; tmS: scales [K/G][N].
-cudaError_t launch_w4a16(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmQ,
-                         const CUtensorMap& tmS, const EpiParams& ep, int M, int N, int K,
-                         int group, const KernelCtl& ctl, cudaStream_t stream);
+// Weight-only quantised GEMM (wq_gemm.cu).  tmA: activations; tmQ: the
+// weight codes (int4, nvfp4: [K][N/2] bytes; fp8: [K][N]); tmS: scales
+// (int4, fp8: bf16 [K/G][N]; nvfp4: E4M3 bytes [K/16][N]).
+enum WqFmt { kWqInt4 = 0, kWqFp8 = 1, kWqNvfp4 = 2 };
+cudaError_t launch_wq_gemm(int fmt, const GemmPlan& plan, const CUtensorMap& tmA,
+                           const CUtensorMap& tmQ, const CUtensorMap& tmS, const EpiParams& ep,
+                           int M, int N, int K, int group, const KernelCtl& ctl,
+                           cudaStream_t stream);
 
 // Pointwise kernels of the unfused compositions (pointwise.cu).  D == null
 // means a zero product (used for K == 0).
@@ -87,6 +90,12 @@ cudaError_t launch_swiglu_pointwise(const __nv_bfloat16* g, const __nv_bfloat16*
 cudaError_t launch_dequant_int4(const uint8_t* Wq, const __nv_bfloat16* scales, int group,
                                 int64_t K, int64_t N, __nv_bfloat16* w, int sms,
                                 cudaStream_t stream);
+// FP8 (bf16 group scales) and NVFP4 (E4M3 block scales) weights -> bf16 [K][N].
+cudaError_t launch_dequant_fp8(const uint8_t* Wq, const __nv_bfloat16* scales, int group,
+                               int64_t K, int64_t N, __nv_bfloat16* w, int sms,
+                               cudaStream_t stream);
+cudaError_t launch_dequant_nvfp4(const uint8_t* Wq, const uint8_t* scales, int64_t K, int64_t N,
+                                 __nv_bfloat16* w, int sms, cudaStream_t stream);
 
 // Fused residual add + RMSNorm (rmsnorm.cu).  x == null: no add (plain
 // RMSNorm of a); resid == null: the residual is not written.  N <= 16384.

@@ -122,6 +122,85 @@ __global__ void __launch_bounds__(kPwThreads)
   }
 }
 
+// E4M3 byte -> float, exact: the sign and the 7 magnitude bits placed in a
+// binary32 with the code's exponent field in the low exponent bits give the
+// value times 2^-120 (subnormal codes land on binary32 subnormals with the
+// same factor); one exact multiply by 2^120 restores it.
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
+  const uint32_t bits = ((b & 0x80u) << 24) | ((b & 0x7Fu) << 20);
+  return __uint_as_float(bits) * 0x1p120f;
+}
+
+// E2M1 code (low 4 bits) -> float, exact, the same way with factor 2^-126.
+__device__ __forceinline__ float e2m1_to_float(uint32_t c) {
+  const uint32_t bits = ((c & 0x8u) << 28) | ((c & 0x7u) << 22);
+  return __uint_as_float(bits) * 0x1p126f;
+}
+
+// w[k][n] = bf16(e4m3(q[k][n]) * s[k/G][n]); the product is exact in fp32
+// (4 x 8 significant bits), so packing rounds once.
+__global__ void __launch_bounds__(kPwThreads)
+    dequant_fp8_kernel(const uint8_t* __restrict__ Wq, const __nv_bfloat16* __restrict__ s,
+                       int group, int64_t K, int64_t N, __nv_bfloat16* __restrict__ w) {
+  const int64_t vecs_per_row = N / 8;
+  const int64_t nvec = K * vecs_per_row;
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < nvec;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t k = v / vecs_per_row;
+    const int64_t n0 = (v % vecs_per_row) * 8;
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>(Wq + k * N + n0));
+    float sc[8];
+    unpack8(ldg_u4(s + (k / group) * N + n0), sc);
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[i] = e4m3_to_float((q.x >> (8 * i)) & 0xFFu) * sc[i];
+      x[4 + i] = e4m3_to_float((q.y >> (8 * i)) & 0xFFu) * sc[4 + i];
+    }
+    st_u4(w + k * N + n0, pack8(x));
+  }
+}
+
+// w[k][n] = e2m1(q[k][n]) * e4m3(S[k/16][n]), exact (at most 6 significant
+// bits); codes packed two per byte along N, column 2j in the high nibble.
+__global__ void __launch_bounds__(kPwThreads)
+    dequant_nvfp4_kernel(const uint8_t* __restrict__ Wq, const uint8_t* __restrict__ S,
+                         int64_t K, int64_t N, __nv_bfloat16* __restrict__ w) {
+  const int64_t vecs_per_row = N / 8;
+  const int64_t nvec = K * vecs_per_row;
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < nvec;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t k = v / vecs_per_row;
+    const int64_t n0 = (v % vecs_per_row) * 8;
+    const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(Wq + k * (N / 2) + n0 / 2));
+    const uint2 sb = __ldg(reinterpret_cast<const uint2*>(S + (k / 16) * N + n0));
+    float x[8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t byte = (word >> (8 * b)) & 0xFFu;
+      const uint32_t sw = b < 2 ? sb.x : sb.y;
+      const int sh = 16 * (b & 1);
+      x[2 * b] = e2m1_to_float(byte >> 4) * e4m3_to_float((sw >> sh) & 0xFFu);
+      x[2 * b + 1] = e2m1_to_float(byte & 0xFu) * e4m3_to_float((sw >> (sh + 8)) & 0xFFu);
+    }
+    st_u4(w + k * N + n0, pack8(x));
+  }
+}
+
+cudaError_t launch_dequant_fp8(const uint8_t* Wq, const __nv_bfloat16* scales, int group,
+                               int64_t K, int64_t N, __nv_bfloat16* w, int sms,
+                               cudaStream_t stream) {
+  dequant_fp8_kernel<<<pw_grid(K * N / 8, sms), kPwThreads, 0, stream>>>(Wq, scales, group, K,
+                                                                          N, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_nvfp4(const uint8_t* Wq, const uint8_t* scales, int64_t K, int64_t N,
+                                 __nv_bfloat16* w, int sms, cudaStream_t stream) {
+  dequant_nvfp4_kernel<<<pw_grid(K * N / 8, sms), kPwThreads, 0, stream>>>(Wq, scales, K, N, w);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pointwise_epilogue(const __nv_bfloat16* D, const EpiParams& ep, int64_t M,
                                       int64_t N, int sms, cudaStream_t stream) {
   const int grid = pw_grid(M * N / 8, sms);

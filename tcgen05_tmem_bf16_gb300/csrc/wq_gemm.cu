@@ -1,10 +1,20 @@
-// w4a16.cu -- weight-only int4 GEMM with on-chip dequantisation, sm_103a.
+// wq_gemm.cu -- weight-only quantised GEMM with on-chip dequantisation,
+// sm_103a: int4, FP8 (E4M3) and NVFP4 (E2M1) weights, bf16 activations.
 //
-// The kernel streams the packed int4 weights and their group scales into
-// shared memory with TMA, dequantises them on-chip to bf16, and feeds them to
-// the tensor cores; the bf16 weight matrix never exists in HBM ("Fusion
-// Thinking", Pattern 3, Dequant + GEMM: load INT4 weights + scales directly,
-// unpack the high and low nibbles, w = (q - 8) * s, accumulate a . w).
+// The kernel streams the packed weights and their scales into shared memory
+// with TMA, dequantises them on-chip to bf16, and feeds them to the tensor
+// cores; the bf16 weight matrix never exists in HBM ("Fusion Thinking",
+// Pattern 3, Dequant + GEMM: load the quantised weights + scales directly,
+// unpack, w = (q - 8) * s for int4, accumulate a . w; the same pattern names
+// NVFP4 weight-only quantisation with BF16 activations).
+//
+// Weight formats (FMT):
+//   int4   [K][N/2] bytes, two codes per byte along N (column 2j = high
+//          nibble of byte j); w = bf16((q - 8) * s[k/G][n]), bf16 scales.
+//   fp8    [K][N] E4M3 bytes; w = bf16(e4m3(q) * s[k/G][n]), bf16 scales.
+//   nvfp4  [K][N/2] E2M1 codes packed like int4; w = e2m1(q) * e4m3(S[k/16][n])
+//          (exact in bf16), E4M3 scale bytes [K/16][N]; the per-tensor
+//          factor is the caller's alpha.
 //
 // GB300 design.  out^T = W~^T * A^T: the weights are the MMA's A operand
 // (128 rows = output columns) and the few activation rows are its N.  The
@@ -14,11 +24,12 @@
 // carries only the half byte the TMA engine wrote and the transform threads
 // read once.
 //
-// Tile: 512 output columns.  Transform thread t (TMEM lane t) owns packed
-// bytes 2t and 2t+1 of every k-row, i.e. output columns n0+4t .. n0+4t+3
-// (high nibble of byte 2t, low nibble of 2t, high of 2t+1, low of 2t+1).
+// Tile: 512 output columns.  Transform thread t (TMEM lane t) owns output
+// columns n0+4t .. n0+4t+3 of every k-row: packed bytes 2t and 2t+1 for the
+// 4-bit formats (high nibble of byte 2t, low nibble of 2t, high of 2t+1, low
+// of 2t+1), bytes 4t .. 4t+3 for FP8.
 // Those four columns are four 128-lane A operands ("regions" 0..3), so each
-// thread writes only its own TMEM lane, a 16-bit shared-memory load per k-row
+// thread writes only its own TMEM lane, one shared-memory load per k-row
 // feeds four weights, and the epilogue stores four adjacent outputs at once.
 // One 64-deep K block = 16 MMAs (4 regions x 4 steps of 16).
 //
@@ -26,13 +37,20 @@
 // [32g, 32g+32) of every shared-memory stage into its own TMEM buffer, so
 // one group fills while the MMAs drain the other.
 //
-// Dequantisation of a nibble q, exact as the definition wants:
+// Dequantisation of an int4 code q, exact as the definition wants:
 //   bits 0x4300 | q  is the bf16 value 128 + q;
 //   (128 + q) - 136 = q - 8 exactly (small integers);
 //   (q - 8) * s with one bf16 multiply = bf16_rne((q - 8) * s).
 // For a k-row pair the two 16-bit loads are joined into X = row_k | row_k+1
 // << 16; the four regions are then (X >> 4), X, (X >> 12), (X >> 8) masked
 // with 0x000F000F -- each a bf16x2 pair (k, k+1) after OR-ing 0x43004300.
+// The floating-point codes are moved bit-wise into a bf16 whose exponent
+// field holds the code's exponent field: an E4M3 byte S.EEEE.MMM becomes the
+// bf16 S.0000EEEE.MMM0000 = value * 2^-120 and an E2M1 code S.EE.M the bf16
+// S.000000EE.M000000 = value * 2^-126 (the codes' subnormals land on bf16
+// subnormals with the same factor).  One exact bf16 multiply by 2^120 or
+// 2^126 restores the value, a second multiplies by the scale (exact for
+// NVFP4: at most 6 significant bits; the one rounding for FP8).
 //
 // K is split across a thread-block cluster; partial sums meet through
 // distributed shared memory and the ending is applied once.
@@ -49,17 +67,20 @@
 namespace gbf {
 
 constexpr int kW4Threads = 384;                 // warps 0-3 roles, 4-11 transform/epilogue
-constexpr int kW4RowBytes = kW4BN / 2;          // packed bytes per k-row of a tile: 256
-constexpr int kW4QBytes = kBK * kW4RowBytes;    // 16 KB packed tile per stage
-static_assert(kW4QBytes == 16384, "packed tile size");
 constexpr int kW4Regions = 4;
+constexpr uint32_t kBf16x2Pow120 = 0x7B807B80u;  // bf16x2 (2^120, 2^120)
+constexpr uint32_t kBf16x2Pow126 = 0x7E807E80u;  // bf16x2 (2^126, 2^126)
 
-template <int MPAD>
+template <int FMT, int MPAD>
 struct W4Cfg {
-  static constexpr int kXBytes = MPAD * kBK * 2;                 // activations, SW128
-  static constexpr int kScaleBytes = 1024;                       // 512 bf16
-  static constexpr int kStageBytes = kW4QBytes + kXBytes + kScaleBytes;
-  static constexpr int kStages = MPAD <= 16 ? 5 : 4;
+  static constexpr int kRowBytes = FMT == kWqFp8 ? kW4BN : kW4BN / 2;  // weight bytes per k-row
+  static constexpr int kQBytes = kBK * kRowBytes;                      // weight tile per stage
+  static constexpr int kXBytes = MPAD * kBK * 2;                       // activations, SW128
+  // int4 / fp8: one row of 512 bf16 group scales per stage (G % 64 == 0);
+  // nvfp4: four rows (k-blocks of 16) of 512 E4M3 bytes.
+  static constexpr int kScaleBytes = FMT == kWqNvfp4 ? 2048 : 1024;
+  static constexpr int kStageBytes = kQBytes + kXBytes + kScaleBytes;
+  static constexpr int kStages = FMT == kWqFp8 ? 3 : (MPAD <= 16 ? 5 : 4);
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
   static constexpr uint32_t kTmemCols = 256;
   // Accumulator sets: the 16-deep K steps alternate between kSets copies of
@@ -72,6 +93,7 @@ struct W4Cfg {
   static_assert(kColA + 128 <= kTmemCols, "TMEM budget");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static_assert(kStages * kStageBytes >= 128 * kW4Regions * MPAD * 4, "reduction buffer");
+  static_assert(kSmem <= 115 * 1024, "two CTAs per SM");
 };
 
 struct W4Args {
@@ -115,6 +137,115 @@ __device__ __forceinline__ void deq_rowpair(uint32_t x0, uint32_t x1, uint32_t c
       : "r"(x0), "r"(x1), "r"(c136), "r"(s0), "r"(s1), "r"(s2), "r"(s3));
 }
 
+// FP8 k-row pair: x0, x1 = the 32-bit loads (bytes = columns 4t..4t+3) of
+// rows k and k+1.  Region r: prmt puts byte r of each row into bytes 1 and 3
+// (the high byte of each half), the magnitude bits move down by 4 into the
+// bf16 exponent/mantissa fields, the sign bit stays at bit 15 / 31; then
+// x 2^120 (exact) and x s (the one rounding).
+__device__ __forceinline__ void deq_fp8_rowpair(uint32_t x0, uint32_t x1, uint32_t s0,
+                                                uint32_t s1, uint32_t s2, uint32_t s3,
+                                                uint32_t& o0, uint32_t& o1, uint32_t& o2,
+                                                uint32_t& o3) {
+  asm("{\n\t"
+      ".reg .b32 y, u;\n\t"
+      "prmt.b32 y, %4, %5, 0x4400;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 u, u, %10;\n\t"
+      "mul.rn.bf16x2 %0, u, %6;\n\t"
+      "prmt.b32 y, %4, %5, 0x5511;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 u, u, %10;\n\t"
+      "mul.rn.bf16x2 %1, u, %7;\n\t"
+      "prmt.b32 y, %4, %5, 0x6622;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 u, u, %10;\n\t"
+      "mul.rn.bf16x2 %2, u, %8;\n\t"
+      "prmt.b32 y, %4, %5, 0x7733;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 u, u, %10;\n\t"
+      "mul.rn.bf16x2 %3, u, %9;\n\t"
+      "}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(x0), "r"(x1), "r"(s0), "r"(s1), "r"(s2), "r"(s3), "r"(kBf16x2Pow120));
+}
+
+// Four E4M3 scale bytes (columns 4t..4t+3) -> four bf16x2 (s, s) pairs, exact.
+__device__ __forceinline__ void e4m3x4_to_bf16x2_dup(uint32_t b, uint32_t& s0, uint32_t& s1,
+                                                     uint32_t& s2, uint32_t& s3) {
+  asm("{\n\t"
+      ".reg .b32 y, u;\n\t"
+      "prmt.b32 y, %4, %4, 0x0000;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 %0, u, %5;\n\t"
+      "prmt.b32 y, %4, %4, 0x1111;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 %1, u, %5;\n\t"
+      "prmt.b32 y, %4, %4, 0x2222;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 %2, u, %5;\n\t"
+      "prmt.b32 y, %4, %4, 0x3333;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 %3, u, %5;\n\t"
+      "}"
+      : "=r"(s0), "=r"(s1), "=r"(s2), "=r"(s3)
+      : "r"(b), "r"(kBf16x2Pow120));
+}
+
+// NVFP4 k-row pair: x0, x1 = the 16-bit loads of rows k and k+1 (packed bytes
+// 2t, 2t+1), joined into X.  Region r's nibble sits at bits 4/0/12/8 of each
+// half; its magnitude bits (EE.M) move to bf16 bits 6..8 and its sign bit to
+// bit 15; then x 2^126 and x s (both exact).
+__device__ __forceinline__ void deq_fp4_rowpair(uint32_t x0, uint32_t x1, uint32_t s0,
+                                                uint32_t s1, uint32_t s2, uint32_t s3,
+                                                uint32_t& o0, uint32_t& o1, uint32_t& o2,
+                                                uint32_t& o3) {
+  asm("{\n\t"
+      ".reg .b32 x, a, b;\n\t"
+      "prmt.b32 x, %4, %5, 0x5410;\n\t"
+      "shl.b32 a, x, 2;\n\t"
+      "shl.b32 b, x, 8;\n\t"
+      "and.b32 a, a, 0x01C001C0;\n\t"
+      "lop3.b32 a, a, b, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 a, a, %10;\n\t"
+      "mul.rn.bf16x2 %0, a, %6;\n\t"
+      "shl.b32 a, x, 6;\n\t"
+      "shl.b32 b, x, 12;\n\t"
+      "and.b32 a, a, 0x01C001C0;\n\t"
+      "lop3.b32 a, a, b, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 a, a, %10;\n\t"
+      "mul.rn.bf16x2 %1, a, %7;\n\t"
+      "shr.b32 a, x, 6;\n\t"
+      "and.b32 a, a, 0x01C001C0;\n\t"
+      "lop3.b32 a, a, x, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 a, a, %10;\n\t"
+      "mul.rn.bf16x2 %2, a, %8;\n\t"
+      "shr.b32 a, x, 2;\n\t"
+      "shl.b32 b, x, 4;\n\t"
+      "and.b32 a, a, 0x01C001C0;\n\t"
+      "lop3.b32 a, a, b, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 a, a, %10;\n\t"
+      "mul.rn.bf16x2 %3, a, %9;\n\t"
+      "}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(x0), "r"(x1), "r"(s0), "r"(s1), "r"(s2), "r"(s3), "r"(kBf16x2Pow126));
+}
+
 // Epilogue of output columns n..n+3 for 8 rows m0..m0+7: operand loads
 // first (independent, overlapping), then the math and 8-byte stores.
 template <int ACT>
@@ -155,11 +286,12 @@ __device__ __forceinline__ void epi_quad8(const float (&v)[kW4Regions][8], int64
   }
 }
 
-template <int MPAD>
+template <int FMT, int MPAD>
 __global__ void __launch_bounds__(kW4Threads, 2)
-    w4a16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmQ,
-                 const __grid_constant__ CUtensorMap tmS, const W4Args a, int group) {
-  using Cfg = W4Cfg<MPAD>;
+    wq_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmQ,
+                   const __grid_constant__ CUtensorMap tmS, const W4Args a, int group) {
+  using Cfg = W4Cfg<FMT, MPAD>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment by pointer arithmetic on the shared array (keeps the
   // shared address space for the compiler).
@@ -223,14 +355,19 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) break;
         uint8_t* sq = stages + s * Cfg::kStageBytes;
-        uint8_t* sx = sq + kW4QBytes;
+        uint8_t* sx = sq + Cfg::kQBytes;
         uint8_t* ss = sx + Cfg::kXBytes;
-        const int srow = (kb * kBK) / group;
-        mbar_arrive_expect_tx(&full[s], kW4QBytes + Cfg::kXBytes + kW4BN * 2);
-        tma_load_2d_hint(sq, &tmQ, &full[s], nb * kW4RowBytes, kb * kBK, stream_policy);
+        // scale rows: one group row (int4, fp8) or four 16-deep blocks (nvfp4)
+        const int srow = FMT == kWqNvfp4 ? kb * (kBK / 16) : (kb * kBK) / group;
+        mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+        // the weight tile in boxes of 256 bytes x 64 k-rows
+#pragma unroll
+        for (int h = 0; h < Cfg::kRowBytes / 256; ++h)
+          tma_load_2d_hint(sq + h * (kBK * 256), &tmQ, &full[s], nb * Cfg::kRowBytes + 256 * h,
+                           kb * kBK, stream_policy);
         tma_load_2d(sx, &tmA, &full[s], kb * kBK, mb * MPAD);
         tma_load_2d(ss, &tmS, &full[s], nb * kW4BN, srow);
-        tma_load_2d(ss + 512, &tmS, &full[s], nb * kW4BN + 256, srow);
+        tma_load_2d(ss + Cfg::kScaleBytes / 2, &tmS, &full[s], nb * kW4BN + 256, srow);
         fills[s]++;
         if (++s == Cfg::kStages) {
           s = 0;
@@ -254,7 +391,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
           ok = false;
           break;
         }
-        const uint32_t x0 = smem_u32(stages + s * Cfg::kStageBytes + kW4QBytes);
+        const uint32_t x0 = smem_u32(stages + s * Cfg::kStageBytes + Cfg::kQBytes);
         for (int g = 0; g < 2; ++g) {
           if (!wait_bar(&afull[g], gph, ctl, kSiteMmaOperand)) {
             ok = false;
@@ -294,7 +431,6 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     const int t = q * 32 + lane;            // TMEM lane = owner of packed bytes 2t, 2t+1
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t abuf = tmem_base + lane_off + Cfg::kColA + 64 * g;
-    const uint32_t c136 = 0x43084308u;  // bf16x2 (136, 136)
     int s = 0;
     uint32_t ph = 0;
     for (int kb = kb0; kb < kb1; ++kb) {
@@ -303,27 +439,67 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       if (!wait_bar(&aempty[g], gph ^ 1, ctl, kSiteXformEmpty)) break;
       tc_fence_after();
       const uint8_t* sq = stages + s * Cfg::kStageBytes;
-      const uint2 sc = *reinterpret_cast<const uint2*>(sq + kW4QBytes + Cfg::kXBytes + 8 * t);
-      const uint32_t s0 = __byte_perm(sc.x, 0, 0x1010);  // bf16x2 (s, s), column 4t
-      const uint32_t s1 = __byte_perm(sc.x, 0, 0x3232);  // column 4t+1
-      const uint32_t s2 = __byte_perm(sc.y, 0, 0x1010);  // column 4t+2
-      const uint32_t s3 = __byte_perm(sc.y, 0, 0x3232);  // column 4t+3
-      const uint8_t* rows = sq + (32 * g) * kW4RowBytes + 2 * t;
+      const uint8_t* ssc = sq + Cfg::kQBytes + Cfg::kXBytes;
+      if constexpr (FMT == kWqFp8) {
+        // bytes 4t..4t+3 of each k-row: box half t/64, word t%64
+        const uint2 sc = *reinterpret_cast<const uint2*>(ssc + 8 * t);
+        const uint32_t s0 = __byte_perm(sc.x, 0, 0x1010);
+        const uint32_t s1 = __byte_perm(sc.x, 0, 0x3232);
+        const uint32_t s2 = __byte_perm(sc.y, 0, 0x1010);
+        const uint32_t s3 = __byte_perm(sc.y, 0, 0x3232);
+        const uint8_t* rows = sq + (t >> 6) * (kBK * 256) + (32 * g) * 256 + 4 * (t & 63);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t o0[8], o1[8], o2[8], o3[8];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o0[8], o1[8], o2[8], o3[8];
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const int row = 16 * h + 2 * p;
-          const uint32_t x0 = *reinterpret_cast<const uint16_t*>(rows + row * kW4RowBytes);
-          const uint32_t x1 = *reinterpret_cast<const uint16_t*>(rows + (row + 1) * kW4RowBytes);
-          // regions: 0 = high nibble of byte 2t, 1 = low of 2t, 2 = high of 2t+1, 3 = low of 2t+1
-          deq_rowpair(x0, x1, c136, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
+          for (int p = 0; p < 8; ++p) {
+            const int row = 16 * h + 2 * p;
+            const uint32_t x0 = *reinterpret_cast<const uint32_t*>(rows + row * 256);
+            const uint32_t x1 = *reinterpret_cast<const uint32_t*>(rows + (row + 1) * 256);
+            deq_fp8_rowpair(x0, x1, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
+          }
+          tmem_st8(abuf + 0 + 8 * h, o0);
+          tmem_st8(abuf + 16 + 8 * h, o1);
+          tmem_st8(abuf + 32 + 8 * h, o2);
+          tmem_st8(abuf + 48 + 8 * h, o3);
         }
-        tmem_st8(abuf + 0 + 8 * h, o0);
-        tmem_st8(abuf + 16 + 8 * h, o1);
-        tmem_st8(abuf + 32 + 8 * h, o2);
-        tmem_st8(abuf + 48 + 8 * h, o3);
+      } else {
+        const uint8_t* rows = sq + (32 * g) * Cfg::kRowBytes + 2 * t;
+        uint32_t s0, s1, s2, s3;
+        if constexpr (FMT == kWqInt4) {
+          const uint2 sc = *reinterpret_cast<const uint2*>(ssc + 8 * t);
+          s0 = __byte_perm(sc.x, 0, 0x1010);  // bf16x2 (s, s), column 4t
+          s1 = __byte_perm(sc.x, 0, 0x3232);  // column 4t+1
+          s2 = __byte_perm(sc.y, 0, 0x1010);  // column 4t+2
+          s3 = __byte_perm(sc.y, 0, 0x3232);  // column 4t+3
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if constexpr (FMT == kWqNvfp4) {
+            // the E4M3 block scale of k-rows [32g + 16h, +16): block row 2g + h
+            const uint32_t b = *reinterpret_cast<const uint32_t*>(
+                ssc + (t >> 6) * 1024 + (2 * g + h) * 256 + 4 * (t & 63));
+            e4m3x4_to_bf16x2_dup(b, s0, s1, s2, s3);
+          }
+          uint32_t o0[8], o1[8], o2[8], o3[8];
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const int row = 16 * h + 2 * p;
+            const uint32_t x0 = *reinterpret_cast<const uint16_t*>(rows + row * Cfg::kRowBytes);
+            const uint32_t x1 =
+                *reinterpret_cast<const uint16_t*>(rows + (row + 1) * Cfg::kRowBytes);
+            // regions: 0 = high nibble of byte 2t, 1 = low of 2t, 2 = high of 2t+1,
+            // 3 = low of 2t+1
+            if constexpr (FMT == kWqInt4)
+              deq_rowpair(x0, x1, 0x43084308u, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
+            else
+              deq_fp4_rowpair(x0, x1, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
+          }
+          tmem_st8(abuf + 0 + 8 * h, o0);
+          tmem_st8(abuf + 16 + 8 * h, o1);
+          tmem_st8(abuf + 32 + 8 * h, o2);
+          tmem_st8(abuf + 48 + 8 * h, o3);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -444,25 +620,25 @@ __global__ void __launch_bounds__(kW4Threads, 2)
 
 namespace {
 
-template <int MPAD>
+template <int FMT, int MPAD>
 cudaError_t run_w4(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmQ,
                    const CUtensorMap& tmS, const W4Args& args, int group, cudaStream_t stream) {
+  using Cfg = W4Cfg<FMT, MPAD>;
   static std::atomic<uint64_t> mask{0};
-  auto kernel = w4a16_kernel<MPAD>;
+  auto kernel = wq_gemm_kernel<FMT, MPAD>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = uint64_t(1) << (dev & 63);
   if (!(mask.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             W4Cfg<MPAD>::kSmem);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     mask.fetch_or(bit, std::memory_order_acq_rel);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.n_tiles, p.m_tiles);
   cfg.blockDim = dim3(kW4Threads, 1, 1);
-  cfg.dynamicSmemBytes = W4Cfg<MPAD>::kSmem;
+  cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -476,13 +652,26 @@ cudaError_t run_w4(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap&
 
 }  // namespace
 
-cudaError_t launch_w4a16(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmQ,
-                         const CUtensorMap& tmS, const EpiParams& ep, int M, int N, int K,
-                         int group, const KernelCtl& ctl, cudaStream_t stream) {
-  W4Args args{M, N, K, plan.num_kb, plan.splits, ep, ctl};
+template <int FMT>
+cudaError_t run_w4_fmt(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmQ,
+                       const CUtensorMap& tmS, const W4Args& args, int group,
+                       cudaStream_t stream) {
   switch (plan.mpad) {
-    case 16: return run_w4<16>(plan, tmA, tmQ, tmS, args, group, stream);
-    case 32: return run_w4<32>(plan, tmA, tmQ, tmS, args, group, stream);
+    case 16: return run_w4<FMT, 16>(plan, tmA, tmQ, tmS, args, group, stream);
+    case 32: return run_w4<FMT, 32>(plan, tmA, tmQ, tmS, args, group, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_wq_gemm(int fmt, const GemmPlan& plan, const CUtensorMap& tmA,
+                           const CUtensorMap& tmQ, const CUtensorMap& tmS, const EpiParams& ep,
+                           int M, int N, int K, int group, const KernelCtl& ctl,
+                           cudaStream_t stream) {
+  W4Args args{M, N, K, plan.num_kb, plan.splits, ep, ctl};
+  switch (fmt) {
+    case kWqInt4: return run_w4_fmt<kWqInt4>(plan, tmA, tmQ, tmS, args, group, stream);
+    case kWqFp8: return run_w4_fmt<kWqFp8>(plan, tmA, tmQ, tmS, args, group, stream);
+    case kWqNvfp4: return run_w4_fmt<kWqNvfp4>(plan, tmA, tmQ, tmS, args, group, stream);
     default: return cudaErrorInvalidValue;
   }
 }

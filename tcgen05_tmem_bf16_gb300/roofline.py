@@ -57,6 +57,19 @@ def w4a16_counts(M, N, K, group, has_c=False, has_bias=False, has_res=False) -> 
     return Counts(2.0 * M * N * K, io, io + 2 * K * N * BF16)
 
 
+def wq_counts(fmt, M, N, K, group, has_c=False, has_bias=False, has_res=False) -> Counts:
+    """Weight-only GEMM with FP8 (1 byte per weight, bf16 group scales) or
+    NVFP4 (half a byte per weight, one E4M3 byte per 16 along K) weights."""
+    if fmt == "w8a16_fp8":
+        wbytes = K * N + (K // group) * N * BF16
+    else:
+        wbytes = K * N // 2 + (K // 16) * N
+    io = M * K * BF16 + wbytes + M * N * BF16
+    io += (M * N * BF16 if has_c else 0) + (N * BF16 if has_bias else 0)
+    io += M * N * BF16 if has_res else 0
+    return Counts(2.0 * M * N * K, io, io + 2 * K * N * BF16)
+
+
 def int4_weight_bytes(K, N) -> int:
     return K * N // 2
 
@@ -124,4 +137,7 @@ def counts_for(cfg: dict) -> Counts:
         return swiglu_pointwise_counts(M, N)
     if op == "mlp":
         return mlp_counts(M, cfg["D"], cfg["F"])
+    if op in ("w8a16_fp8", "w4a16_nvfp4"):
+        return wq_counts(op, M, N, K, cfg.get("group", 16), cfg.get("has_c", False),
+                         cfg.get("has_bias", False), cfg.get("has_res", False))
     raise KeyError(op)

@@ -56,6 +56,13 @@ CONFIGS = {
     # the input width K = D, the hidden width F.
     "mlp_decode": dict(id=8, op="mlp", M=16, N=4096, K=4096, D=4096, F=14336, alpha=1.0,
                        beta=0.0, act="silu"),
+    # the W4A16 decode shape with FP8 (E4M3, bf16 group scales) and NVFP4
+    # (E2M1, E4M3 scales per 16 along K, per-tensor factor as alpha) weights
+    "w8a16_fp8": dict(id=9, op="w8a16_fp8", M=16, N=28672, K=8192, group=128, alpha=1.0,
+                      beta=0.0, act="identity", has_c=False, has_bias=False, has_res=False),
+    "w4a16_nvfp4": dict(id=10, op="w4a16_nvfp4", M=16, N=28672, K=8192, group=16,
+                        alpha=1.0 / 256, beta=0.0, act="identity", has_c=False,
+                        has_bias=False, has_res=False),
 }
 
 
@@ -82,6 +89,13 @@ def bf16_uniform(rng: np.random.Generator, shape, lo: float, hi: float) -> np.nd
 def int4_packed(rng: np.random.Generator, K: int, N: int) -> np.ndarray:
     """K x N/2 bytes, every nibble a uniform code in 0..15."""
     return rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+
+
+def e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """float32 values -> OCP E4M3 codes (uint8) via torch's float8 cast,
+    clamped to the finite range +-448 first (no NaN codes)."""
+    t = torch.from_numpy(np.clip(np.ascontiguousarray(x, dtype=np.float32), -448.0, 448.0))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
 
 
 def make(name: str, M: int | None = None, sigma_is_std: bool = False,
@@ -131,6 +145,18 @@ def make(name: str, M: int | None = None, sigma_is_std: bool = False,
         out["g"] = bf16_normal(rng_for(cid, 0), (Mv, Nv), 64.0, s)
         out["u"] = bf16_normal(rng_for(cid, 1), (Mv, Nv), 64.0, s)
         out["C"] = None
+    elif name == "w8a16_fp8":
+        out["A"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), 1.0, s)
+        # codes spread over the E4M3 range (N(0, 64^2), subnormals included)
+        out["Wq"] = e4m3_codes(rng_for(cid, 1).standard_normal((Kv, Nv), dtype=np.float32) * 64)
+        out["scales"] = bf16_uniform(rng_for(cid, 2), (Kv // cfg["group"], Nv), 1e-4, 4e-4)
+        out["C"] = out["bias"] = out["residual"] = None
+    elif name == "w4a16_nvfp4":
+        out["A"] = bf16_normal(rng_for(cid, 0), (Mv, Kv), 1.0, s)
+        out["Wq"] = int4_packed(rng_for(cid, 1), Kv, Nv)  # all 16 E2M1 codes equally likely
+        # block scales: E4M3 codes 0x30..0x3F (0.5 .. 1.875)
+        out["scales"] = rng_for(cid, 2).integers(0x30, 0x40, size=(Kv // 16, Nv), dtype=np.uint8)
+        out["C"] = out["bias"] = out["residual"] = None
     elif name == "mlp_decode":
         D, F = cfg["D"], cfg["F"]
         out["x"] = bf16_normal(rng_for(cid, 0), (Mv, D), 1.0, s)
