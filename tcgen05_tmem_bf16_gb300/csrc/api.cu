@@ -250,7 +250,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const De
   GemmPlan p;
   if (M == 0 || N == 0 || K == 0) return p;
   p.num_kb = ceil_div(K, kBK);
-  if (!dual && M <= 128) {
+  if (M <= (dual ? kSwapDualMaxM : 128)) {
     p.path = kPathSwap;
     p.mpad = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
     p.m_tiles = 1;

@@ -279,20 +279,28 @@ __device__ __forceinline__ void acc_sum16(uint32_t taddr, float (&out)[16]) {
   }
 }
 
-template <int MPAD>
+template <int MPAD, bool DUAL = false>
 struct SwapCfg {
-  static constexpr int kWBytes = kSwapBN * kBK * 2;          // 16 KB weight tile
+  // weight tile: 128 rows x 64 k (16 KB); the gate/up GEMM stages the gate
+  // and the up tile of the same 128 output columns (32 KB)
+  static constexpr int kWTile = kSwapBN * kBK * 2;
+  static constexpr int kWBytes = (DUAL ? 2 : 1) * kWTile;
   static constexpr int kXBytes = MPAD * kBK * 2;             // activation tile
   static constexpr int kStageBytes = kWBytes + kXBytes;
-  static constexpr int kStages = MPAD <= 32 ? 5 : (MPAD <= 64 ? 4 : 3);
+  static constexpr int kStages = DUAL ? 3 : (MPAD <= 32 ? 5 : (MPAD <= 64 ? 4 : 3));
   // Consecutive 16-deep K steps go to kAcc accumulators in turn: with a
   // narrow MMA (N = MPAD) the time per MMA is set by the accumulator's
   // read-after-write chain, not by its arithmetic, so independent chains
-  // multiply the MMA rate; the epilogue sums them in a fixed order.
+  // multiply the MMA rate; the epilogue sums them in a fixed order.  The
+  // gate/up GEMM keeps kAcc gate and kAcc up accumulators.
   static constexpr int kAcc = MPAD <= 32 ? 4 : 2;
-  static constexpr uint32_t kTmemCols = kAcc * MPAD <= 64 ? 64 : (kAcc * MPAD <= 128 ? 128 : 256);
+  static constexpr int kProducts = DUAL ? 2 : 1;
+  static constexpr int kCols = kProducts * kAcc * MPAD;
+  static constexpr uint32_t kTmemCols = kCols <= 64 ? 64 : (kCols <= 128 ? 128 : 256);
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
-  static_assert(kStages * kStageBytes >= 128 * MPAD * 4, "reduction buffer must fit");
+  static_assert(kCols <= 256, "TMEM budget of two CTAs per SM");
+  static_assert(!DUAL || kSmem <= 113 * 1024, "two CTAs per SM");
+  static_assert(kStages * kStageBytes >= kProducts * 128 * MPAD * 4, "reduction buffer must fit");
 };
 
 struct SwapArgs {
@@ -303,11 +311,31 @@ struct SwapArgs {
   KernelCtl ctl;
 };
 
-template <int MPAD, bool W_KN>
+// GLU ending of one output column for 16 consecutive rows (swapped gate/up
+// GEMM): h = act(alpha*g) * (alpha*u) + beta*C.
+template <int ACT>
+__device__ __forceinline__ void epi_col16_glu(const float (&g)[16], const float (&u)[16],
+                                              const ColLoads& L, int64_t m0, int n, int M,
+                                              int N, const EpiParams& e, uint64_t pol) {
+  if (n >= N) return;
+  const float beta = e.C ? e.beta : 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int64_t m = m0 + j;
+    if (m < M)
+      st_stream_u16(e.out + m * N + n,
+                    f_to_bf16bits(fmaf(beta, L.c[j],
+                                       act_apply<ACT>(e.alpha * g[j]) * (e.alpha * u[j]))),
+                    pol);
+  }
+}
+
+template <int MPAD, bool W_KN, bool DUAL>
 __global__ void __launch_bounds__(256, 2)
     gemm_swap_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmW, const SwapArgs a) {
-  using Cfg = SwapCfg<MPAD>;
+                     const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tmW2, const SwapArgs a) {
+  using Cfg = SwapCfg<MPAD, DUAL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
@@ -338,6 +366,7 @@ __global__ void __launch_bounds__(256, 2)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
+    if constexpr (DUAL) tma_prefetch_desc(&tmW2);
   }
   if (warp == 2) {
     tmem_alloc(tmem_holder, Cfg::kTmemCols);
@@ -362,11 +391,16 @@ __global__ void __launch_bounds__(256, 2)
         uint8_t* sw = stages + s * Cfg::kStageBytes;
         uint8_t* sx = sw + Cfg::kWBytes;
         mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-        if constexpr (W_KN) {
-          tma_load_2d(sw, &tmW, &full[s], nb * kSwapBN, kb * kBK);
-          tma_load_2d(sw + 8192, &tmW, &full[s], nb * kSwapBN + 64, kb * kBK);
-        } else {
-          tma_load_2d(sw, &tmW, &full[s], kb * kBK, nb * kSwapBN);
+#pragma unroll
+        for (int w = 0; w < Cfg::kProducts; ++w) {
+          const CUtensorMap* map = w == 0 ? &tmW : &tmW2;
+          uint8_t* dst = sw + w * Cfg::kWTile;
+          if constexpr (W_KN) {
+            tma_load_2d(dst, map, &full[s], nb * kSwapBN, kb * kBK);
+            tma_load_2d(dst + 8192, map, &full[s], nb * kSwapBN + 64, kb * kBK);
+          } else {
+            tma_load_2d(dst, map, &full[s], kb * kBK, nb * kSwapBN);
+          }
         }
         tma_load_2d(sx, &tmA, &full[s], kb * kBK, mb * MPAD);
         fills[s]++;
@@ -400,6 +434,13 @@ __global__ void __launch_bounds__(256, 2)
           const uint64_t bd = sdesc_sw128(x0 + k * 32, 16, 1024);
           const int j = (kb - kb0) * (kBK / kUK) + k;  // K step within this CTA's range
           mma_ss(tmem_base + (j % Cfg::kAcc) * MPAD, ad, bd, idesc, j >= Cfg::kAcc ? 1u : 0u);
+          if constexpr (DUAL) {
+            const uint32_t w1 = w0 + Cfg::kWTile;
+            const uint64_t ad2 = W_KN ? sdesc_sw128(w1 + k * 2048, 8192, 1024)
+                                      : sdesc_sw128(w1 + k * 32, 16, 1024);
+            mma_ss(tmem_base + (Cfg::kAcc + j % Cfg::kAcc) * MPAD, ad2, bd, idesc,
+                   j >= Cfg::kAcc ? 1u : 0u);
+          }
         }
         mma_commit(&empty[s]);
         if (++s == Cfg::kStages) {
@@ -438,9 +479,10 @@ __global__ void __launch_bounds__(256, 2)
     tc_fence_after();
     if (S > 1) {
 #pragma unroll 1
-      for (int c = 0; c < kChunks; ++c) {
+      for (int c = 0; c < Cfg::kProducts * kChunks; ++c) {  // gate chunks, then up chunks
         float r[16];
-        acc_sum16<Cfg::kAcc, MPAD>(tb + c * 16, r);
+        acc_sum16<Cfg::kAcc, MPAD>(tb + (c / kChunks) * Cfg::kAcc * MPAD + (c % kChunks) * 16,
+                                   r);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
           red[(c * 4 + v) * 128 + tid] = make_float4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
@@ -453,38 +495,53 @@ __global__ void __launch_bounds__(256, 2)
     for (int c = static_cast<int>(rank); c < kChunks; c += S) {
       if (c != static_cast<int>(rank))
         col16_prefetch(L, static_cast<int64_t>(mb) * MPAD + c * 16, n, a.M, a.N, a.ep, pol);
-      float v[16];
-      if (S == 1) {
-        float r[16];
-        acc_sum16<Cfg::kAcc, MPAD>(tb + c * 16, r);
+      float v[Cfg::kProducts][16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = have ? r[j] : 0.0f;
-      } else {
+      for (int pr = 0; pr < Cfg::kProducts; ++pr) {
+        if (S == 1) {
+          float r[16];
+          acc_sum16<Cfg::kAcc, MPAD>(tb + pr * Cfg::kAcc * MPAD + c * 16, r);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-        for (int p = 0; p < S; ++p) {
+          for (int j = 0; j < 16; ++j) v[pr][j] = have ? r[j] : 0.0f;
+        } else {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            float4 f;
-            if (p == static_cast<int>(rank)) {
-              f = red[(c * 4 + w) * 128 + tid];
-            } else {
-              f = ld_dsmem_f4(mapa_shared(smem_u32(&red[(c * 4 + w) * 128 + tid]),
-                                          static_cast<uint32_t>(p)));
+          for (int j = 0; j < 16; ++j) v[pr][j] = 0.0f;
+          const int cc = pr * kChunks + c;
+          for (int p = 0; p < S; ++p) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              float4 f;
+              if (p == static_cast<int>(rank)) {
+                f = red[(cc * 4 + w) * 128 + tid];
+              } else {
+                f = ld_dsmem_f4(mapa_shared(smem_u32(&red[(cc * 4 + w) * 128 + tid]),
+                                            static_cast<uint32_t>(p)));
+              }
+              v[pr][4 * w] += f.x;
+              v[pr][4 * w + 1] += f.y;
+              v[pr][4 * w + 2] += f.z;
+              v[pr][4 * w + 3] += f.w;
             }
-            v[4 * w] += f.x;
-            v[4 * w + 1] += f.y;
-            v[4 * w + 2] += f.z;
-            v[4 * w + 3] += f.w;
           }
         }
       }
       const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;
-      switch (a.ep.act) {
-        case kActRelu: epi_col16<kActRelu>(v, L, m0, n, a.M, a.N, a.ep, pol); break;
-        case kActSilu: epi_col16<kActSilu>(v, L, m0, n, a.M, a.N, a.ep, pol); break;
-        case kActGeluTanh: epi_col16<kActGeluTanh>(v, L, m0, n, a.M, a.N, a.ep, pol); break;
-        default: epi_col16<kActIdentity>(v, L, m0, n, a.M, a.N, a.ep, pol); break;
+      if constexpr (DUAL) {
+        switch (a.ep.act) {
+          case kActRelu: epi_col16_glu<kActRelu>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
+          case kActSilu: epi_col16_glu<kActSilu>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
+          case kActGeluTanh:
+            epi_col16_glu<kActGeluTanh>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol);
+            break;
+          default: epi_col16_glu<kActIdentity>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
+        }
+      } else {
+        switch (a.ep.act) {
+          case kActRelu: epi_col16<kActRelu>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+          case kActSilu: epi_col16<kActSilu>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+          case kActGeluTanh: epi_col16<kActGeluTanh>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+          default: epi_col16<kActIdentity>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+        }
       }
     }
   }
@@ -528,17 +585,18 @@ cudaError_t run_persistent(const GemmPlan& p, const CUtensorMap& tmA, const CUte
   return cudaGetLastError();
 }
 
-template <int MPAD, bool W_KN>
+template <int MPAD, bool W_KN, bool DUAL>
 cudaError_t run_swap(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                     const SwapArgs& args, cudaStream_t stream) {
+                     const CUtensorMap& tmW2, const SwapArgs& args, cudaStream_t stream) {
   static std::atomic<uint64_t> mask{0};
-  auto kernel = gemm_swap_kernel<MPAD, W_KN>;
-  cudaError_t e = ensure_smem_attr(kernel, SwapCfg<MPAD>::kSmem, mask);
+  auto kernel = gemm_swap_kernel<MPAD, W_KN, DUAL>;
+  using Cfg = SwapCfg<MPAD, DUAL>;
+  cudaError_t e = ensure_smem_attr(kernel, Cfg::kSmem, mask);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.n_tiles, p.m_tiles);
   cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = SwapCfg<MPAD>::kSmem;
+  cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -547,17 +605,25 @@ cudaError_t run_swap(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMa
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, args);
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, tmW2, args);
 }
 
 template <bool W_KN>
-cudaError_t run_swap_mpad(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                          const SwapArgs& args, cudaStream_t stream) {
+cudaError_t run_swap_mpad(const GemmPlan& p, bool dual, const CUtensorMap& tmA,
+                          const CUtensorMap& tmW, const CUtensorMap& tmW2, const SwapArgs& args,
+                          cudaStream_t stream) {
+  if (dual) {
+    switch (p.mpad) {
+      case 16: return run_swap<16, W_KN, true>(p, tmA, tmW, tmW2, args, stream);
+      case 32: return run_swap<32, W_KN, true>(p, tmA, tmW, tmW2, args, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (p.mpad) {
-    case 16: return run_swap<16, W_KN>(p, tmA, tmW, args, stream);
-    case 32: return run_swap<32, W_KN>(p, tmA, tmW, args, stream);
-    case 64: return run_swap<64, W_KN>(p, tmA, tmW, args, stream);
-    case 128: return run_swap<128, W_KN>(p, tmA, tmW, args, stream);
+    case 16: return run_swap<16, W_KN, false>(p, tmA, tmW, tmW, args, stream);
+    case 32: return run_swap<32, W_KN, false>(p, tmA, tmW, tmW, args, stream);
+    case 64: return run_swap<64, W_KN, false>(p, tmA, tmW, tmW, args, stream);
+    case 128: return run_swap<128, W_KN, false>(p, tmA, tmW, tmW, args, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -576,10 +642,10 @@ cudaError_t launch_gemm(const GemmPlan& plan, bool w_kn, bool dual, const CUtens
     return dual ? run_persistent<false, true>(plan, tmA, tmW, tmW2, args, stream)
                 : run_persistent<false, false>(plan, tmA, tmW, tmW2, args, stream);
   }
-  if (plan.path == kPathSwap && !dual) {
+  if (plan.path == kPathSwap) {
     SwapArgs args{M, N, K, plan.num_kb, plan.splits, ep, ctl};
-    return w_kn ? run_swap_mpad<true>(plan, tmA, tmW, args, stream)
-                : run_swap_mpad<false>(plan, tmA, tmW, args, stream);
+    return w_kn ? run_swap_mpad<true>(plan, dual, tmA, tmW, tmW2, args, stream)
+                : run_swap_mpad<false>(plan, dual, tmA, tmW, tmW2, args, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -110,6 +110,7 @@ constexpr int kBM = 128;        // MMA M: rows of TMEM / output tile height
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kPersistBN = 256; // persistent kernel: MMA N
 constexpr int kSwapBN = 128;    // swapped kernel: output columns per tile (= MMA M)
+constexpr int kSwapDualMaxM = 32;  // gate/up GEMM on the swapped kernel up to this M
 constexpr int kW4BN = 512;      // W4A16 kernel: output columns per tile
 constexpr int kMaxSplits = 8;   // portable cluster size limit
 constexpr int kPairMinM = 512;  // M from which the CTA-pair kernel is used

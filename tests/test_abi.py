@@ -55,6 +55,10 @@ def test_workspace_sizes(lib):
     assert gbf.gbf_workspace_size("gemm_epilogue", 4096, 4096, 16, False) == 4096 * 4096 * 2
     assert gbf.gbf_workspace_size("swiglu", 2048, 14336, 4096, False) == 2 * 2048 * 14336 * 2
     assert gbf.gbf_workspace_size("w4a16", 16, 28672, 8192, False) == 8192 * 28672 * 2
+    assert gbf.gbf_workspace_size("w8a16_fp8", 16, 28672, 8192, False) == 8192 * 28672 * 2
+    assert gbf.gbf_workspace_size("mlp", 16, 4096, 14336, True) == 16 * 14336 * 2
+    assert gbf.gbf_workspace_size("mlp", 16, 4096, 14336, False) == 4 * 16 * 14336 * 2 + \
+        16 * 4096 * 2
 
 
 def test_kernel_path_planning(lib):
@@ -64,6 +68,13 @@ def test_kernel_path_planning(lib):
     assert path == "swap_splitk" and 1 <= splits <= 8
     assert gbf.gbf_kernel_path("swiglu", 2048, 14336, 4096)[0] == "pair"
     assert gbf.gbf_kernel_path("swiglu", 200, 14336, 4096)[0] == "persistent"
+    assert gbf.gbf_kernel_path("swiglu", 33, 14336, 4096)[0] == "persistent"
+    path, splits = gbf.gbf_kernel_path("swiglu", 16, 14336, 4096)
+    assert path == "swap_splitk" and 1 <= splits <= 8
+    for op in ("w8a16_fp8", "w4a16_nvfp4"):
+        assert gbf.gbf_kernel_path(op, 16, 28672, 8192)[0] == "w4a16"
+    assert gbf.gbf_kernel_path("w4a16_nvfp4", 16, 64, 48)[0] == "w4a16"
+    assert gbf.gbf_kernel_path("w8a16_fp8", 16, 64, 48)[0] == "rejected"
     path, splits = gbf.gbf_kernel_path("w4a16", 16, 28672, 8192)
     assert path == "w4a16" and 1 <= splits <= 8
     assert gbf.gbf_kernel_path("gemm_epilogue", 0, 8, 8)[0] == "none"

@@ -34,6 +34,38 @@ def test_swiglu_dual_gemm(cuda_lib, layout, M, N, K):
     assert_parity(down(h), ref, f"swiglu {layout} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+@pytest.mark.parametrize("M,N,K", [(1, 136, 64), (16, 1000, 4096), (17, 264, 200),
+                                   (32, 4096, 1024), (5, 128, 8)])
+def test_swiglu_decode_sizes_swapped_kernel(cuda_lib, layout, M, N, K):
+    # M <= 32: the gate/up GEMM on the swapped split-K kernel (two weight
+    # tiles per stage, gate and up accumulators, GLU ending per column)
+    x = rand_bf16(M + 11, (M, K))
+    shp = (N, K) if layout == "nk" else (K, N)
+    wg = rand_bf16(M + 12, shp, std=K ** -0.5)
+    wu = rand_bf16(M + 13, shp, std=K ** -0.5)
+    h = poison_bf16(M, N)
+    assert cuda_lib.gbf_kernel_path("swiglu", M, N, K, layout)[0] == "swap_splitk"
+    cuda_lib.swiglu_dual_gemm(up(x), up(wg), up(wu), layout, h, M, N, K)
+    assert cuda_lib.gbf_check_device_error() == 0
+    ref = oracle.swiglu(x, wg, wu, layout, M=M, N=N, K=K)
+    assert_parity(down(h), ref, f"swiglu swapped {layout} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh", "relu", "identity"])
+def test_swiglu_decode_gates_alpha_beta_c(cuda_lib, act):
+    M, N, K = 16, 392, 640
+    x = rand_bf16(31, (M, K))
+    wg = rand_bf16(32, (N, K), std=K ** -0.5)
+    wu = rand_bf16(33, (N, K), std=K ** -0.5)
+    C = rand_bf16(34, (M, N))
+    h = poison_bf16(M, N)
+    cuda_lib.swiglu_dual_gemm(up(x), up(wg), up(wu), "nk", h, M, N, K, 0.75, 1.5, up(C), act)
+    assert cuda_lib.gbf_check_device_error() == 0
+    ref = oracle.swiglu(x, wg, wu, "nk", C, M=M, N=N, K=K, alpha=0.75, beta=1.5, act=act)
+    assert_parity(down(h), ref, f"swiglu decode {act}")
+
+
 @pytest.mark.parametrize("act", ["silu", "gelu_tanh", "relu", "identity"])
 def test_swiglu_other_gates_alpha_beta_c(cuda_lib, act):
     M, N, K = 200, 136, 256
