@@ -34,9 +34,8 @@
 // One 64-deep K block = 16 MMAs (4 regions x 4 steps of 16).
 //
 // Eight transform warps form two groups; group g dequantises k-rows
-// [32g, 32g+32) of every shared-memory stage into its own TMEM buffer, in two
-// halves of 16 k-rows that are handed to the MMA one at a time, so the MMAs
-// of one half run while the next half is being dequantised.
+// [32g, 32g+32) of every shared-memory stage into its own TMEM buffer, so
+// one group fills while the MMAs drain the other.
 //
 // Dequantisation of an int4 code q, exact as the definition wants:
 //   bits 0x4300 | q  is the bf16 value 128 + q;
@@ -300,10 +299,9 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kStages * Cfg::kStageBytes);
   uint64_t* empty = full + Cfg::kStages;
-  // TMEM operand halves: [2g + h] = group g, k-rows [32g + 16h, +16) of a stage
-  uint64_t* afull = empty + Cfg::kStages;  // [4]: transform -> MMA
-  uint64_t* aempty = afull + 4;            // [4]: MMA -> transform
-  uint64_t* dfull = aempty + 4;
+  uint64_t* afull = empty + Cfg::kStages;  // [2]: transform group g -> MMA
+  uint64_t* aempty = afull + 2;            // [2]: MMA -> transform group g
+  uint64_t* dfull = aempty + 2;
   uint64_t* done = dfull + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
@@ -322,7 +320,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 8 + 1);  // 8 transform warps + the MMA commit
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&afull[i], 4);
       mbar_init(&aempty[i], 1);
     }
@@ -394,23 +392,25 @@ __global__ void __launch_bounds__(kW4Threads, 2)
           break;
         }
         const uint32_t x0 = smem_u32(stages + s * Cfg::kStageBytes + Cfg::kQBytes);
-        // the four 16-deep K steps of the stage, each as soon as its operand
-        // half is in TMEM; each half is released as soon as its MMAs finish
-        for (int hk = 0; hk < 4; ++hk) {
-          if (!wait_bar(&afull[hk], gph, ctl, kSiteMmaOperand)) {
+        for (int g = 0; g < 2; ++g) {
+          if (!wait_bar(&afull[g], gph, ctl, kSiteMmaOperand)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t abuf = tmem_base + Cfg::kColA + 64 * (hk >> 1) + 8 * (hk & 1);
-          const uint64_t bd = sdesc_sw128(x0 + hk * 32, 16, 1024);
-          const int j = (kb - kb0) * 4 + hk;  // K step within this CTA's range
-          const int e = j % Cfg::kSets;
-          const uint32_t accum = j >= Cfg::kSets ? 1u : 0u;
+          const uint32_t abuf = tmem_base + Cfg::kColA + 64 * g;
 #pragma unroll
-          for (int r = 0; r < kW4Regions; ++r)
-            mma_ts(tmem_base + (e * kW4Regions + r) * MPAD, abuf + 16 * r, bd, idesc, accum);
-          mma_commit(&aempty[hk]);
+          for (int k = 0; k < 2; ++k) {
+            const uint64_t bd = sdesc_sw128(x0 + (2 * g + k) * 32, 16, 1024);
+            const int j = (kb - kb0) * 4 + 2 * g + k;  // K step within this CTA's range
+            const int e = j % Cfg::kSets;
+            const uint32_t accum = j >= Cfg::kSets ? 1u : 0u;
+#pragma unroll
+            for (int r = 0; r < kW4Regions; ++r)
+              mma_ts(tmem_base + (e * kW4Regions + r) * MPAD, abuf + 16 * r + 8 * k, bd, idesc,
+                     accum);
+          }
+          mma_commit(&aempty[g]);
         }
         if (!ok) break;
         mma_commit(&empty[s]);
@@ -433,47 +433,58 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     const uint32_t abuf = tmem_base + lane_off + Cfg::kColA + 64 * g;
     int s = 0;
     uint32_t ph = 0;
-    bool ok = true;
-    for (int kb = kb0; kb < kb1 && ok; ++kb) {
+    for (int kb = kb0; kb < kb1; ++kb) {
       const uint32_t gph = (kb - kb0) & 1;
       if (!wait_bar(&full[s], ph, ctl, kSiteXformFull)) break;
+      if (!wait_bar(&aempty[g], gph ^ 1, ctl, kSiteXformEmpty)) break;
+      tc_fence_after();
       const uint8_t* sq = stages + s * Cfg::kStageBytes;
       const uint8_t* ssc = sq + Cfg::kQBytes + Cfg::kXBytes;
-      // this thread's weight bytes of k-row 32g of the stage
-      const uint8_t* rows = FMT == kWqFp8
-                                ? sq + (t >> 6) * (kBK * 256) + (32 * g) * 256 + 4 * (t & 63)
-                                : sq + (32 * g) * Cfg::kRowBytes + 2 * t;
-      uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
-      if constexpr (FMT != kWqNvfp4) {
+      if constexpr (FMT == kWqFp8) {
+        // bytes 4t..4t+3 of each k-row: box half t/64, word t%64
         const uint2 sc = *reinterpret_cast<const uint2*>(ssc + 8 * t);
-        s0 = __byte_perm(sc.x, 0, 0x1010);  // bf16x2 (s, s), column 4t
-        s1 = __byte_perm(sc.x, 0, 0x3232);  // column 4t+1
-        s2 = __byte_perm(sc.y, 0, 0x1010);  // column 4t+2
-        s3 = __byte_perm(sc.y, 0, 0x3232);  // column 4t+3
-      }
+        const uint32_t s0 = __byte_perm(sc.x, 0, 0x1010);
+        const uint32_t s1 = __byte_perm(sc.x, 0, 0x3232);
+        const uint32_t s2 = __byte_perm(sc.y, 0, 0x1010);
+        const uint32_t s3 = __byte_perm(sc.y, 0, 0x3232);
+        const uint8_t* rows = sq + (t >> 6) * (kBK * 256) + (32 * g) * 256 + 4 * (t & 63);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // half h: k-rows [32g + 16h, +16) into TMEM operand half 2g + h
-        if (!wait_bar(&aempty[2 * g + h], gph ^ 1, ctl, kSiteXformEmpty)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if constexpr (FMT == kWqNvfp4) {
-          // the E4M3 block scale of these 16 k-rows: block row 2g + h
-          const uint32_t b = *reinterpret_cast<const uint32_t*>(
-              ssc + (t >> 6) * 1024 + (2 * g + h) * 256 + 4 * (t & 63));
-          e4m3x4_to_bf16x2_dup(b, s0, s1, s2, s3);
-        }
-        uint32_t o0[8], o1[8], o2[8], o3[8];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o0[8], o1[8], o2[8], o3[8];
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const int row = 16 * h + 2 * p;
-          if constexpr (FMT == kWqFp8) {
+          for (int p = 0; p < 8; ++p) {
+            const int row = 16 * h + 2 * p;
             const uint32_t x0 = *reinterpret_cast<const uint32_t*>(rows + row * 256);
             const uint32_t x1 = *reinterpret_cast<const uint32_t*>(rows + (row + 1) * 256);
             deq_fp8_rowpair(x0, x1, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
-          } else {
+          }
+          tmem_st8(abuf + 0 + 8 * h, o0);
+          tmem_st8(abuf + 16 + 8 * h, o1);
+          tmem_st8(abuf + 32 + 8 * h, o2);
+          tmem_st8(abuf + 48 + 8 * h, o3);
+        }
+      } else {
+        const uint8_t* rows = sq + (32 * g) * Cfg::kRowBytes + 2 * t;
+        uint32_t s0, s1, s2, s3;
+        if constexpr (FMT == kWqInt4) {
+          const uint2 sc = *reinterpret_cast<const uint2*>(ssc + 8 * t);
+          s0 = __byte_perm(sc.x, 0, 0x1010);  // bf16x2 (s, s), column 4t
+          s1 = __byte_perm(sc.x, 0, 0x3232);  // column 4t+1
+          s2 = __byte_perm(sc.y, 0, 0x1010);  // column 4t+2
+          s3 = __byte_perm(sc.y, 0, 0x3232);  // column 4t+3
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if constexpr (FMT == kWqNvfp4) {
+            // the E4M3 block scale of k-rows [32g + 16h, +16): block row 2g + h
+            const uint32_t b = *reinterpret_cast<const uint32_t*>(
+                ssc + (t >> 6) * 1024 + (2 * g + h) * 256 + 4 * (t & 63));
+            e4m3x4_to_bf16x2_dup(b, s0, s1, s2, s3);
+          }
+          uint32_t o0[8], o1[8], o2[8], o3[8];
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const int row = 16 * h + 2 * p;
             const uint32_t x0 = *reinterpret_cast<const uint16_t*>(rows + row * Cfg::kRowBytes);
             const uint32_t x1 =
                 *reinterpret_cast<const uint16_t*>(rows + (row + 1) * Cfg::kRowBytes);
@@ -484,18 +495,19 @@ __global__ void __launch_bounds__(kW4Threads, 2)
             else
               deq_fp4_rowpair(x0, x1, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
           }
+          tmem_st8(abuf + 0 + 8 * h, o0);
+          tmem_st8(abuf + 16 + 8 * h, o1);
+          tmem_st8(abuf + 32 + 8 * h, o2);
+          tmem_st8(abuf + 48 + 8 * h, o3);
         }
-        tmem_st8(abuf + 0 + 8 * h, o0);
-        tmem_st8(abuf + 16 + 8 * h, o1);
-        tmem_st8(abuf + 32 + 8 * h, o2);
-        tmem_st8(abuf + 48 + 8 * h, o3);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[2 * g + h]);
       }
-      if (!ok) break;
-      if (lane == 0) mbar_arrive(&empty[s]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&afull[g]);
+        mbar_arrive(&empty[s]);
+      }
       if (++s == Cfg::kStages) {
         s = 0;
         ph ^= 1;
