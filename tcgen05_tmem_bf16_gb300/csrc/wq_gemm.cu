@@ -88,6 +88,11 @@ struct W4Cfg {
   // chains are in flight (a narrow MMA's time is set by its accumulator's
   // read-after-write chain); the epilogue adds the sets, set 0 first.
   static constexpr int kSets = MPAD <= 16 ? 2 : 1;
+  // MMA issuing threads.  tcgen05.mma instructions from one thread complete
+  // one after another (about 150 cycles each on this part, whatever their N),
+  // while those of different threads overlap; with two accumulator sets, set
+  // g is fed by its own issuer from transform group g's operand buffer.
+  static constexpr int kIssuers = kSets;
   static constexpr uint32_t kColA = kSets * kW4Regions * MPAD;  // D(set e, region r) at (4e+r)*MPAD
   // A buffer of group g at kColA + 64g; region r at +16r (16 columns = 32 k).
   static_assert(kColA + 128 <= kTmemCols, "TMEM budget");
@@ -318,14 +323,14 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 8 + 1);  // 8 transform warps + the MMA commit
+      mbar_init(&empty[i], 8 + Cfg::kIssuers);  // 8 transform warps + the MMA commits
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&afull[i], 4);
       mbar_init(&aempty[i], 1);
     }
-    mbar_init(dfull, 1);
-    mbar_init(done, 1);
+    mbar_init(dfull, Cfg::kIssuers);
+    mbar_init(done, Cfg::kIssuers);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -378,10 +383,15 @@ __global__ void __launch_bounds__(kW4Threads, 2)
         if (fills[i]) wait_bar(&full[i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (warp == 3 && Cfg::kIssuers == 2)) {
+    // ------------------------------------------------------------ MMA issuers
+    // one issuer: both groups' buffers, K steps alternating over the sets;
+    // two issuers: issuer i takes group i's buffer into accumulator set i
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kBM, MPAD, false, false);
+      const int issuer = warp == 1 ? 0 : 1;
+      const int g0 = Cfg::kIssuers == 2 ? issuer : 0;
+      const int g1 = Cfg::kIssuers == 2 ? issuer + 1 : 2;
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
           break;
         }
         const uint32_t x0 = smem_u32(stages + s * Cfg::kStageBytes + Cfg::kQBytes);
-        for (int g = 0; g < 2; ++g) {
+        for (int g = g0; g < g1; ++g) {
           if (!wait_bar(&afull[g], gph, ctl, kSiteMmaOperand)) {
             ok = false;
             break;
@@ -403,8 +413,9 @@ __global__ void __launch_bounds__(kW4Threads, 2)
           for (int k = 0; k < 2; ++k) {
             const uint64_t bd = sdesc_sw128(x0 + (2 * g + k) * 32, 16, 1024);
             const int j = (kb - kb0) * 4 + 2 * g + k;  // K step within this CTA's range
-            const int e = j % Cfg::kSets;
-            const uint32_t accum = j >= Cfg::kSets ? 1u : 0u;
+            const int e = Cfg::kIssuers == 2 ? issuer : j % Cfg::kSets;
+            const uint32_t accum =
+                Cfg::kIssuers == 2 ? ((kb > kb0 || k > 0) ? 1u : 0u) : (j >= Cfg::kSets ? 1u : 0u);
 #pragma unroll
             for (int r = 0; r < kW4Regions; ++r)
               mma_ts(tmem_base + (e * kW4Regions + r) * MPAD, abuf + 16 * r + 8 * k, bd, idesc,
@@ -433,11 +444,13 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     const uint32_t abuf = tmem_base + lane_off + Cfg::kColA + 64 * g;
     int s = 0;
     uint32_t ph = 0;
-    for (int kb = kb0; kb < kb1; ++kb) {
+    bool ok = true;
+    // The operand buffer is waited for only once the first half's weights
+    // are dequantised in registers, so that work overlaps the MMAs still
+    // reading the buffer.
+    for (int kb = kb0; kb < kb1 && ok; ++kb) {
       const uint32_t gph = (kb - kb0) & 1;
       if (!wait_bar(&full[s], ph, ctl, kSiteXformFull)) break;
-      if (!wait_bar(&aempty[g], gph ^ 1, ctl, kSiteXformEmpty)) break;
-      tc_fence_after();
       const uint8_t* sq = stages + s * Cfg::kStageBytes;
       const uint8_t* ssc = sq + Cfg::kQBytes + Cfg::kXBytes;
       if constexpr (FMT == kWqFp8) {
@@ -457,6 +470,13 @@ __global__ void __launch_bounds__(kW4Threads, 2)
             const uint32_t x0 = *reinterpret_cast<const uint32_t*>(rows + row * 256);
             const uint32_t x1 = *reinterpret_cast<const uint32_t*>(rows + (row + 1) * 256);
             deq_fp8_rowpair(x0, x1, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
+          }
+          if (h == 0) {
+            if (!wait_bar(&aempty[g], gph ^ 1, ctl, kSiteXformEmpty)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
           tmem_st8(abuf + 0 + 8 * h, o0);
           tmem_st8(abuf + 16 + 8 * h, o1);
@@ -495,12 +515,20 @@ __global__ void __launch_bounds__(kW4Threads, 2)
             else
               deq_fp4_rowpair(x0, x1, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
           }
+          if (h == 0) {
+            if (!wait_bar(&aempty[g], gph ^ 1, ctl, kSiteXformEmpty)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           tmem_st8(abuf + 0 + 8 * h, o0);
           tmem_st8(abuf + 16 + 8 * h, o1);
           tmem_st8(abuf + 32 + 8 * h, o2);
           tmem_st8(abuf + 48 + 8 * h, o3);
         }
       }
+      if (!ok) break;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
