@@ -19,6 +19,20 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
+// Pull the C and residual segments [col0, col1) of one row into L2 ahead of
+// their loads (one prefetch per 128-byte line), so that an epilogue that
+// starts as soon as an accumulator is ready does not wait on HBM latency.
+__device__ __forceinline__ void epi_row_l2_prefetch(int64_t row, int col0, int col1, int M,
+                                                    int N, const EpiParams& e) {
+  if (row >= M) return;
+  if (col1 > N) col1 = N;
+  for (int col = col0; col < col1; col += 64) {
+    const int64_t off = row * N + col;
+    if (e.C) asm volatile("prefetch.global.L2 [%0];" ::"l"(e.C + off));
+    if (e.residual) asm volatile("prefetch.global.L2 [%0];" ::"l"(e.residual + off));
+  }
+}
+
 // Operands of the ending for 32 consecutive columns of one row, loaded
 // before the accumulator is read from TMEM so that their latency overlaps.
 struct RowLoads {

@@ -21,6 +21,15 @@
 // Per SM this halves the shared-memory fill of the B operand compared with a
 // 128 x 256 tile on one SM (32 KB instead of 48 KB per 64-deep K step for the
 // same number of MMA cycles), which is what limits the single-CTA kernel.
+//
+// Two streams per pair.  The tcgen05.mma instructions of one issuing thread
+// complete one after another, about 150 cycles each on this part whatever
+// their N, which caps one stream of 256 x BN x 16 MMAs at 112-128 cycles of
+// tensor work per 150.  So the pair runs two independent pipelines: stream i
+// takes every other tile of the pair's sequence, with its own producer
+// threads, its own 3-stage ring, its own MMA issuer (both in the even CTA),
+// its own accumulator (TMEM columns 256i .. 256i+BN) and its own epilogue
+// warpgroup.  The two issuers' MMAs overlap in the tensor cores.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,6 +44,8 @@
 namespace gbf {
 
 constexpr int kQStages = 6;
+constexpr int kQStreams = 2;
+constexpr int kQRing = kQStages / kQStreams;  // stages per stream
 constexpr int kQABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int kQThreads = 384;                 // warps 0-3 roles, 4-11 epilogue
 constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
@@ -48,7 +59,6 @@ struct PairCfg {
   static constexpr int kStageBytes = kQABytes + kBBytes;
   static constexpr int kSmem = 1024 + kQStages * kStageBytes + 256;
   static constexpr int kChunks = BN / 32;             // 32-column epilogue chunks
-  static constexpr int kHalf0 = (kChunks + 1) / 2;    // chunks of the first warpgroup
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN <= 256, "tile width");
 };
@@ -95,11 +105,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kQStreams; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 16);  // 8 epilogue warps in each CTA of the pair
     }
-    mbar_init(done, 1);
+    mbar_init(done, kQStreams);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -121,27 +131,31 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int num_kb = a.num_kb;
   const int out_bn = DUAL ? 128 : BN;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers (both CTAs)
+    // warp 0 feeds stream 0, warp 3 stream 1; stream i's stages are
+    // [kQRing*i, kQRing*(i+1)) and its tiles every other one of the pair's.
     if (lane == 0) {
-      uint32_t fills[kQStages];
+      const int st = warp == 0 ? 0 : 1;
+      uint32_t fills[kQRing];
 #pragma unroll
-      for (int i = 0; i < kQStages; ++i) fills[i] = 0;
+      for (int i = 0; i < kQRing; ++i) fills[i] = 0;
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += npairs) {
+      for (int t = pair + st * npairs; t < num_tiles && ok; t += kQStreams * npairs) {
         int mb, nb;
         tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) {
+          const int g = st * kQRing + s;
+          if (!wait_bar(&empty[g], ph ^ 1, ctl, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
-          uint8_t* sa = stages + s * Cfg::kStageBytes;
+          uint8_t* sa = stages + g * Cfg::kStageBytes;
           uint8_t* sb = sa + kQABytes;
-          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
-          if (leader) mbar_arrive_expect_tx(&full[s], 2 * Cfg::kStageBytes);
+          const uint32_t bar = mapa_shared(smem_u32(&full[g]), 0);
+          if (leader) mbar_arrive_expect_tx(&full[g], 2 * Cfg::kStageBytes);
           tma_load_2d_pair(sa, &tmA, bar, kb * kBK, mb * kQTileM + static_cast<int>(rank) * kBM);
           const CUtensorMap* wmap = (DUAL && rank) ? &tmW2 : &tmW;
           const int n0 = DUAL ? nb * 128 : nb * BN + static_cast<int>(rank) * (BN / 2);
@@ -152,7 +166,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             tma_load_2d_pair(sb, wmap, bar, kb * kBK, n0);
           }
           fills[s]++;
-          if (++s == kQStages) {
+          if (++s == kQRing) {
             s = 0;
             ph ^= 1;
           }
@@ -160,34 +174,37 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
       if (ok) {
         // Every copy is consumed before the MMA reports the stage empty.
-        for (int i = 0; i < kQStages; ++i)
-          if (fills[i]) wait_bar(&empty[i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
+        for (int i = 0; i < kQRing; ++i)
+          if (fills[i])
+            wait_bar(&empty[st * kQRing + i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
       } else {
         settle_after_abort();
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers (even CTA)
+    // warp 1 lane 0 issues stream 0, warp 2 lane 0 stream 1 (warp 2 also
+    // allocates and frees the tensor memory, outside this loop)
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_bf16(kQTileM, BN, false, W_KN);
+      const int st = warp - 1;
+      const uint32_t d = tmem_base + st * 256;
       int s = 0;
       uint32_t ph = 0;
       int local = 0;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += npairs, ++local) {
-        const int buf = local & 1;
-        const uint32_t aph = (local >> 1) & 1;
-        if (!wait_bar(&tempty[buf], aph ^ 1, ctl, kSiteMmaAccEmpty)) break;
+      for (int t = pair + st * npairs; t < num_tiles && ok; t += kQStreams * npairs, ++local) {
+        if (!wait_bar(&tempty[st], (local & 1) ^ 1, ctl, kSiteMmaAccEmpty)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * 256;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
+          const int g = st * kQRing + s;
+          if (!wait_bar(&full[g], ph, ctl, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(stages + s * Cfg::kStageBytes);
+          const uint32_t a0 = smem_u32(stages + g * Cfg::kStageBytes);
           const uint32_t b0 = a0 + kQABytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
@@ -196,14 +213,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
                                      : sdesc_sw128(b0 + k * 32, 16, 1024);
             mma_ss_pair(d, ad, bd, idesc, (kb | k) != 0);
           }
-          mma_commit_pair(&empty[s], 0x3);
-          if (++s == kQStages) {
+          mma_commit_pair(&empty[g], 0x3);
+          if (++s == kQRing) {
             s = 0;
             ph ^= 1;
           }
         }
         if (!ok) break;
-        if (!(a.ctl.inject && local == 0)) mma_commit_pair(&tfull[buf], 0x3);
+        if (!(a.ctl.inject && st == 0 && local == 0)) mma_commit_pair(&tfull[st], 0x3);
       }
       mma_commit_pair(done, 0x1);
       wait_bar(done, 0, ctl, kSiteDrain, false);
@@ -211,28 +228,31 @@ __global__ void __launch_bounds__(kQThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    // the pair's tiles in order: local tile l belongs to stream l % 2
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;
     const uint64_t pol = l2_evict_first_policy();
     constexpr int kChunks = DUAL ? 4 : Cfg::kChunks;
-    constexpr int kFirst = DUAL ? 2 : Cfg::kHalf0;  // chunks of warpgroup 0; the rest go to 1
+    constexpr int kFirst = (kChunks + 1) / 2;  // chunks of warpgroup 0; the rest go to 1
     const int c_begin = half == 0 ? 0 : kFirst;
     const int c_end = half == 0 ? kFirst : kChunks;
-    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
-                                       mapa_shared(smem_u32(&tempty[1]), 0)};
+    const uint32_t tempty_leader[kQStreams] = {mapa_shared(smem_u32(&tempty[0]), 0),
+                                               mapa_shared(smem_u32(&tempty[1]), 0)};
     int local = 0;
     for (int t = pair; t < num_tiles; t += npairs, ++local) {
       int mb, nb;
       tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
-      const int buf = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
+      const int st = local % kQStreams;
+      const uint32_t aph = (local / kQStreams) & 1;
       const int64_t row =
           static_cast<int64_t>(mb) * kQTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
+      epi_row_l2_prefetch(row, nb * out_bn + c_begin * 32, nb * out_bn + c_end * 32, a.M, a.N,
+                          a.ep);
       RowLoads L;
       epi_row_prefetch(L, row, nb * out_bn + c_begin * 32, a.M, a.N, a.ep, pol);
-      if (!wait_bar(&tfull[buf], aph, ctl, kSiteEpiAccFull)) break;
+      if (!wait_bar(&tfull[st], aph, ctl, kSiteEpiAccFull)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + buf * 256 + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t tb = tmem_base + st * 256 + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
       for (int c = c_begin; c < c_end; ++c) {
         const int col0 = nb * out_bn + c * 32;
@@ -244,8 +264,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            if (leader) mbar_arrive(&tempty[buf]);
-            else mbar_arrive_cluster(tempty_leader[buf]);
+            if (leader) mbar_arrive(&tempty[st]);
+            else mbar_arrive_cluster(tempty_leader[st]);
           }
         }
         const RowLoads cur = L;
