@@ -135,3 +135,29 @@ def test_stream_argument_is_honoured(cuda_lib):
         cuda_lib.gemm_epilogue(dA, dB, "nk", None, None, None, out, M, N, K, stream=s)
     assert cuda_lib.gbf_check_device_error(s) == 0
     assert_parity(down(out), oracle.gemm_epilogue(A, B, "nk", M=M, N=N, K=K), "side stream")
+
+
+@pytest.mark.parametrize("M", [16, 32])
+def test_weight_only_kernel_timeout_is_reported_and_recoverable(cuda_lib, M):
+    # the weight-only kernel at M <= 16 issues its MMAs from the transform
+    # warps (group barriers), at M = 32 from one issuer warp; a withheld
+    # accumulator-ready signal must end in GBF_ERR_TIMEOUT on both, and the
+    # next call on the same context must be correct
+    N, K, G = 1024, 1024, 128
+    w = workloads.make("w4a16", shape=dict(M=M, N=N, K=K, group=G))
+    out = poison_bf16(M, N)
+    cuda_lib.gbf_set_wait_timeout_ns(50_000_000)
+    cuda_lib.gbf_debug_inject_timeout(True)
+    try:
+        cuda_lib.w4a16_gemm(up(w["A"]), up(w["Wq"]), up(w["scales"]), G, None, None, None, out,
+                            M, N, K)
+        assert cuda_lib.gbf_check_device_error() == 6
+    finally:
+        cuda_lib.gbf_debug_inject_timeout(False)
+        cuda_lib.gbf_set_wait_timeout_ns(2_000_000_000)
+    assert cuda_lib.gbf_check_device_error() == 0
+    cuda_lib.w4a16_gemm(up(w["A"]), up(w["Wq"]), up(w["scales"]), G, None, None, None, out,
+                        M, N, K)
+    assert cuda_lib.gbf_check_device_error() == 0
+    assert_parity(down(out), oracle.w4a16(w["A"], w["Wq"], w["scales"], G, M=M, N=N, K=K),
+                  "after timeout")
