@@ -640,7 +640,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="prefill",
                     help="prefill | swiglu | w4a16 | tiny | sweep-<M>")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--unfused-steps", type=int, default=200)
+    ap.add_argument("--unfused-steps", type=int, default=200,
+                    help="upper bound on the steps of one block of the fused/unfused comparison")
+    ap.add_argument("--speedup-rounds", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -717,13 +719,24 @@ def main(argv=None):
         raise SystemExit("kernel reported a timeout in the timed region")
     value = total_units / max_region / vscale
 
-    # unfused composition, same workload, same rotation of input sets
+    # unfused composition, same workload, same rotation of input sets.  The
+    # speedup is taken from alternating blocks of fused and unfused steps of
+    # equal length (about 0.1 s each), so that both see the same clock and
+    # power-cap state; the median block ratio is reported.
     for i in range(3):
         wl.unfused(i)
     torch.cuda.synchronize()
-    un_region, _ = time_loop(wl.unfused, args.unfused_steps, stream, per_launch=False)
-    un_ms = un_region / args.unfused_steps * 1e3
     fu_ms = max_region / args.steps * 1e3
+    block = max(3, min(args.unfused_steps, int(0.1 / max(per_launch, 1e-6))))
+    ratios, un_times, fu_times = [], [], []
+    for _ in range(args.speedup_rounds):
+        f_reg, _ = time_loop(wl.fused, block, stream, per_launch=False)
+        u_reg, _ = time_loop(wl.unfused, block, stream, per_launch=False)
+        ratios.append(u_reg / f_reg)
+        un_times.append(u_reg / block * 1e3)
+        fu_times.append(f_reg / block * 1e3)
+    un_ms = statistics.median(un_times)
+    speedup = statistics.median(ratios)
 
     # end to end through the public API with host buffers
     for _ in range(2):
@@ -788,7 +801,10 @@ def main(argv=None):
         "roofline": roof,
         "unfused_ms_per_step": un_ms,
         "unfused_kind": wl.unfused_kind(),
-        "speedup_vs_unfused": un_ms / fu_ms,
+        "speedup_vs_unfused": speedup,
+        "speedup_method": (f"median over {args.speedup_rounds} alternating blocks of {block} fused "
+                           f"and {block} unfused steps (fused block {statistics.median(fu_times):.4f}"
+                           f" ms/step)"),
         "e2e": {"value": e2e_units / e2e_max / vscale, "unit": vunit,
                 "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
         "gpu_launches": args.steps * wl.launches_per_step(),
