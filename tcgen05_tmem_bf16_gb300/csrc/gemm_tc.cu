@@ -279,6 +279,8 @@ __device__ __forceinline__ void acc_sum16(uint32_t taddr, float (&out)[16]) {
   }
 }
 
+constexpr int kSwapIssuers = 2;  // MMA issuing threads of the swapped kernel
+
 template <int MPAD, bool DUAL = false>
 struct SwapCfg {
   // weight tile: 128 rows x 64 k (16 KB); the gate/up GEMM stages the gate
@@ -358,10 +360,10 @@ __global__ void __launch_bounds__(256, 2)
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], kSwapIssuers);
     }
-    mbar_init(dfull, 1);
-    mbar_init(done, 1);
+    mbar_init(dfull, kSwapIssuers);
+    mbar_init(done, kSwapIssuers);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -413,9 +415,16 @@ __global__ void __launch_bounds__(256, 2)
         if (fills[i]) wait_bar(&full[i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3) {
+    // Two MMA issuers: warp 1 issues K steps 0-1 and warp 3 K steps 2-3 of
+    // every stage (the MMAs of one thread complete one after another, those
+    // of two threads overlap).  K step k goes to accumulator k*kAcc/4, so each
+    // accumulator has one writer.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kBM, MPAD, W_KN, false);
+      constexpr int kSteps = kBK / kUK;              // 4
+      constexpr int kPer = kSteps / kSwapIssuers;    // K steps per issuer and stage
+      const int k0 = warp == 1 ? 0 : kPer;
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -428,18 +437,18 @@ __global__ void __launch_bounds__(256, 2)
         const uint32_t w0 = smem_u32(stages + s * Cfg::kStageBytes);
         const uint32_t x0 = w0 + Cfg::kWBytes;
 #pragma unroll
-        for (int k = 0; k < kBK / kUK; ++k) {
+        for (int k = k0; k < k0 + kPer; ++k) {
           const uint64_t ad = W_KN ? sdesc_sw128(w0 + k * 2048, 8192, 1024)
                                    : sdesc_sw128(w0 + k * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(x0 + k * 32, 16, 1024);
-          const int j = (kb - kb0) * (kBK / kUK) + k;  // K step within this CTA's range
-          mma_ss(tmem_base + (j % Cfg::kAcc) * MPAD, ad, bd, idesc, j >= Cfg::kAcc ? 1u : 0u);
+          const int acc = k * Cfg::kAcc / kSteps;
+          const uint32_t accum = (kb > kb0 || (k % (kSteps / Cfg::kAcc)) != 0) ? 1u : 0u;
+          mma_ss(tmem_base + acc * MPAD, ad, bd, idesc, accum);
           if constexpr (DUAL) {
             const uint32_t w1 = w0 + Cfg::kWTile;
             const uint64_t ad2 = W_KN ? sdesc_sw128(w1 + k * 2048, 8192, 1024)
                                       : sdesc_sw128(w1 + k * 32, 16, 1024);
-            mma_ss(tmem_base + (Cfg::kAcc + j % Cfg::kAcc) * MPAD, ad2, bd, idesc,
-                   j >= Cfg::kAcc ? 1u : 0u);
+            mma_ss(tmem_base + (Cfg::kAcc + acc) * MPAD, ad2, bd, idesc, accum);
           }
         }
         mma_commit(&empty[s]);
