@@ -381,18 +381,16 @@ __global__ void __launch_bounds__(256, 2)
   const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
   const long long t_start = clock64();
 
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
   if (warp == 0) {
     if (lane == 0) {
       uint32_t fills[Cfg::kStages];
 #pragma unroll
       for (int i = 0; i < Cfg::kStages; ++i) fills[i] = 0;
-      int s = 0;
-      uint32_t ph = 0;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) break;
+      // weight tiles of k block kb into stage s (read-only inputs)
+      auto load_w = [&](int s, int kb) {
         uint8_t* sw = stages + s * Cfg::kStageBytes;
-        uint8_t* sx = sw + Cfg::kWBytes;
-        mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
 #pragma unroll
         for (int w = 0; w < Cfg::kProducts; ++w) {
           const CUtensorMap* map = w == 0 ? &tmW : &tmW2;
@@ -404,7 +402,28 @@ __global__ void __launch_bounds__(256, 2)
             tma_load_2d(dst, map, &full[s], kb * kBK, nb * kSwapBN);
           }
         }
-        tma_load_2d(sx, &tmA, &full[s], kb * kBK, mb * MPAD);
+      };
+      auto load_x = [&](int s, int kb) {
+        tma_load_2d(stages + s * Cfg::kStageBytes + Cfg::kWBytes, &tmA, &full[s], kb * kBK,
+                    mb * MPAD);
+      };
+      // The first stages' weights are requested before waiting for the
+      // previous kernel in the stream (which may produce the activations).
+      const int pre = kb1 - kb0 < Cfg::kStages ? kb1 - kb0 : Cfg::kStages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], Cfg::kStageBytes);
+        load_w(i, kb0 + i);
+        fills[i]++;
+      }
+      griddep_wait();
+      for (int i = 0; i < pre; ++i) load_x(i, kb0 + i);
+      int s = pre % Cfg::kStages;
+      uint32_t ph = pre == Cfg::kStages ? 1u : 0u;
+      for (int kb = kb0 + pre; kb < kb1; ++kb) {
+        if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) break;
+        mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+        load_w(s, kb);
+        load_x(s, kb);
         fills[s]++;
         if (++s == Cfg::kStages) {
           s = 0;
@@ -480,6 +499,7 @@ __global__ void __launch_bounds__(256, 2)
   const uint64_t pol = l2_evict_first_policy();
   const int n = nb * kSwapBN + tid;
   ColLoads L;
+  if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
   if (epi && static_cast<int>(rank) < kChunks)  // this rank's first chunk: operands early
     col16_prefetch(L, static_cast<int64_t>(mb) * MPAD + static_cast<int>(rank) * 16, n, a.M,
                    a.N, a.ep, pol);
@@ -607,13 +627,17 @@ cudaError_t run_swap(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMa
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel in the stream finishes (it waits
+  // with griddepcontrol.wait before touching anything that kernel writes)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, tmW2, args);
 }
 

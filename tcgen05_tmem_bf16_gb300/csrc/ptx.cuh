@@ -114,6 +114,18 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait: block until the grids this
+// one depends on (the previous kernel in the stream, when launched with
+// programmatic stream serialization) have completed and their writes are
+// visible; a no-op otherwise.  griddep_launch_dependents: let the next grid
+// be scheduled once every CTA of this one has issued it or exited.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

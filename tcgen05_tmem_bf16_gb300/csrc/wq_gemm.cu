@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   const uint32_t tmem_base = *tmem_holder;
   const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
   const long long t_start = clock64();
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -355,24 +356,42 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       uint32_t fills[Cfg::kStages];
 #pragma unroll
       for (int i = 0; i < Cfg::kStages; ++i) fills[i] = 0;
-      int s = 0;
-      uint32_t ph = 0;
-      for (int kb = kb0; kb < kb1; ++kb) {
-        if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) break;
+      // weight codes and scales of k block kb into stage s (read-only inputs)
+      auto load_w = [&](int s, int kb) {
         uint8_t* sq = stages + s * Cfg::kStageBytes;
-        uint8_t* sx = sq + Cfg::kQBytes;
-        uint8_t* ss = sx + Cfg::kXBytes;
+        uint8_t* ss = sq + Cfg::kQBytes + Cfg::kXBytes;
         // scale rows: one group row (int4, fp8) or four 16-deep blocks (nvfp4)
         const int srow = FMT == kWqNvfp4 ? kb * (kBK / 16) : (kb * kBK) / group;
-        mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
         // the weight tile in boxes of 256 bytes x 64 k-rows
 #pragma unroll
         for (int h = 0; h < Cfg::kRowBytes / 256; ++h)
           tma_load_2d_hint(sq + h * (kBK * 256), &tmQ, &full[s], nb * Cfg::kRowBytes + 256 * h,
                            kb * kBK, stream_policy);
-        tma_load_2d(sx, &tmA, &full[s], kb * kBK, mb * MPAD);
         tma_load_2d(ss, &tmS, &full[s], nb * kW4BN, srow);
         tma_load_2d(ss + Cfg::kScaleBytes / 2, &tmS, &full[s], nb * kW4BN + 256, srow);
+      };
+      auto load_x = [&](int s, int kb) {
+        tma_load_2d(stages + s * Cfg::kStageBytes + Cfg::kQBytes, &tmA, &full[s], kb * kBK,
+                    mb * MPAD);
+      };
+      // The first stages' weights are requested before waiting for the
+      // previous kernel in the stream (which may produce the activations):
+      // they overlap its tail.
+      const int pre = kb1 - kb0 < Cfg::kStages ? kb1 - kb0 : Cfg::kStages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], Cfg::kStageBytes);
+        load_w(i, kb0 + i);
+        fills[i]++;
+      }
+      griddep_wait();
+      for (int i = 0; i < pre; ++i) load_x(i, kb0 + i);
+      int s = pre % Cfg::kStages;
+      uint32_t ph = pre == Cfg::kStages ? 1u : 0u;
+      for (int kb = kb0 + pre; kb < kb1; ++kb) {
+        if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) break;
+        mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+        load_w(s, kb);
+        load_x(s, kb);
         fills[s]++;
         if (++s == Cfg::kStages) {
           s = 0;
@@ -548,6 +567,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   // to the (rank, group) workers round-robin and are summed over ranks
   // 0..S-1 in that order through distributed shared memory.
   const bool epi = warp >= 4;
+  if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
   const int g = (warp - 4) >> 2;
   const int q = warp & 3;
   const int tid = q * 32 + lane;
@@ -668,13 +688,17 @@ cudaError_t run_w4(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap&
   cfg.blockDim = dim3(kW4Threads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel in the stream finishes (it waits
+  // with griddepcontrol.wait before touching anything that kernel writes)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmQ, tmS, args, group);
 }
 

@@ -1,0 +1,71 @@
+"""Back-to-back dependent calls on one stream, with no host synchronisation in
+between: the decode kernels (swapped split-K GEMM, weight-only GEMM) may start
+while the previous kernel finishes and prefetch their weights, so each call
+must still see the complete output of the call before it.  Every stage is
+checked against the oracle on the GPU's own input of that stage."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_util import assert_parity, down, poison_bf16, up
+
+pytestmark = pytest.mark.gpu
+
+
+def rand_bf16(seed, shape, std=1.0):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return workloads.to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
+
+
+def test_chain_of_swapped_gemms_reads_each_previous_output(cuda_lib):
+    # x_{i+1} = x_i * W_i^T + x_i (the residual is the previous output too)
+    M, D, steps = 16, 2048, 6
+    ws = [rand_bf16(100 + i, (D, D), std=D ** -0.5) for i in range(steps)]
+    x0 = rand_bf16(99, (M, D))
+    xs = [up(x0)] + [poison_bf16(M, D) for _ in range(steps)]
+    dws = [up(w) for w in ws]
+    for i in range(steps):
+        cuda_lib.gemm_epilogue(xs[i], dws[i], "nk", None, None, xs[i], xs[i + 1], M, D, D)
+    assert cuda_lib.gbf_check_device_error() == 0
+    assert cuda_lib.gbf_kernel_path("gemm_epilogue", M, D, D, "nk")[0] == "swap_splitk"
+    for i in range(steps):
+        xin = down(xs[i])
+        want = oracle.gemm_epilogue(xin, ws[i], "nk", residual=xin, M=M, N=D, K=D)
+        assert_parity(down(xs[i + 1]), want, f"chain step {i}")
+
+
+def test_chain_of_weight_only_gemms_reads_each_previous_output(cuda_lib):
+    M, D, G, steps = 16, 2048, 128, 5
+    rng = np.random.Generator(np.random.PCG64(7))
+    qs = [rng.integers(0, 256, size=(D, D // 2), dtype=np.uint8) for _ in range(steps)]
+    ss = [workloads.to_bf16_bits(rng.uniform(0.002, 0.006, size=(D // G, D)).astype(np.float32))
+          for _ in range(steps)]
+    x0 = rand_bf16(5, (M, D))
+    xs = [up(x0)] + [poison_bf16(M, D) for _ in range(steps)]
+    dq, ds = [up(q) for q in qs], [up(s) for s in ss]
+    for i in range(steps):
+        cuda_lib.w4a16_gemm(xs[i], dq[i], ds[i], G, None, None, None, xs[i + 1], M, D, D,
+                            act="silu")
+    assert cuda_lib.gbf_check_device_error() == 0
+    for i in range(steps):
+        want = oracle.w4a16(down(xs[i]), qs[i], ss[i], G, M=M, N=D, K=D, act="silu")
+        assert_parity(down(xs[i + 1]), want, f"w4a16 chain step {i}")
+
+
+def test_weight_only_gemm_after_a_plain_kernel_sees_its_writes(cuda_lib):
+    # a torch kernel (no programmatic launch) writes the activations right
+    # before the call
+    M, N, K, G = 16, 1024, 1024, 128
+    w = workloads.make("w4a16", shape=dict(M=M, N=N, K=K, group=G))
+    A = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    out = poison_bf16(M, N)
+    src = up(w["A"])
+    for _ in range(3):
+        A.zero_()
+        A.copy_(src)
+        cuda_lib.w4a16_gemm(A, up(w["Wq"]), up(w["scales"]), G, None, None, None, out, M, N, K)
+    assert cuda_lib.gbf_check_device_error() == 0
+    assert_parity(down(out), oracle.w4a16(w["A"], w["Wq"], w["scales"], G, M=M, N=N, K=K),
+                  "after a copy kernel")
