@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int num_tiles = a.m_tiles * a.n_tiles;
   const int num_kb = a.num_kb;
   const int out_bn = DUAL ? 128 : BN;
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
@@ -143,10 +144,29 @@ __global__ void __launch_bounds__(kQThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
+      // The B (weight) tiles of the first tile's first stages are requested
+      // before waiting for the previous kernel in the stream, which may
+      // produce A; their A tiles follow the wait.
+      bool waited = false;
+      int deferred = 0;
+      int mb_first = 0;
+      auto flush = [&]() {
+        if (waited) return;
+        griddep_wait();
+        waited = true;
+        for (int j = 0; j < deferred; ++j) {
+          const int g = st * kQRing + j;
+          tma_load_2d_pair(stages + g * Cfg::kStageBytes, &tmA,
+                           mapa_shared(smem_u32(&full[g]), 0), j * kBK,
+                           mb_first * kQTileM + static_cast<int>(rank) * kBM);
+        }
+      };
       for (int t = pair + st * npairs; t < num_tiles && ok; t += kQStreams * npairs) {
         int mb, nb;
         tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+        if (!waited) mb_first = mb;
         for (int kb = 0; kb < num_kb; ++kb) {
+          if (!waited && kb >= kQRing) flush();
           const int g = st * kQRing + s;
           if (!wait_bar(&empty[g], ph ^ 1, ctl, kSiteProducerEmpty)) {
             ok = false;
@@ -156,7 +176,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
           uint8_t* sb = sa + kQABytes;
           const uint32_t bar = mapa_shared(smem_u32(&full[g]), 0);
           if (leader) mbar_arrive_expect_tx(&full[g], 2 * Cfg::kStageBytes);
-          tma_load_2d_pair(sa, &tmA, bar, kb * kBK, mb * kQTileM + static_cast<int>(rank) * kBM);
+          if (waited)
+            tma_load_2d_pair(sa, &tmA, bar, kb * kBK, mb * kQTileM + static_cast<int>(rank) * kBM);
+          else
+            ++deferred;
           const CUtensorMap* wmap = (DUAL && rank) ? &tmW2 : &tmW;
           const int n0 = DUAL ? nb * 128 : nb * BN + static_cast<int>(rank) * (BN / 2);
           if constexpr (W_KN) {
@@ -171,6 +194,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             ph ^= 1;
           }
         }
+        flush();
       }
       if (ok) {
         // Every copy is consumed before the MMA reports the stage empty.
@@ -229,6 +253,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     // the pair's tiles in order: local tile l belongs to stream l % 2
+    griddep_wait();  // the ending reads C, bias, residual and writes out
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;
     const uint64_t pol = l2_evict_first_policy();
@@ -316,13 +341,17 @@ cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMa
   cfg.blockDim = dim3(kQThreads, 1, 1);
   cfg.dynamicSmemBytes = kQSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel in the stream finishes (it waits
+  // with griddepcontrol.wait before touching anything that kernel writes)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, tmW2, args);
 }
 

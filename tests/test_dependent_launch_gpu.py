@@ -36,6 +36,25 @@ def test_chain_of_swapped_gemms_reads_each_previous_output(cuda_lib):
         assert_parity(down(xs[i + 1]), want, f"chain step {i}")
 
 
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+def test_chain_of_pair_gemms_reads_each_previous_output(cuda_lib, layout):
+    # M >= 512: the CTA-pair kernel, which also requests its first weight
+    # tiles before waiting for the previous kernel
+    M, D, steps = 1024, 1024, 4
+    ws = [rand_bf16(200 + i, (D, D), std=D ** -0.5) for i in range(steps)]
+    x0 = rand_bf16(199, (M, D))
+    xs = [up(x0)] + [poison_bf16(M, D) for _ in range(steps)]
+    dws = [up(w) for w in ws]
+    for i in range(steps):
+        cuda_lib.gemm_epilogue(xs[i], dws[i], layout, None, None, xs[i], xs[i + 1], M, D, D)
+    assert cuda_lib.gbf_check_device_error() == 0
+    assert cuda_lib.gbf_kernel_path("gemm_epilogue", M, D, D, layout)[0] == "pair"
+    for i in range(steps):
+        xin = down(xs[i])
+        want = oracle.gemm_epilogue(xin, ws[i], layout, residual=xin, M=M, N=D, K=D)
+        assert_parity(down(xs[i + 1]), want, f"pair chain {layout} step {i}")
+
+
 def test_chain_of_weight_only_gemms_reads_each_previous_output(cuda_lib):
     M, D, G, steps = 16, 2048, 128, 5
     rng = np.random.Generator(np.random.PCG64(7))
