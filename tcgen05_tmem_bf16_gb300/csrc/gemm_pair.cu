@@ -144,29 +144,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      // The B (weight) tiles of the first tile's first stages are requested
-      // before waiting for the previous kernel in the stream, which may
-      // produce A; their A tiles follow the wait.
-      bool waited = false;
-      int deferred = 0;
-      int mb_first = 0;
-      auto flush = [&]() {
-        if (waited) return;
-        griddep_wait();
-        waited = true;
-        for (int j = 0; j < deferred; ++j) {
-          const int g = st * kQRing + j;
-          tma_load_2d_pair(stages + g * Cfg::kStageBytes, &tmA,
-                           mapa_shared(smem_u32(&full[g]), 0), j * kBK,
-                           mb_first * kQTileM + static_cast<int>(rank) * kBM);
-        }
-      };
+      // Nothing is read before the previous kernel in the stream has
+      // completed: any input, weights included, may be its output.
+      griddep_wait();
       for (int t = pair + st * npairs; t < num_tiles && ok; t += kQStreams * npairs) {
         int mb, nb;
         tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
-        if (!waited) mb_first = mb;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!waited && kb >= kQRing) flush();
           const int g = st * kQRing + s;
           if (!wait_bar(&empty[g], ph ^ 1, ctl, kSiteProducerEmpty)) {
             ok = false;
@@ -176,10 +160,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           uint8_t* sb = sa + kQABytes;
           const uint32_t bar = mapa_shared(smem_u32(&full[g]), 0);
           if (leader) mbar_arrive_expect_tx(&full[g], 2 * Cfg::kStageBytes);
-          if (waited)
-            tma_load_2d_pair(sa, &tmA, bar, kb * kBK, mb * kQTileM + static_cast<int>(rank) * kBM);
-          else
-            ++deferred;
+          tma_load_2d_pair(sa, &tmA, bar, kb * kBK, mb * kQTileM + static_cast<int>(rank) * kBM);
           const CUtensorMap* wmap = (DUAL && rank) ? &tmW2 : &tmW;
           const int n0 = DUAL ? nb * 128 : nb * BN + static_cast<int>(rank) * (BN / 2);
           if constexpr (W_KN) {
@@ -194,7 +175,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
             ph ^= 1;
           }
         }
-        flush();
       }
       if (ok) {
         // Every copy is consumed before the MMA reports the stage empty.

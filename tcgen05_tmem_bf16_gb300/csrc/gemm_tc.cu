@@ -407,19 +407,12 @@ __global__ void __launch_bounds__(256, 2)
         tma_load_2d(stages + s * Cfg::kStageBytes + Cfg::kWBytes, &tmA, &full[s], kb * kBK,
                     mb * MPAD);
       };
-      // The first stages' weights are requested before waiting for the
-      // previous kernel in the stream (which may produce the activations).
-      const int pre = kb1 - kb0 < Cfg::kStages ? kb1 - kb0 : Cfg::kStages;
-      for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], Cfg::kStageBytes);
-        load_w(i, kb0 + i);
-        fills[i]++;
-      }
+      // Nothing is read before the previous kernel in the stream has
+      // completed: any input, weights included, may be its output.
       griddep_wait();
-      for (int i = 0; i < pre; ++i) load_x(i, kb0 + i);
-      int s = pre % Cfg::kStages;
-      uint32_t ph = pre == Cfg::kStages ? 1u : 0u;
-      for (int kb = kb0 + pre; kb < kb1; ++kb) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) break;
         mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
         load_w(s, kb);

@@ -88,3 +88,22 @@ def test_weight_only_gemm_after_a_plain_kernel_sees_its_writes(cuda_lib):
     assert cuda_lib.gbf_check_device_error() == 0
     assert_parity(down(out), oracle.w4a16(w["A"], w["Wq"], w["scales"], G, M=M, N=N, K=K),
                   "after a copy kernel")
+
+
+@pytest.mark.parametrize("M1", [128, 640])
+def test_weight_operand_written_by_the_previous_call(cuda_lib, M1):
+    # the first call's output becomes the second call's B operand (W [N][K]),
+    # so the second kernel must not fetch any operand before the first ends
+    K1, N2, M2 = 256, 1024, 16
+    X = rand_bf16(301, (M1, K1))
+    Y = rand_bf16(302, (N2, K1), std=K1 ** -0.5)
+    A = rand_bf16(303, (M2, N2))
+    W = poison_bf16(M1, N2)  # written by call 1: [M1][N2] = W [N][K] of call 2
+    out = poison_bf16(M2, M1)
+    cuda_lib.gemm_epilogue(up(X), up(Y), "nk", None, None, None, W, M1, N2, K1)
+    cuda_lib.gemm_epilogue(up(A), W, "nk", None, None, None, out, M2, M1, N2)
+    assert cuda_lib.gbf_check_device_error() == 0
+    w = down(W)
+    assert_parity(w, oracle.gemm_epilogue(X, Y, "nk", M=M1, N=N2, K=K1), "first call")
+    assert_parity(down(out), oracle.gemm_epilogue(A, w, "nk", M=M2, N=M1, K=N2),
+                  "second call on the first call's output")
