@@ -328,11 +328,18 @@ GBF_API gbf_status_t gbf_debug_set_profile(void *counters, size_t bytes);
 GBF_API gbf_status_t gbf_debug_force_splits(int splits);
 
 /* Which kernel family a call with these arguments runs (for tests and the
- * benchmark's roofline attribution): 1 = persistent 128x256-tile kernel,
- * 2 = small-M swapped kernel with cluster split-K, 3 = W4A16 kernel,
- * 4 = persistent 256x256-tile kernel on CTA pairs (large M),
+ * benchmark's roofline attribution).  op: GBF_OP_GEMM_EPILOGUE,
+ * GBF_OP_SWIGLU, GBF_OP_W4A16, GBF_OP_W8A16_FP8 or GBF_OP_W4A16_NVFP4.
+ * Returns 1 = persistent 128x256-tile kernel, 2 = small-M swapped kernel
+ * with cluster split-K (also the gate/up GEMM at M <= 32), 3 = weight-only
+ * kernel (int4, FP8, NVFP4), 4 = persistent kernel on CTA pairs (M >= 512),
  * 0 = no launch (empty output), -1 = the arguments would be rejected.
- * `*splits` (may be NULL) receives the split-K cluster size. */
+ * `*splits` (may be NULL) receives the split-K cluster size.
+ *
+ * Kernels of families 2, 3 and 4 are launched with programmatic stream
+ * serialization: they may begin while the previous kernel in the stream is
+ * finishing, and read or write nothing in global memory before it has
+ * completed (griddepcontrol.wait), so stream order is preserved. */
 GBF_API int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int *splits);
 
 /* Library version, e.g. 100 for 1.0.0. */
