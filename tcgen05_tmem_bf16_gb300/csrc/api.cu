@@ -264,17 +264,18 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const De
     if (!dual && !kn) {
       // A 224-wide tile when it wastes less of the last round of tiles:
       // compare useful area / (rounds * pairs * tile area).
+      // (a pair computes two M-tiles at a time: 512 x bn per round)
       auto eff = [&](int bn) {
-        const int64_t tiles = static_cast<int64_t>(p.m_tiles) * ceil_div(N, bn);
+        const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * ceil_div(N, bn);
         const int64_t rounds = (tiles + dev.pairs - 1) / dev.pairs;
-        return static_cast<double>(M) * N / (static_cast<double>(rounds) * dev.pairs * 256 * bn);
+        return static_cast<double>(M) * N / (static_cast<double>(rounds) * dev.pairs * 512 * bn);
       };
       if (eff(224) > eff(256) * 1.02) {
         p.bn = 224;
         p.n_tiles = ceil_div(N, 224);
       }
     }
-    p.grid = 2 * std::min(p.m_tiles * p.n_tiles, dev.pairs);
+    p.grid = 2 * std::min(((p.m_tiles + 1) / 2) * p.n_tiles, dev.pairs);
   } else {
     p.path = kPathPersistent;
     p.m_tiles = ceil_div(M, kBM);

@@ -25,11 +25,15 @@
 // Two streams per pair.  The tcgen05.mma instructions of one issuing thread
 // complete one after another, about 150 cycles each on this part whatever
 // their N, which caps one stream of 256 x BN x 16 MMAs at 112-128 cycles of
-// tensor work per 150.  So the pair runs two independent pipelines: stream i
-// takes every other tile of the pair's sequence, with its own producer
-// threads, its own 3-stage ring, its own MMA issuer (both in the even CTA),
-// its own accumulator (TMEM columns 256i .. 256i+BN) and its own epilogue
-// warpgroup.  The two issuers' MMAs overlap in the tensor cores.
+// tensor work per 150.  So the pair runs two MMA streams, one per
+// accumulator (TMEM columns 256i .. 256i+BN), issued by two threads of the
+// even CTA.  They compute the two M-tiles of an M-tile pair with the same B
+// tile: each ring stage holds both A tiles and the shared B tile, so a k
+// step moves 2 x 16 KB of A and one B half per CTA for two tiles' MMAs
+// (23 KB per tile instead of 30-32 KB).  The two epilogue warpgroups drain
+// the accumulators in tile order (stream 0's, then stream 1's), each taking
+// half of the tile's columns, with the C / residual rows of a tile pulled
+// into L2 before its accumulator is ready.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,9 +47,8 @@
 
 namespace gbf {
 
-constexpr int kQStages = 6;
-constexpr int kQStreams = 2;
-constexpr int kQRing = kQStages / kQStreams;  // stages per stream
+constexpr int kQStages = 4;
+constexpr int kQStreams = 2;                   // MMA streams = M-tiles per stage
 constexpr int kQABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int kQThreads = 384;                 // warps 0-3 roles, 4-11 epilogue
 constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
@@ -56,7 +59,7 @@ constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
 template <int BN>
 struct PairCfg {
   static constexpr int kBBytes = (BN / 2) * kBK * 2;
-  static constexpr int kStageBytes = kQABytes + kBBytes;
+  static constexpr int kStageBytes = kQStreams * kQABytes + kBBytes;  // A0 | A1 | B
   static constexpr int kSmem = 1024 + kQStages * kStageBytes + 256;
   static constexpr int kChunks = BN / 32;             // 32-column epilogue chunks
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], kQStreams);  // both issuers' commits
     }
     for (int i = 0; i < kQStreams; ++i) {
       mbar_init(&tfull[i], 1);
@@ -127,40 +130,40 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
   const long long t_start = clock64();
-  const int num_tiles = a.m_tiles * a.n_tiles;
+  const int m_pairs = (a.m_tiles + 1) / 2;      // M-tile pairs (the last may be half empty)
+  const int num_super = m_pairs * a.n_tiles;     // a super tile = an M-tile pair x one N-tile
   const int num_kb = a.num_kb;
   const int out_bn = DUAL ? 128 : BN;
   if (threadIdx.x == 0) griddep_launch_dependents();
 
-  if (warp == 0 || warp == 3) {
-    // ------------------------------------------------------------ TMA producers (both CTAs)
-    // warp 0 feeds stream 0, warp 3 stream 1; stream i's stages are
-    // [kQRing*i, kQRing*(i+1)) and its tiles every other one of the pair's.
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      const int st = warp == 0 ? 0 : 1;
-      uint32_t fills[kQRing];
+      uint32_t fills[kQStages];
 #pragma unroll
-      for (int i = 0; i < kQRing; ++i) fills[i] = 0;
+      for (int i = 0; i < kQStages; ++i) fills[i] = 0;
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
       // Nothing is read before the previous kernel in the stream has
       // completed: any input, weights included, may be its output.
       griddep_wait();
-      for (int t = pair + st * npairs; t < num_tiles && ok; t += kQStreams * npairs) {
-        int mb, nb;
-        tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+      for (int t = pair; t < num_super && ok; t += npairs) {
+        int mp, nb;
+        tile_coords(t, m_pairs, a.n_tiles, mp, nb);
         for (int kb = 0; kb < num_kb; ++kb) {
-          const int g = st * kQRing + s;
-          if (!wait_bar(&empty[g], ph ^ 1, ctl, kSiteProducerEmpty)) {
+          if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
-          uint8_t* sa = stages + g * Cfg::kStageBytes;
-          uint8_t* sb = sa + kQABytes;
-          const uint32_t bar = mapa_shared(smem_u32(&full[g]), 0);
-          if (leader) mbar_arrive_expect_tx(&full[g], 2 * Cfg::kStageBytes);
-          tma_load_2d_pair(sa, &tmA, bar, kb * kBK, mb * kQTileM + static_cast<int>(rank) * kBM);
+          uint8_t* sa = stages + s * Cfg::kStageBytes;
+          uint8_t* sb = sa + kQStreams * kQABytes;
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * Cfg::kStageBytes);
+#pragma unroll
+          for (int i = 0; i < kQStreams; ++i)  // rows past M read as zeros
+            tma_load_2d_pair(sa + i * kQABytes, &tmA, bar, kb * kBK,
+                             (2 * mp + i) * kQTileM + static_cast<int>(rank) * kBM);
           const CUtensorMap* wmap = (DUAL && rank) ? &tmW2 : &tmW;
           const int n0 = DUAL ? nb * 128 : nb * BN + static_cast<int>(rank) * (BN / 2);
           if constexpr (W_KN) {
@@ -170,17 +173,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
             tma_load_2d_pair(sb, wmap, bar, kb * kBK, n0);
           }
           fills[s]++;
-          if (++s == kQRing) {
+          if (++s == kQStages) {
             s = 0;
             ph ^= 1;
           }
         }
       }
       if (ok) {
-        // Every copy is consumed before the MMA reports the stage empty.
-        for (int i = 0; i < kQRing; ++i)
-          if (fills[i])
-            wait_bar(&empty[st * kQRing + i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
+        // Every copy is consumed before the MMAs report the stage empty.
+        for (int i = 0; i < kQStages; ++i)
+          if (fills[i]) wait_bar(&empty[i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
       } else {
         settle_after_abort();
       }
@@ -188,8 +190,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers (even CTA)
-    // warp 1 lane 0 issues stream 0, warp 2 lane 0 stream 1 (warp 2 also
-    // allocates and frees the tensor memory, outside this loop)
+    // warp 1 lane 0 issues stream 0 (the pair's even M-tile), warp 2 lane 0
+    // stream 1 (the odd one) from the same stages; warp 2 also allocates and
+    // frees the tensor memory, outside this loop
     if (lane == 0 && leader) {
       constexpr uint32_t idesc = idesc_bf16(kQTileM, BN, false, W_KN);
       const int st = warp - 1;
@@ -198,18 +201,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
       uint32_t ph = 0;
       int local = 0;
       bool ok = true;
-      for (int t = pair + st * npairs; t < num_tiles && ok; t += kQStreams * npairs, ++local) {
+      for (int t = pair; t < num_super && ok; t += npairs, ++local) {
         if (!wait_bar(&tempty[st], (local & 1) ^ 1, ctl, kSiteMmaAccEmpty)) break;
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          const int g = st * kQRing + s;
-          if (!wait_bar(&full[g], ph, ctl, kSiteMmaFull)) {
+          if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(stages + g * Cfg::kStageBytes);
-          const uint32_t b0 = a0 + kQABytes;
+          const uint32_t s0 = smem_u32(stages + s * Cfg::kStageBytes);
+          const uint32_t a0 = s0 + st * kQABytes;
+          const uint32_t b0 = s0 + kQStreams * kQABytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
@@ -217,8 +220,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
                                      : sdesc_sw128(b0 + k * 32, 16, 1024);
             mma_ss_pair(d, ad, bd, idesc, (kb | k) != 0);
           }
-          mma_commit_pair(&empty[g], 0x3);
-          if (++s == kQRing) {
+          mma_commit_pair(&empty[s], 0x3);
+          if (++s == kQStages) {
             s = 0;
             ph ^= 1;
           }
@@ -243,11 +246,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int c_end = half == 0 ? kFirst : kChunks;
     const uint32_t tempty_leader[kQStreams] = {mapa_shared(smem_u32(&tempty[0]), 0),
                                                mapa_shared(smem_u32(&tempty[1]), 0)};
-    int local = 0;
-    for (int t = pair; t < num_tiles; t += npairs, ++local) {
-      int mb, nb;
-      tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+    // tile l of the pair: super tile pair + (l / 2) * npairs, M-tile l % 2 of it
+    for (int local = 0; pair + (local / kQStreams) * npairs < num_super; ++local) {
       const int st = local % kQStreams;
+      int mp, nb;
+      tile_coords(pair + (local / kQStreams) * npairs, m_pairs, a.n_tiles, mp, nb);
+      const int mb = 2 * mp + st;
       const uint32_t aph = (local / kQStreams) & 1;
       const int64_t row =
           static_cast<int64_t>(mb) * kQTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
