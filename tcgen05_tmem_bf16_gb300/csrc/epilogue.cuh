@@ -95,16 +95,17 @@ __device__ __forceinline__ void epi_row32(const uint32_t (&acc)[32], const uint3
   }
 }
 
-// Persistent tile raster: groups of kGroupM M-tiles; inside a group the
-// N-tile index varies slowest, so the CTAs working at the same time share
-// weight panels (and activation panels) in L2.
+// Persistent tile raster: groups of `group` M-tiles (kGroupM by default);
+// inside a group the N-tile index varies slowest, so the CTAs working at the
+// same time share weight panels (and activation panels) in L2.
 constexpr int kGroupM = 16;
 
-__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mb, int& nb) {
-  const int per_group = kGroupM * n_tiles;
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mb, int& nb,
+                                            int group = kGroupM) {
+  const int per_group = group * n_tiles;
   const int g = t / per_group;
-  const int first_m = g * kGroupM;
-  const int gm = min(kGroupM, m_tiles - first_m);
+  const int first_m = g * group;
+  const int gm = min(group, m_tiles - first_m);
   const int local = t - g * per_group;
   nb = local / gm;
   mb = first_m + local % gm;

@@ -49,6 +49,9 @@ namespace gbf {
 
 constexpr int kQStages = 4;
 constexpr int kQStreams = 2;                   // MMA streams = M-tiles per stage
+// Raster group of M-tile pairs: the ~152 tiles in flight then span about 16
+// M-tiles x 9 N-tiles, whose A and B panels (K = 8192: 64 + 40 MB) stay in L2.
+constexpr int kQGroup = 8;
 constexpr int kQABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int kQThreads = 384;                 // warps 0-3 roles, 4-11 epilogue
 constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       griddep_wait();
       for (int t = pair; t < num_super && ok; t += npairs) {
         int mp, nb;
-        tile_coords(t, m_pairs, a.n_tiles, mp, nb);
+        tile_coords(t, m_pairs, a.n_tiles, mp, nb, kQGroup);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) {
             ok = false;
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int local = 0; pair + (local / kQStreams) * npairs < num_super; ++local) {
       const int st = local % kQStreams;
       int mp, nb;
-      tile_coords(pair + (local / kQStreams) * npairs, m_pairs, a.n_tiles, mp, nb);
+      tile_coords(pair + (local / kQStreams) * npairs, m_pairs, a.n_tiles, mp, nb, kQGroup);
       const int mb = 2 * mp + st;
       const uint32_t aph = (local / kQStreams) & 1;
       const int64_t row =
