@@ -111,21 +111,23 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
   mb = first_m + local % gm;
 }
 
-// Epilogue of one output column n for 16 consecutive rows m0..m0+15 (the
-// swapped kernels): the operands are fetched first (col16_prefetch, which can
+// Epilogue of one output column n for R consecutive rows m0..m0+R-1 (the
+// swapped kernels): the operands are fetched first (col_prefetch, which can
 // run before the accumulator is ready), then the math and the stores.
+template <int R = 16>
 struct ColLoads {
-  float c[16];
-  float r[16];
+  float c[R];
+  float r[R];
   float b;
 };
 
-__device__ __forceinline__ void col16_prefetch(ColLoads& L, int64_t m0, int n, int M, int N,
-                                               const EpiParams& e, uint64_t pol) {
+template <int R>
+__device__ __forceinline__ void col_prefetch(ColLoads<R>& L, int64_t m0, int n, int M, int N,
+                                             const EpiParams& e, uint64_t pol) {
   const bool nok = n < N;
   L.b = (nok && e.bias) ? __bfloat162float(e.bias[n]) : 0.0f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < R; ++j) {
     const int64_t m = m0 + j;
     const bool ok = nok && m < M;
     const int64_t off = m * N + n;
@@ -134,14 +136,13 @@ __device__ __forceinline__ void col16_prefetch(ColLoads& L, int64_t m0, int n, i
   }
 }
 
-template <int ACT>
-__device__ __forceinline__ void epi_col16(const float (&v)[16], const ColLoads& L, int64_t m0,
-                                          int n, int M, int N, const EpiParams& e,
-                                          uint64_t pol) {
+template <int ACT, int R>
+__device__ __forceinline__ void epi_col(const float (&v)[R], const ColLoads<R>& L, int64_t m0,
+                                        int n, int M, int N, const EpiParams& e, uint64_t pol) {
   if (n >= N) return;
   const float beta = e.C ? e.beta : 0.0f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < R; ++j) {
     const int64_t m = m0 + j;
     if (m < M)
       st_stream_u16(e.out + m * N + n,

@@ -300,6 +300,14 @@ struct SwapCfg {
   static constexpr int kCols = kProducts * kAcc * MPAD;
   static constexpr uint32_t kTmemCols = kCols <= 64 ? 64 : (kCols <= 128 ? 128 : 256);
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
+  // Split-K exchange by pushing (see the kernel's epilogue): the partial, as
+  // kQuads 4-row groups of every product, plus the largest receive area
+  // (S * ceil(kQuads / S) < kQuads + kMaxSplits groups) must fit in the
+  // stage memory; otherwise the ranks pull through distributed shared memory.
+  static constexpr int kQuads = MPAD / 4;
+  static constexpr int kQuadBytes = kProducts * 128 * 16;
+  static constexpr bool kPush =
+      (2 * kQuads + kMaxSplits) * kQuadBytes <= kStages * kStageBytes;
   static_assert(kCols <= 256, "TMEM budget of two CTAs per SM");
   static_assert(!DUAL || kSmem <= 113 * 1024, "two CTAs per SM");
   static_assert(kStages * kStageBytes >= kProducts * 128 * MPAD * 4, "reduction buffer must fit");
@@ -313,16 +321,16 @@ struct SwapArgs {
   KernelCtl ctl;
 };
 
-// GLU ending of one output column for 16 consecutive rows (swapped gate/up
+// GLU ending of one output column for R consecutive rows (swapped gate/up
 // GEMM): h = act(alpha*g) * (alpha*u) + beta*C.
-template <int ACT>
-__device__ __forceinline__ void epi_col16_glu(const float (&g)[16], const float (&u)[16],
-                                              const ColLoads& L, int64_t m0, int n, int M,
-                                              int N, const EpiParams& e, uint64_t pol) {
+template <int ACT, int R>
+__device__ __forceinline__ void epi_col_glu(const float (&g)[R], const float (&u)[R],
+                                            const ColLoads<R>& L, int64_t m0, int n, int M,
+                                            int N, const EpiParams& e, uint64_t pol) {
   if (n >= N) return;
   const float beta = e.C ? e.beta : 0.0f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < R; ++j) {
     const int64_t m = m0 + j;
     if (m < M)
       st_stream_u16(e.out + m * N + n,
@@ -345,7 +353,8 @@ __global__ void __launch_bounds__(256, 2)
   uint64_t* empty = full + Cfg::kStages;
   uint64_t* dfull = empty + Cfg::kStages;
   uint64_t* done = dfull + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* recvb = done + 1;  // split-K partials pushed here by the other ranks
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(recvb + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -364,6 +373,13 @@ __global__ void __launch_bounds__(256, 2)
     }
     mbar_init(dfull, kSwapIssuers);
     mbar_init(done, kSwapIssuers);
+    if (Cfg::kPush && S > 1) {
+      // expects the other S - 1 ranks' copies of this rank's 4-row groups
+      const int r = static_cast<int>(rank);
+      const int nq = ((r + 1) * Cfg::kQuads) / S - (r * Cfg::kQuads) / S;
+      mbar_init(recvb, 1);
+      mbar_arrive_expect_tx(recvb, static_cast<uint32_t>((S - 1) * nq * Cfg::kQuadBytes));
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -477,11 +493,14 @@ __global__ void __launch_bounds__(256, 2)
   }
 
   // ---- epilogue warps: partial sums, cluster reduction, ending
-  // With split-K every rank parks its fp32 partial in its own shared memory;
-  // after the cluster barrier the 16-row chunks of the output are shared out
-  // among the ranks (chunk c goes to rank c % S), and each chunk is summed
-  // over ranks 0..S-1 in that order (deterministic) through distributed
-  // shared memory.
+  // With split-K every rank parks its fp32 partial in its own shared memory.
+  // Push exchange (when it fits): the output rows are shared out among the
+  // ranks as 4-row groups, each rank copies every other rank's groups to
+  // that rank with one bulk copy, and each rank sums its own groups over
+  // ranks 0..S-1 in that order (deterministic) from local shared memory.
+  // Otherwise the 16-row chunks go to the ranks round-robin (chunk c to rank
+  // c % S) and each rank pulls the other partials of its chunks through
+  // distributed shared memory, again summing in rank order.
   const bool epi = warp >= 4;
   const int q = warp & 3;
   const int tid = threadIdx.x - 128;  // 0..127 for the epilogue warps = TMEM lane
@@ -491,83 +510,180 @@ __global__ void __launch_bounds__(256, 2)
   bool have = false;
   const uint64_t pol = l2_evict_first_policy();
   const int n = nb * kSwapBN + tid;
-  ColLoads L;
-  if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
-  if (epi && static_cast<int>(rank) < kChunks)  // this rank's first chunk: operands early
-    col16_prefetch(L, static_cast<int64_t>(mb) * MPAD + static_cast<int>(rank) * 16, n, a.M,
-                   a.N, a.ep, pol);
-  if (epi) {
-    have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
-    tc_fence_after();
+  bool pushed = false;
+  if constexpr (Cfg::kPush) {
     if (S > 1) {
+      pushed = true;
+      constexpr int kP = Cfg::kProducts;
+      const int r = static_cast<int>(rank);
+      const int qa = (r * Cfg::kQuads) / S;        // this rank's 4-row groups [qa, qb)
+      const int nq = ((r + 1) * Cfg::kQuads) / S - qa;
+      uint8_t* recv = stages + Cfg::kQuads * Cfg::kQuadBytes;  // [sender][group][product][lane]
+      ColLoads<4> L4;
+      if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
+      if (epi && nq > 0)
+        col_prefetch<4>(L4, static_cast<int64_t>(mb) * MPAD + 4 * qa, n, a.M, a.N, a.ep, pol);
+      if (epi) {
+        have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
+        tc_fence_after();
+        // park: red[(group * kP + product) * 128 + lane] = rows 4 group .. +3
 #pragma unroll 1
-      for (int c = 0; c < Cfg::kProducts * kChunks; ++c) {  // gate chunks, then up chunks
-        float r[16];
-        acc_sum16<Cfg::kAcc, MPAD>(tb + (c / kChunks) * Cfg::kAcc * MPAD + (c % kChunks) * 16,
-                                   r);
+        for (int c = 0; c < kP * kChunks; ++c) {
+          float v[16];
+          acc_sum16<Cfg::kAcc, MPAD>(tb + (c / kChunks) * Cfg::kAcc * MPAD + (c % kChunks) * 16,
+                                     v);
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          red[(c * 4 + v) * 128 + tid] = make_float4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          for (int w = 0; w < 4; ++w)
+            red[(((c % kChunks) * 4 + w) * kP + c / kChunks) * 128 + tid] =
+                make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+        }
+        fence_proxy_async_smem();  // the bulk copies read what these threads wrote
       }
-    }
-  }
-  if (S > 1) cluster_sync_all();
-  if (epi) {
+      cluster_sync_all();  // every rank parked, every receive barrier armed
+      if (threadIdx.x == 128) {
+        for (int i = 1; i < S; ++i) {
+          const int p = (r + i) % S;
+          const int pa = (p * Cfg::kQuads) / S;
+          const int pn = ((p + 1) * Cfg::kQuads) / S - pa;
+          if (pn > 0)
+            bulk_copy_to_peer(
+                mapa_shared(smem_u32(recv + r * pn * Cfg::kQuadBytes), static_cast<uint32_t>(p)),
+                smem_u32(stages + pa * Cfg::kQuadBytes), static_cast<uint32_t>(pn * Cfg::kQuadBytes),
+                mapa_shared(smem_u32(recvb), static_cast<uint32_t>(p)));
+        }
+      }
+      if (epi && nq > 0) {
+        wait_bar(recvb, 0, ctl, kSiteEpiAccFull);
+        const float4* in = reinterpret_cast<const float4*>(recv);
 #pragma unroll 1
-    for (int c = static_cast<int>(rank); c < kChunks; c += S) {
-      if (c != static_cast<int>(rank))
-        col16_prefetch(L, static_cast<int64_t>(mb) * MPAD + c * 16, n, a.M, a.N, a.ep, pol);
-      float v[Cfg::kProducts][16];
+        for (int g = qa; g < qa + nq; ++g) {
+          const int i = g - qa;
+          if (g != qa)
+            col_prefetch<4>(L4, static_cast<int64_t>(mb) * MPAD + 4 * g, n, a.M, a.N, a.ep, pol);
+          float v[kP][4];
 #pragma unroll
-      for (int pr = 0; pr < Cfg::kProducts; ++pr) {
-        if (S == 1) {
-          float r[16];
-          acc_sum16<Cfg::kAcc, MPAD>(tb + pr * Cfg::kAcc * MPAD + c * 16, r);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[pr][j] = have ? r[j] : 0.0f;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[pr][j] = 0.0f;
-          const int cc = pr * kChunks + c;
-          for (int p = 0; p < S; ++p) {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              float4 f;
-              if (p == static_cast<int>(rank)) {
-                f = red[(cc * 4 + w) * 128 + tid];
+          for (int pr = 0; pr < kP; ++pr) {
+            float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            for (int p = 0; p < S; ++p) {
+              const float4 f = p == r ? red[(g * kP + pr) * 128 + tid]
+                                      : in[((p * nq + i) * kP + pr) * 128 + tid];
+              if (p == 0) {
+                t = f;
               } else {
-                f = ld_dsmem_f4(mapa_shared(smem_u32(&red[(cc * 4 + w) * 128 + tid]),
-                                            static_cast<uint32_t>(p)));
+                t.x += f.x;
+                t.y += f.y;
+                t.z += f.z;
+                t.w += f.w;
               }
-              v[pr][4 * w] += f.x;
-              v[pr][4 * w + 1] += f.y;
-              v[pr][4 * w + 2] += f.z;
-              v[pr][4 * w + 3] += f.w;
+            }
+            v[pr][0] = t.x;
+            v[pr][1] = t.y;
+            v[pr][2] = t.z;
+            v[pr][3] = t.w;
+          }
+          const int64_t m0 = static_cast<int64_t>(mb) * MPAD + 4 * g;
+          if constexpr (DUAL) {
+            switch (a.ep.act) {
+              case kActRelu: epi_col_glu<kActRelu, 4>(v[0], v[kP - 1], L4, m0, n, a.M, a.N, a.ep, pol); break;
+              case kActSilu: epi_col_glu<kActSilu, 4>(v[0], v[kP - 1], L4, m0, n, a.M, a.N, a.ep, pol); break;
+              case kActGeluTanh:
+                epi_col_glu<kActGeluTanh, 4>(v[0], v[kP - 1], L4, m0, n, a.M, a.N, a.ep, pol);
+                break;
+              default: epi_col_glu<kActIdentity, 4>(v[0], v[kP - 1], L4, m0, n, a.M, a.N, a.ep, pol); break;
+            }
+          } else {
+            switch (a.ep.act) {
+              case kActRelu: epi_col<kActRelu, 4>(v[0], L4, m0, n, a.M, a.N, a.ep, pol); break;
+              case kActSilu: epi_col<kActSilu, 4>(v[0], L4, m0, n, a.M, a.N, a.ep, pol); break;
+              case kActGeluTanh: epi_col<kActGeluTanh, 4>(v[0], L4, m0, n, a.M, a.N, a.ep, pol); break;
+              default: epi_col<kActIdentity, 4>(v[0], L4, m0, n, a.M, a.N, a.ep, pol); break;
             }
           }
         }
       }
-      const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;
-      if constexpr (DUAL) {
-        switch (a.ep.act) {
-          case kActRelu: epi_col16_glu<kActRelu>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
-          case kActSilu: epi_col16_glu<kActSilu>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
-          case kActGeluTanh:
-            epi_col16_glu<kActGeluTanh>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol);
-            break;
-          default: epi_col16_glu<kActIdentity>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
-        }
-      } else {
-        switch (a.ep.act) {
-          case kActRelu: epi_col16<kActRelu>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
-          case kActSilu: epi_col16<kActSilu>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
-          case kActGeluTanh: epi_col16<kActGeluTanh>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
-          default: epi_col16<kActIdentity>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+      // no rank leaves while copies from or into its shared memory may be in flight
+      cluster_sync_all();
+    }
+  }
+  if (!pushed) {
+    ColLoads<16> L;
+    if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
+    if (epi && static_cast<int>(rank) < kChunks)  // this rank's first chunk: operands early
+      col_prefetch<16>(L, static_cast<int64_t>(mb) * MPAD + static_cast<int>(rank) * 16, n, a.M,
+                     a.N, a.ep, pol);
+    if (epi) {
+      have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
+      tc_fence_after();
+      if (!Cfg::kPush && S > 1) {  // (with the push exchange this path runs with S = 1 only)
+#pragma unroll 1
+        for (int c = 0; c < Cfg::kProducts * kChunks; ++c) {  // gate chunks, then up chunks
+          float r[16];
+          acc_sum16<Cfg::kAcc, MPAD>(tb + (c / kChunks) * Cfg::kAcc * MPAD + (c % kChunks) * 16,
+                                     r);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            red[(c * 4 + v) * 128 + tid] = make_float4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
         }
       }
     }
+    if (S > 1) cluster_sync_all();
+    if (epi) {
+#pragma unroll 1
+      for (int c = static_cast<int>(rank); c < kChunks; c += S) {
+        if (c != static_cast<int>(rank))
+          col_prefetch<16>(L, static_cast<int64_t>(mb) * MPAD + c * 16, n, a.M, a.N, a.ep, pol);
+        float v[Cfg::kProducts][16];
+#pragma unroll
+        for (int pr = 0; pr < Cfg::kProducts; ++pr) {
+          if (S == 1) {
+            float r[16];
+            acc_sum16<Cfg::kAcc, MPAD>(tb + pr * Cfg::kAcc * MPAD + c * 16, r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[pr][j] = have ? r[j] : 0.0f;
+          } else if constexpr (!Cfg::kPush) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[pr][j] = 0.0f;
+            const int cc = pr * kChunks + c;
+            for (int p = 0; p < S; ++p) {
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                float4 f;
+                if (p == static_cast<int>(rank)) {
+                  f = red[(cc * 4 + w) * 128 + tid];
+                } else {
+                  f = ld_dsmem_f4(mapa_shared(smem_u32(&red[(cc * 4 + w) * 128 + tid]),
+                                              static_cast<uint32_t>(p)));
+                }
+                v[pr][4 * w] += f.x;
+                v[pr][4 * w + 1] += f.y;
+                v[pr][4 * w + 2] += f.z;
+                v[pr][4 * w + 3] += f.w;
+              }
+            }
+          }
+        }
+        const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;
+        if constexpr (DUAL) {
+          switch (a.ep.act) {
+            case kActRelu: epi_col_glu<kActRelu, 16>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
+            case kActSilu: epi_col_glu<kActSilu, 16>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
+            case kActGeluTanh:
+              epi_col_glu<kActGeluTanh, 16>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol);
+              break;
+            default: epi_col_glu<kActIdentity, 16>(v[0], v[1], L, m0, n, a.M, a.N, a.ep, pol); break;
+          }
+        } else {
+          switch (a.ep.act) {
+            case kActRelu: epi_col<kActRelu, 16>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+            case kActSilu: epi_col<kActSilu, 16>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+            case kActGeluTanh: epi_col<kActGeluTanh, 16>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+            default: epi_col<kActIdentity, 16>(v[0], L, m0, n, a.M, a.N, a.ep, pol); break;
+          }
+        }
+      }
+    }
+    if (S > 1) cluster_sync_all();
   }
-  if (S > 1) cluster_sync_all();
 
   if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
   tc_fence_before();

@@ -280,6 +280,19 @@ __device__ __forceinline__ void cluster_sync_all() {
                    : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// the shared memory of another CTA of the cluster; the copy completes
+// `bytes` transactions on that CTA's mbarrier.  dst and mbar are
+// shared::cluster addresses (mapa_shared), src a shared::cta address.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   uint32_t r;

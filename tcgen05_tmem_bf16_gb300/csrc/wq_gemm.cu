@@ -99,6 +99,12 @@ struct W4Cfg {
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static_assert(kStages * kStageBytes >= 128 * kW4Regions * MPAD * 4, "reduction buffer");
   static_assert(kSmem <= 115 * 1024, "two CTAs per SM");
+  // Split-K exchange by pushing (see the kernel's epilogue): the partial
+  // (MPAD rows of 128 lanes x 4 regions, fp32) plus the largest receive area
+  // (S * ceil(MPAD / S) < MPAD + kMaxSplits rows) must fit in the stage
+  // memory; otherwise the ranks pull through distributed shared memory.
+  static constexpr int kRowPartBytes = 128 * kW4Regions * 4;
+  static constexpr bool kPush = (2 * MPAD + kMaxSplits) * kRowPartBytes <= kStages * kStageBytes;
 };
 
 struct W4Args {
@@ -291,6 +297,32 @@ __device__ __forceinline__ void epi_quad8(const float (&v)[kW4Regions][8], int64
   }
 }
 
+// Epilogue of output columns n..n+3 of one row m.
+template <int ACT>
+__device__ __forceinline__ void epi_quad1(const float4& v, int64_t m, int n, int M, int N,
+                                          const EpiParams& e) {
+  if (n >= N || m >= M) return;
+  const int64_t off = m * N + n;
+  const uint2 c = e.C ? *reinterpret_cast<const uint2*>(e.C + off) : make_uint2(0, 0);
+  const uint2 r = e.residual ? *reinterpret_cast<const uint2*>(e.residual + off)
+                             : make_uint2(0, 0);
+  float b[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (e.bias) {
+    const uint2 bb = *reinterpret_cast<const uint2*>(e.bias + n);
+    b[0] = bf16lo(bb.x); b[1] = bf16hi(bb.x); b[2] = bf16lo(bb.y); b[3] = bf16hi(bb.y);
+  }
+  const float beta = e.C ? e.beta : 0.0f;
+  const float acc[4] = {v.x, v.y, v.z, v.w};
+  const float cc[4] = {bf16lo(c.x), bf16hi(c.x), bf16lo(c.y), bf16hi(c.y)};
+  const float rr[4] = {bf16lo(r.x), bf16hi(r.x), bf16lo(r.y), bf16hi(r.y)};
+  float x[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    x[q] = act_apply<ACT>(fmaf(beta, cc[q], e.alpha * acc[q]) + b[q]) + rr[q];
+  *reinterpret_cast<uint2*>(e.out + off) =
+      make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+}
+
 template <int FMT, int MPAD>
 __global__ void __launch_bounds__(kW4Threads, 2)
     wq_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -308,7 +340,8 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   uint64_t* aempty = afull + 2;            // [2]: MMA -> transform group g
   uint64_t* dfull = aempty + 2;
   uint64_t* done = dfull + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* recvb = done + 1;  // split-K partials pushed here by the other ranks
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(recvb + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -331,6 +364,13 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     }
     mbar_init(dfull, Cfg::kIssuers);
     mbar_init(done, Cfg::kIssuers);
+    if (Cfg::kPush && S > 1) {
+      // expects the other S - 1 ranks' copies of this rank's rows
+      const int r = static_cast<int>(rank);
+      const int nrow = ((r + 1) * MPAD) / S - (r * MPAD) / S;
+      mbar_init(recvb, 1);
+      mbar_arrive_expect_tx(recvb, static_cast<uint32_t>((S - 1) * nrow * Cfg::kRowPartBytes));
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -555,9 +595,13 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   }
 
   // ---- epilogue: cluster reduction of the partial sums, then the ending.
-  // Every rank parks its partial in its own shared memory; 8-row chunks go
-  // to the (rank, group) workers round-robin and are summed over ranks
-  // 0..S-1 in that order through distributed shared memory.
+  // Every rank parks its partial in its own shared memory.  Push exchange
+  // (when it fits): the output rows are shared out among the ranks in
+  // contiguous ranges, each rank copies every other rank's rows to that rank
+  // with one bulk copy, and each rank sums its own rows over ranks 0..S-1 in
+  // that order (deterministic) from local shared memory.  Otherwise 8-row
+  // chunks go to the (rank, group) workers round-robin and are summed over
+  // ranks 0..S-1 in that order through distributed shared memory.
   const bool epi = warp >= 4;
   if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
   const int g = (warp - 4) >> 2;
@@ -567,10 +611,91 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   float4* red = reinterpret_cast<float4*>(stages);
   constexpr int kChunks = MPAD / 8;
   bool have = false;
+  bool pushed = false;
+  if constexpr (Cfg::kPush) {
+    if (S > 1) {
+      pushed = true;
+      const int r = static_cast<int>(rank);
+      const int ra = (r * MPAD) / S;  // this rank's rows [ra, ra + nrow)
+      const int nrow = ((r + 1) * MPAD) / S - ra;
+      uint8_t* recv = stages + MPAD * Cfg::kRowPartBytes;  // [sender][row][lane] float4
+      if (epi) {
+        have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
+        tc_fence_after();
+        // park red[m * 128 + lane] = the lane's four columns of row m; group g
+        // takes the 8-row chunks c = g, g + 2, ..., one region at a time
+        float* redf = reinterpret_cast<float*>(stages);
+#pragma unroll 1
+        for (int c = g; c < kChunks; c += 2) {
+#pragma unroll 1
+          for (int rg = 0; rg < kW4Regions; ++rg) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < Cfg::kSets; ++e) {
+              uint32_t u[8];
+              tmem_ld8(tb + (e * kW4Regions + rg) * MPAD + c * 8, u);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] += __uint_as_float(u[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) redf[((c * 8 + j) * 128 + tid) * 4 + rg] = v[j];
+          }
+        }
+        fence_proxy_async_smem();  // the bulk copies read what these threads wrote
+      }
+      cluster_sync_all();  // every rank parked, every receive barrier armed
+      if (threadIdx.x == 128) {
+        for (int i = 1; i < S; ++i) {
+          const int p = (r + i) % S;
+          const int pa = (p * MPAD) / S;
+          const int pn = ((p + 1) * MPAD) / S - pa;
+          if (pn > 0)
+            bulk_copy_to_peer(
+                mapa_shared(smem_u32(recv + r * pn * Cfg::kRowPartBytes), static_cast<uint32_t>(p)),
+                smem_u32(stages + pa * Cfg::kRowPartBytes),
+                static_cast<uint32_t>(pn * Cfg::kRowPartBytes),
+                mapa_shared(smem_u32(recvb), static_cast<uint32_t>(p)));
+        }
+      }
+      if (epi && nrow > 0) {
+        wait_bar(recvb, 0, ctl, kSiteEpiAccFull);
+        const float4* in = reinterpret_cast<const float4*>(recv);
+        const int n = nb * kW4BN + 4 * tid;
+#pragma unroll 1
+        for (int i = g; i < nrow; i += 2) {
+          float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int p = 0; p < S; ++p) {
+            const float4 f = p == r ? red[(ra + i) * 128 + tid] : in[(p * nrow + i) * 128 + tid];
+            if (p == 0) {
+              t = f;
+            } else {
+              t.x += f.x;
+              t.y += f.y;
+              t.z += f.z;
+              t.w += f.w;
+            }
+          }
+          const int64_t row = static_cast<int64_t>(mb) * MPAD + ra + i;
+          switch (a.ep.act) {
+            case kActRelu: epi_quad1<kActRelu>(t, row, n, a.M, a.N, a.ep); break;
+            case kActSilu: epi_quad1<kActSilu>(t, row, n, a.M, a.N, a.ep); break;
+            case kActGeluTanh: epi_quad1<kActGeluTanh>(t, row, n, a.M, a.N, a.ep); break;
+            default: epi_quad1<kActIdentity>(t, row, n, a.M, a.N, a.ep); break;
+          }
+        }
+      }
+      // no rank leaves while copies from or into its shared memory may be in flight
+      cluster_sync_all();
+    }
+  }
+  if (!pushed) {
   if (epi) {
     have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
     tc_fence_after();
-    if (S > 1 && g == 0) {
+    if (!Cfg::kPush && S > 1 && g == 0) {  // (with the push exchange: S = 1 here)
 #pragma unroll 1
       for (int r = 0; r < kW4Regions; ++r) {
 #pragma unroll 1
@@ -615,7 +740,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
             for (int j = 0; j < 8; ++j) v[r][j] += have ? __uint_as_float(u[j]) : 0.0f;
           }
         }
-      } else {
+      } else if constexpr (!Cfg::kPush) {
 #pragma unroll
         for (int r = 0; r < kW4Regions; ++r)
 #pragma unroll
@@ -648,6 +773,7 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     }
   }
   if (S > 1) cluster_sync_all();
+  }
 
   if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
   tc_fence_before();
