@@ -327,12 +327,20 @@ GBF_API gbf_status_t gbf_debug_set_profile(void *counters, size_t bytes);
  * result beyond the order of the fp32 partial sums. */
 GBF_API gbf_status_t gbf_debug_force_splits(int splits);
 
+/* Tuning hook: for the dense product (and the gate/up GEMM) at M above the
+ * swapped kernel's range, run the persistent kernel (1) or the CTA-pair
+ * kernel (4) for later launches instead of the automatic choice (0, the
+ * default).  Other values return GBF_ERR_INVALID_ARG.  Changes which kernel
+ * computes the result, not the result beyond the order of rounding. */
+GBF_API gbf_status_t gbf_debug_force_path(int path);
+
 /* Which kernel family a call with these arguments runs (for tests and the
  * benchmark's roofline attribution).  op: GBF_OP_GEMM_EPILOGUE,
  * GBF_OP_SWIGLU, GBF_OP_W4A16, GBF_OP_W8A16_FP8 or GBF_OP_W4A16_NVFP4.
  * Returns 1 = persistent 128x256-tile kernel, 2 = small-M swapped kernel
  * with cluster split-K (also the gate/up GEMM at M <= 32), 3 = weight-only
- * kernel (int4, FP8, NVFP4), 4 = persistent kernel on CTA pairs (M >= 512),
+ * kernel (int4, FP8, NVFP4), 4 = persistent kernel on CTA pairs (chosen over 1
+ * when its 512-row units fill the GPU better),
  * 0 = no launch (empty output), -1 = the arguments would be rejected.
  * `*splits` (may be NULL) receives the split-K cluster size.
  *

@@ -35,7 +35,7 @@ EXPORTS = ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unf
            "swiglu_dual_gemm_unfused", "w4a16_gemm_unfused", "gbf_workspace_size",
            "gbf_check_device_error", "gbf_status_string", "gbf_set_wait_timeout_ns",
            "gbf_debug_inject_timeout", "gbf_kernel_path", "gbf_version",
-           "gemm_epilogue_unfused_noalloc", "gbf_debug_force_splits", "gbf_debug_set_profile",
+           "gemm_epilogue_unfused_noalloc", "gbf_debug_force_splits", "gbf_debug_force_path", "gbf_debug_set_profile",
            "swiglu_pointwise", "add_rmsnorm", "add_rmsnorm_unfused", "mlp_swiglu_down",
            "mlp_swiglu_down_unfused", "w8a16_fp8_gemm", "w8a16_fp8_gemm_unfused",
            "w4a16_nvfp4_gemm", "w4a16_nvfp4_gemm_unfused")
@@ -107,6 +107,8 @@ def load(path: str | None = None):
         lib.gbf_debug_set_profile.restype = I
         lib.gbf_debug_force_splits.argtypes = [I]
         lib.gbf_debug_force_splits.restype = I
+        lib.gbf_debug_force_path.argtypes = [I]
+        lib.gbf_debug_force_path.restype = I
         lib.gbf_kernel_path.argtypes = [I, I64, I64, I64, I, ctypes.POINTER(I)]
         lib.gbf_kernel_path.restype = I
         lib.gbf_version.argtypes = []
@@ -312,6 +314,13 @@ def gbf_debug_set_profile(counters, nbytes: int = 0) -> int:
 
 def gbf_debug_force_splits(splits: int) -> int:
     return int(load().gbf_debug_force_splits(int(splits)))
+
+
+def gbf_debug_force_path(path) -> int:
+    """Force the dense kernel above the swapped range: "persistent", "pair",
+    or None / "auto" for the automatic choice."""
+    code = {None: 0, "auto": 0, "persistent": 1, "pair": 4}.get(path, path)
+    return int(load().gbf_debug_force_path(int(code)))
 
 
 def gbf_kernel_path(op, M, N, K, b_layout="nk"):

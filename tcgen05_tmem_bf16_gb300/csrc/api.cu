@@ -25,6 +25,7 @@ namespace {
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_inject{0};
 std::atomic<int> g_force_splits{0};
+std::atomic<int> g_force_path{0};
 std::atomic<unsigned long long*> g_prof{nullptr};
 std::atomic<size_t> g_prof_bytes{0};
 
@@ -246,43 +247,86 @@ gbf_status_t check_nvfp4(int64_t M, int64_t N, int64_t K, int act) {
 
 }  // namespace
 
+namespace {
+
+// The CTA-pair kernel: pairs of 256-row M-tiles share each B tile (a unit of
+// 512 x bn per pair of SMs), persistent over the units.
+GemmPlan pair_plan(int64_t M, int64_t N, bool dual, bool kn, const DeviceInfo& dev) {
+  GemmPlan p;
+  p.path = kPathPair;
+  p.m_tiles = ceil_div(M, 2 * kBM);
+  p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
+  p.bn = 256;
+  if (!dual && !kn) {
+    // A 224-wide tile when it wastes less of the last round of tiles:
+    // compare useful area / (rounds * pairs * tile area).
+    // (a pair computes two M-tiles at a time: 512 x bn per round)
+    auto eff = [&](int bn) {
+      const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * ceil_div(N, bn);
+      const int64_t rounds = (tiles + dev.pairs - 1) / dev.pairs;
+      return static_cast<double>(M) * N / (static_cast<double>(rounds) * dev.pairs * 512 * bn);
+    };
+    if (eff(224) > eff(256) * 1.02) {
+      p.bn = 224;
+      p.n_tiles = ceil_div(N, 224);
+    }
+  }
+  p.grid = 2 * std::min(((p.m_tiles + 1) / 2) * p.n_tiles, dev.pairs);
+  return p;
+}
+
+// The one-SM persistent kernel: 128 x 256 tiles (128 x 128 of each product
+// for the gate/up GEMM).
+GemmPlan persistent_plan(int64_t M, int64_t N, bool dual, const DeviceInfo& dev) {
+  GemmPlan p;
+  p.path = kPathPersistent;
+  p.m_tiles = ceil_div(M, kBM);
+  p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
+  p.grid = std::min(p.m_tiles * p.n_tiles, std::max(1, dev.sms));
+  return p;
+}
+
+// Relative time of a plan: rounds of units times the MMA area of a unit per
+// SM, over the rate of one SM.  A pair unit is 512 x bn on two SMs; a
+// persistent tile 128 x 256 on one SM, whose single MMA stream runs at
+// about 0.8 of the rate of the pair kernel's two streams (measured: ~8.7
+// against ~11 TFLOP/s per SM).
+double plan_time(const GemmPlan& p, bool dual, const DeviceInfo& dev) {
+  if (p.path == kPathPair) {
+    const int64_t units = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+    const int64_t rounds = (units + dev.pairs - 1) / dev.pairs;
+    return static_cast<double>(rounds) * 512.0 * (dual ? 256 : p.bn) / 2.0;
+  }
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  const int64_t rounds = (tiles + std::max(1, dev.sms) - 1) / std::max(1, dev.sms);
+  return static_cast<double>(rounds) * 128.0 * 256.0 / 0.8;
+}
+
+}  // namespace
+
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const DeviceInfo& dev) {
   GemmPlan p;
   if (M == 0 || N == 0 || K == 0) return p;
-  p.num_kb = ceil_div(K, kBK);
   if (M <= (dual ? kSwapDualMaxM : 128)) {
+    p.num_kb = ceil_div(K, kBK);
     p.path = kPathSwap;
     p.mpad = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
     p.m_tiles = 1;
     p.n_tiles = ceil_div(N, kSwapBN);
     p.splits = choose_splits(p.n_tiles, p.num_kb, dev);
-  } else if (M >= kPairMinM && dev.pairs > 0) {
-    p.path = kPathPair;
-    p.m_tiles = ceil_div(M, 2 * kBM);
-    p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
-    p.bn = 256;
-    if (!dual && !kn) {
-      // A 224-wide tile when it wastes less of the last round of tiles:
-      // compare useful area / (rounds * pairs * tile area).
-      // (a pair computes two M-tiles at a time: 512 x bn per round)
-      auto eff = [&](int bn) {
-        const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * ceil_div(N, bn);
-        const int64_t rounds = (tiles + dev.pairs - 1) / dev.pairs;
-        return static_cast<double>(M) * N / (static_cast<double>(rounds) * dev.pairs * 512 * bn);
-      };
-      if (eff(224) > eff(256) * 1.02) {
-        p.bn = 224;
-        p.n_tiles = ceil_div(N, 224);
-      }
-    }
-    p.grid = 2 * std::min(((p.m_tiles + 1) / 2) * p.n_tiles, dev.pairs);
-  } else {
-    p.path = kPathPersistent;
-    p.m_tiles = ceil_div(M, kBM);
-    p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
-    p.grid = std::min(p.m_tiles * p.n_tiles, std::max(1, dev.sms));
+    return p;
   }
-  return p;
+  // Above the swapped kernel's range: the kernel with the shorter estimated
+  // time (the pair kernel's 512-row units leave most SMs idle when there are
+  // few of them), unless a tuning hook forces one.
+  const int force = g_force_path.load();
+  GemmPlan pp = persistent_plan(M, N, dual, dev);
+  pp.num_kb = ceil_div(K, kBK);
+  if (dev.pairs <= 0 || force == kPathPersistent) return pp;
+  GemmPlan qp = pair_plan(M, N, dual, kn, dev);
+  qp.num_kb = pp.num_kb;
+  if (force == kPathPair) return qp;
+  return plan_time(qp, dual, dev) < plan_time(pp, dual, dev) ? qp : pp;
 }
 
 GemmPlan plan_w4a16(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
@@ -710,6 +754,12 @@ gbf_status_t gbf_debug_set_profile(void* counters, size_t bytes) {
 gbf_status_t gbf_debug_force_splits(int splits) {
   if (splits < 0 || splits > kMaxSplits) return GBF_ERR_INVALID_ARG;
   g_force_splits.store(splits);
+  return GBF_OK;
+}
+
+gbf_status_t gbf_debug_force_path(int path) {
+  if (path != 0 && path != kPathPersistent && path != kPathPair) return GBF_ERR_INVALID_ARG;
+  g_force_path.store(path);
   return GBF_OK;
 }
 

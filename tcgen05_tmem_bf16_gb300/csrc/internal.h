@@ -113,6 +113,5 @@ constexpr int kSwapBN = 128;    // swapped kernel: output columns per tile (= MM
 constexpr int kSwapDualMaxM = 32;  // gate/up GEMM on the swapped kernel up to this M
 constexpr int kW4BN = 512;      // W4A16 kernel: output columns per tile
 constexpr int kMaxSplits = 8;   // portable cluster size limit
-constexpr int kPairMinM = 512;  // M from which the CTA-pair kernel is used
 
 }  // namespace gbf

@@ -64,6 +64,9 @@ def test_workspace_sizes(lib):
 def test_kernel_path_planning(lib):
     assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096) == ("pair", 1)
     assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096) == ("persistent", 1)
+    # mid-size M: the pair kernel's 512 x 256 units would leave most SMs idle
+    assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 4096) == ("persistent", 1)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 8192, 8192, "kn") == ("pair", 1)
     path, splits = gbf.gbf_kernel_path("gemm_epilogue", 16, 8192, 8192, "kn")
     assert path == "swap_splitk" and 1 <= splits <= 8
     assert gbf.gbf_kernel_path("swiglu", 2048, 14336, 4096)[0] == "pair"
@@ -116,3 +119,18 @@ def test_validation_errors_are_returned_before_any_launch(lib):
 def test_timeout_setting_is_clamped(lib):
     assert gbf.gbf_set_wait_timeout_ns(1) == 0
     assert gbf.gbf_set_wait_timeout_ns(2_000_000_000) == 0
+
+
+def test_force_path_hook(lib):
+    try:
+        assert gbf.gbf_debug_force_path("persistent") == 0
+        assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096)[0] == "persistent"
+        assert gbf.gbf_kernel_path("gemm_epilogue", 16, 4096, 4096)[0] == "swap_splitk"
+        assert gbf.gbf_debug_force_path("pair") == 0
+        assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096)[0] == "pair"
+        assert gbf.gbf_kernel_path("swiglu", 200, 14336, 4096)[0] == "pair"
+        assert gbf.gbf_debug_force_path(2) == 1  # GBF_ERR_INVALID_ARG
+        assert gbf.gbf_debug_force_path(7) == 1
+    finally:
+        gbf.gbf_debug_force_path(None)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096)[0] == "pair"

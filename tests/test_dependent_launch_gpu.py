@@ -38,17 +38,21 @@ def test_chain_of_swapped_gemms_reads_each_previous_output(cuda_lib):
 
 @pytest.mark.parametrize("layout", ["nk", "kn"])
 def test_chain_of_pair_gemms_reads_each_previous_output(cuda_lib, layout):
-    # M >= 512: the CTA-pair kernel, which also requests its first weight
-    # tiles before waiting for the previous kernel
+    # the CTA-pair kernel (forced: at this size the planner prefers the
+    # one-SM kernel)
     M, D, steps = 1024, 1024, 4
     ws = [rand_bf16(200 + i, (D, D), std=D ** -0.5) for i in range(steps)]
     x0 = rand_bf16(199, (M, D))
     xs = [up(x0)] + [poison_bf16(M, D) for _ in range(steps)]
     dws = [up(w) for w in ws]
-    for i in range(steps):
-        cuda_lib.gemm_epilogue(xs[i], dws[i], layout, None, None, xs[i], xs[i + 1], M, D, D)
+    assert cuda_lib.gbf_debug_force_path("pair") == 0
+    try:
+        assert cuda_lib.gbf_kernel_path("gemm_epilogue", M, D, D, layout)[0] == "pair"
+        for i in range(steps):
+            cuda_lib.gemm_epilogue(xs[i], dws[i], layout, None, None, xs[i], xs[i + 1], M, D, D)
+    finally:
+        cuda_lib.gbf_debug_force_path(None)
     assert cuda_lib.gbf_check_device_error() == 0
-    assert cuda_lib.gbf_kernel_path("gemm_epilogue", M, D, D, layout)[0] == "pair"
     for i in range(steps):
         xin = down(xs[i])
         want = oracle.gemm_epilogue(xin, ws[i], layout, residual=xin, M=M, N=D, K=D)

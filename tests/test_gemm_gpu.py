@@ -30,12 +30,19 @@ def case(M, N, K, layout, seed, c=True, bias=True, res=True):
 
 
 def run_and_check(gbf, M, N, K, layout, act, alpha, beta, seed, c=True, bias=True, res=True,
-                  expect_path=None):
+                  expect_path=None, force_path=None):
     A, B, C, bi, r = case(M, N, K, layout, seed, c, bias, res)
-    if expect_path:
-        assert gbf.gbf_kernel_path("gemm_epilogue", M, N, K, layout)[0] == expect_path
-    out = poison_bf16(M, N)
-    gbf.gemm_epilogue(up(A), up(B), layout, up(C), up(bi), up(r), out, M, N, K, alpha, beta, act)
+    if force_path:
+        assert gbf.gbf_debug_force_path(force_path) == 0
+    try:
+        if expect_path:
+            assert gbf.gbf_kernel_path("gemm_epilogue", M, N, K, layout)[0] == expect_path
+        out = poison_bf16(M, N)
+        gbf.gemm_epilogue(up(A), up(B), layout, up(C), up(bi), up(r), out, M, N, K, alpha, beta,
+                          act)
+    finally:
+        if force_path:
+            gbf.gbf_debug_force_path(None)
     assert gbf.gbf_check_device_error() == 0
     ref = oracle.gemm_epilogue(A, B, layout, C, bi, r, M=M, N=N, K=K, alpha=alpha, beta=beta,
                                act=act)
@@ -63,18 +70,26 @@ def test_small_m_swapped_kernel(cuda_lib, layout, M):
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("M,N,K", [(129, 136, 72), (300, 520, 1000), (256, 512, 64),
-                                   (511, 264, 128)])
+                                   (511, 264, 128), (1030, 1048, 136)])
 def test_persistent_kernel(cuda_lib, layout, M, N, K):
     run_and_check(cuda_lib, M, N, K, layout, "silu", 0.5, 1.5, seed=M + N + K,
-                  expect_path="persistent")
+                  expect_path="persistent", force_path="persistent")
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("M,N,K", [(512, 256, 64), (515, 264, 256), (1030, 1048, 136),
-                                   (777, 520, 328), (2048, 1024, 512)])
+                                   (777, 520, 328), (2048, 1024, 512), (129, 264, 128),
+                                   (300, 520, 200), (400, 1048, 136)])
 def test_cta_pair_kernel(cuda_lib, layout, M, N, K):
     run_and_check(cuda_lib, M, N, K, layout, "gelu_tanh", 0.75, -0.25, seed=M + 3 * N + K,
-                  expect_path="pair")
+                  expect_path="pair", force_path="pair")
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 4096, 256), (768, 2048, 192), (1024, 8192, 128),
+                                   (3000, 1024, 64)])
+def test_automatic_kernel_choice(cuda_lib, M, N, K):
+    # whichever of the two kernels the planner picks for mid-size M
+    run_and_check(cuda_lib, M, N, K, "nk", "relu", 1.25, 0.5, seed=M + N)
 
 
 @pytest.mark.parametrize("act", ["identity", "relu", "silu", "gelu_tanh"])
