@@ -32,6 +32,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -81,18 +82,25 @@ KERNEL_SOURCE = {"gemm_pair_kernel": "gemm_pair.cu", "gemm_persistent_kernel": "
                  "add_rmsnorm_kernel": "rmsnorm.cu", "swiglu_pointwise_kernel": "pointwise.cu"}
 
 
+def _code_only(src: str) -> str:
+    """C++/CUDA source without its comments (the sources hold no comment
+    markers inside string literals)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.sub(r"//[^\n]*", "", src)
+
+
 def kernel_source_sha(kernel: str) -> str:
-    """Hash of the sources a kernel is built from: its own .cu file, the
-    shared headers and the launch planner."""
+    """Hash of the code a kernel is built from (comments left out): its own
+    .cu file, the shared headers and the launch planner."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tcgen05_tmem_bf16_gb300", "csrc")
     own = KERNEL_SOURCE.get(kernel)
     for name in sorted(os.listdir(csrc)):
         if name.endswith(".cu") and name not in (own, "api.cu"):
             continue
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
