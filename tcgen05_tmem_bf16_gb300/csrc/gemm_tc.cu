@@ -9,7 +9,9 @@
 // Thinking", Pattern 2, level 2).
 //
 // Two kernels:
-//  * gemm_persistent_kernel -- large M.  One CTA per SM walks output tiles
+//  * gemm_persistent_kernel -- mid-size M (the planner picks it over the
+//    CTA-pair kernel of gemm_pair.cu when it fills the SMs better).  One CTA
+//    per SM walks output tiles
 //    of 128 x 256 (dual: 128 x 128 from a 256-wide stacked [gate; up] B
 //    tile).  Warp 0 issues TMA loads into a 4-stage shared-memory ring, warp 1
 //    issues tcgen05.mma into one of two 256-column TMEM accumulators, warps
@@ -18,9 +20,11 @@
 //  * gemm_swap_kernel -- small M (<= 128).  Computes out^T = W~^T * A^T so
 //    that the weight tile fills the 128-row MMA and the few rows of A become
 //    the MMA's N (16..128).  The K range is split across the CTAs of a thread
-//    block cluster; partial accumulators are summed in rank order through
-//    distributed shared memory by the cluster's rank-0 CTA, which then
-//    applies the ending.  No global scratch memory is used.
+//    block cluster; the output rows are shared out among the ranks, each
+//    rank receives the other ranks' partial sums of its rows in its shared
+//    memory (bulk copies; for M = 128 it loads them through distributed
+//    shared memory), sums them in rank order and applies the ending.  No
+//    global scratch memory is used.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

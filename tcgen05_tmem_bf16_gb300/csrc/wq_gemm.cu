@@ -52,8 +52,11 @@
 // 2^126 restores the value, a second multiplies by the scale (exact for
 // NVFP4: at most 6 significant bits; the one rounding for FP8).
 //
-// K is split across a thread-block cluster; partial sums meet through
-// distributed shared memory and the ending is applied once.
+// K is split across a thread-block cluster; the ranks exchange partial sums
+// through shared memory (each rank gets the other ranks' partials of its own
+// output rows by bulk copy, or loads them through distributed shared memory
+// for the larger tile of M > 16), sum them in rank order and apply the
+// ending once.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
