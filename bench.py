@@ -83,10 +83,12 @@ KERNEL_SOURCE = {"gemm_pair_kernel": "gemm_pair.cu", "gemm_persistent_kernel": "
 
 
 def _code_only(src: str) -> str:
-    """C++/CUDA source without its comments (the sources hold no comment
-    markers inside string literals)."""
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return re.sub(r"//[^\n]*", "", src)
+    """C++/CUDA source without its comments and with every run of white
+    space reduced to one blank (the sources hold no comment markers inside
+    string literals)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return re.sub(r"\s+", " ", src).strip()
 
 
 def kernel_source_sha(kernel: str) -> str:
