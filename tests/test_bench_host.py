@@ -79,3 +79,30 @@ def test_aggregate_over_two_gloo_ranks():
 
 def test_single_rank_aggregate_is_identity():
     assert bench.aggregate(1.5, 7.0, 1) == (1.5, 7.0)
+
+
+def test_source_hash_covers_code_not_comments(tmp_path, monkeypatch):
+    # the hash that keys recorded DRAM traffic changes with the code of a
+    # kernel's sources, not with their comments or layout
+    a = "int f(int x) {  // the input\n  /* doubled */ return 2 * x;\n}\n"
+    b = "// a header comment\nint f(int x) {\n  return 2 * x;  /* still doubled,\n  over two lines */\n}\n"
+    c = "int f(int x) { return 3 * x; }\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    csrc = tmp_path / "tcgen05_tmem_bf16_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "api.cu").write_text("int plan();\n")
+    (csrc / "common.cuh").write_text("// helpers\n")
+    (csrc / "wq_gemm.cu").write_text(a)
+    (csrc / "gemm_tc.cu").write_text("int g();\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_sha("wq_gemm_kernel")
+    (csrc / "wq_gemm.cu").write_text(b)
+    assert bench.kernel_source_sha("wq_gemm_kernel") == h0
+    (csrc / "gemm_tc.cu").write_text("int g2();\n")  # another kernel's file
+    assert bench.kernel_source_sha("wq_gemm_kernel") == h0
+    (csrc / "wq_gemm.cu").write_text(c)
+    assert bench.kernel_source_sha("wq_gemm_kernel") != h0
+    (csrc / "wq_gemm.cu").write_text(a)
+    (csrc / "common.cuh").write_text("// helpers\nint h();\n")  # a shared header
+    assert bench.kernel_source_sha("wq_gemm_kernel") != h0
