@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(256, 2)
       pushed = true;
       constexpr int kP = Cfg::kProducts;
       const int r = static_cast<int>(rank);
-      const int qa = (r * Cfg::kQuads) / S;        // this rank's 4-row groups [qa, qb)
+      const int qa = (r * Cfg::kQuads) / S;  // this rank's 4-row groups [qa, qa + nq)
       const int nq = ((r + 1) * Cfg::kQuads) / S - qa;
       uint8_t* recv = stages + Cfg::kQuads * Cfg::kQuadBytes;  // [sender][group][product][lane]
       ColLoads<4> L4;
