@@ -134,3 +134,23 @@ def test_force_path_hook(lib):
     finally:
         gbf.gbf_debug_force_path(None)
     assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096)[0] == "pair"
+
+
+@pytest.mark.parametrize("op,M,N,K,layout,want", [
+    # measured on a GB300 with both kernels forced (TFLOP/s pair / one-SM):
+    ("gemm_epilogue", 512, 4096, 4096, "nk", "persistent"),    # 414 / 644
+    ("gemm_epilogue", 1024, 4096, 4096, "nk", "persistent"),   # 812 / 1112
+    ("gemm_epilogue", 1536, 4096, 4096, "nk", "pair"),         # 1203 / 956
+    ("gemm_epilogue", 4096, 4096, 4096, "nk", "pair"),         # 1595 / 1354
+    ("gemm_epilogue", 512, 8192, 8192, "kn", "persistent"),    # 843 / 1267
+    ("gemm_epilogue", 768, 8192, 8192, "kn", "pair"),          # 1235 / 1057
+    ("gemm_epilogue", 1536, 8192, 8192, "kn", "persistent"),   # 1258 / 1438
+    ("gemm_epilogue", 3072, 8192, 8192, "kn", "pair"),         # 1648 / 1447
+    ("gemm_epilogue", 384, 14336, 4096, "nk", "pair"),         # 929 / 709
+    ("gemm_epilogue", 640, 14336, 4096, "nk", "persistent"),   # 814 / 1262
+    ("gemm_epilogue", 4096, 14336, 4096, "nk", "pair"),        # 1633 / 1489
+    ("swiglu", 512, 14336, 4096, "nk", "persistent"),          # 1347 / 1456
+    ("swiglu", 1024, 14336, 4096, "nk", "pair"),               # 1790 / 1581
+])
+def test_planner_picks_the_measured_faster_kernel(lib, op, M, N, K, layout, want):
+    assert gbf.gbf_kernel_path(op, M, N, K, layout)[0] == want
