@@ -277,11 +277,13 @@ GBF_API gbf_status_t w4a16_nvfp4_gemm_unfused(const void *A, const uint8_t *Wq,
  *   to hand over a workspace.  The bf16 intermediate lives in a scratch
  *   array built into the library instead.  The pages have no counterpart to
  *   this entry point; it exists for such callers only.
- *   Limit: M*N <= 4194304 elements (an 8 MiB array that every GPU loading
- *   the library holds until the process exits); larger sizes return
- *   GBF_ERR_WORKSPACE before anything is launched.  The first call on a
- *   device looks up the array's device address, so make it before any
- *   stream capture.  Every call shares the one array: calls whose work
+ *   Arguments are checked as gemm_epilogue_unfused checks them (same status
+ *   codes); then sizes with M*N > 4194304 elements (the array holds 8 MiB,
+ *   and every GPU that loads the library holds it until the process exits)
+ *   return GBF_ERR_WORKSPACE before anything is launched.  The first call on
+ *   a device looks up the array's device address, so make it before any
+ *   stream capture; a failed lookup returns GBF_ERR_CUDA and is tried again
+ *   by the next call.  Every call shares the one array: calls whose work
  *   overlaps on the GPU race on it and must be serialised by the caller.
  *   Allocates nothing.  Other arguments and results as gemm_epilogue.
  */
@@ -307,32 +309,6 @@ GBF_API const char *gbf_status_string(gbf_status_t status);
  * 2e9 = 2 s; clamped to [1e6, 6e10]).  Applies to later launches. */
 GBF_API gbf_status_t gbf_set_wait_timeout_ns(uint64_t ns);
 
-/* Test hook: when `on` is non-zero, the next launches of the fused GEMM
- * kernels withhold one accumulator-ready signal so that the epilogue's
- * bounded wait runs out; the kernel then records GBF_ERR_TIMEOUT and exits
- * cleanly.  Off by default. */
-GBF_API gbf_status_t gbf_debug_inject_timeout(int on);
-
-/* Profiling hook: with a zeroed device buffer of `bytes` registered, each CTA
- * of later launches (if the buffer has room for 32 counters per CTA) adds,
- * per wait site i of its pipeline, the cycles spent waiting to counter 2i and
- * the number of waits to counter 2i+1, and its total cycles to counter 31
- * (unsigned 64-bit, CTA b at offset 32*b, b = linear block index).  NULL
- * turns it off (the default).  The caller owns and clears the buffer. */
-GBF_API gbf_status_t gbf_debug_set_profile(void *counters, size_t bytes);
-
-/* Tuning hook: the split-K cluster size of the swapped small-M and W4A16
- * kernels (1..8) for later launches, or 0 (default) for the automatic choice
- * (about two CTAs per SM).  Changes the partition of the work, not its
- * result beyond the order of the fp32 partial sums. */
-GBF_API gbf_status_t gbf_debug_force_splits(int splits);
-
-/* Tuning hook: for the dense product (and the gate/up GEMM) at M above the
- * swapped kernel's range, run the persistent kernel (1) or the CTA-pair
- * kernel (4) for later launches instead of the automatic choice (0, the
- * default).  Other values return GBF_ERR_INVALID_ARG.  Changes which kernel
- * computes the result, not the result beyond the order of rounding. */
-GBF_API gbf_status_t gbf_debug_force_path(int path);
 
 /* Which kernel family a call with these arguments runs (for tests and the
  * benchmark's roofline attribution).  op: GBF_OP_GEMM_EPILOGUE,

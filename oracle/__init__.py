@@ -2,8 +2,15 @@
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  It wraps ``gbf_oracle.c`` (plain C,
-single-threaded, fp64, one bf16 rounding at the end) through ctypes and
-shares no code with the CUDA library in ``tcgen05_tmem_bf16_gb300``.
+fp64, one bf16 rounding at the end) through ctypes and shares no code with
+the CUDA library in ``tcgen05_tmem_bf16_gb300``.
+
+The C file is built twice: single-threaded (the default) and with OpenMP,
+which shares the loop over output elements among the host's cores
+(``set_parallel(True)`` or ``with all_cores():``).  Each element is computed
+the same way by one thread in both builds, so their results are identical;
+the parallel build serves the all-cores timing and the full-output checks of
+the large workloads.
 
 bf16 tensors are passed as numpy ``uint16`` arrays holding the raw bits;
 packed int4 weights as ``uint8`` arrays (K x N/2, high nibble = even column).
@@ -35,35 +42,74 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gbf_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libgbf_oracle.so")
+_OMP_LIB_PATH = os.path.join(_BUILD, "libgbf_oracle_omp.so")
 
 ACT = {"identity": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
 LAYOUT = {"kn": 0, "nk": 1}
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}
+_parallel = False
+
+
+def _compile(path: str, extra) -> str:
+    if os.path.exists(path) and os.path.getmtime(path) >= os.path.getmtime(_SRC):
+        return path
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", *extra, "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+    return path
 
 
 def build(force: bool = False) -> str:
     """Compile gbf_oracle.c with gcc (no fast-math, no FMA contraction so
-    x86 and Arm hosts give the same fp64 results)."""
+    x86 and Arm hosts give the same fp64 results), once single-threaded and
+    once with OpenMP."""
     os.makedirs(_BUILD, exist_ok=True)
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-           "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    if force:
+        for p in (_LIB_PATH, _OMP_LIB_PATH):
+            if os.path.exists(p):
+                os.unlink(p)
+    _compile(_OMP_LIB_PATH, ["-fopenmp"])
+    return _compile(_LIB_PATH, [])
+
+
+def set_parallel(on: bool) -> bool:
+    """Use the OpenMP build (all host cores) for later calls; returns the
+    previous setting."""
+    global _parallel
+    prev, _parallel = _parallel, bool(on)
+    return prev
+
+
+class all_cores:
+    """``with all_cores(): ...`` runs the enclosed oracle calls on the OpenMP
+    build."""
+
+    def __enter__(self):
+        self._prev = set_parallel(True)
+        return self
+
+    def __exit__(self, *exc):
+        set_parallel(self._prev)
+        return False
+
+
+def threads() -> int:
+    """Threads the oracle calls use (the OpenMP build's count when it is on)."""
+    return int(_load().oracle_threads())
 
 
 def _load():
-    global _lib
+    key = "omp" if _parallel else "serial"
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
+        lib = _libs.get(key)
+        if lib is not None:
+            return lib
+        build()
+        lib = ctypes.CDLL(_OMP_LIB_PATH if _parallel else _LIB_PATH)
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         D = ctypes.c_double
@@ -100,7 +146,9 @@ def _load():
         lib.oracle_swiglu_pointwise.restype = I
         lib.oracle_add_rmsnorm.argtypes = [P, P, P, I64, I64, D, I, P, P]
         lib.oracle_add_rmsnorm.restype = I
-        _lib = lib
+        lib.oracle_threads.argtypes = []
+        lib.oracle_threads.restype = I
+        _libs[key] = lib
         return lib
 
 

@@ -1,5 +1,5 @@
 /*
- * gbf_oracle.c -- plain, slow, single-threaded fp64 CPU oracle for the fused
+ * gbf_oracle.c -- plain, slow fp64 CPU oracle for the fused
  * GEMM + epilogue path.  TEST INFRASTRUCTURE ONLY: it is used by tests/,
  * by the smoke check and by the CPU-baseline leg of the benchmark.  No
  * product code path links or calls it, and it shares no code, header or
@@ -54,6 +54,12 @@
  *   gelu_tanh(v) = 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))
  * (the tanh form of GELU; the pages name SiLU but define no GELU).
  *
+ * Threads: the same file is also built with OpenMP (a second library, for
+ * the all-cores timing and for the full-output checks of the large
+ * workloads).  Then the loop over output elements (or rows) is shared out
+ * among threads; each element is still computed by one thread with the same
+ * sequential fp64 sum in the same order, so both builds give identical bits.
+ *
  * Parity pins live in tests/test_oracle_pins.py.
  */
 #include <math.h>
@@ -64,6 +70,24 @@
 #ifndef M_PI
 #define M_PI 3.14159265358979323846
 #endif
+
+/* Independent iterations of an output loop (ignored without OpenMP). */
+#ifdef _OPENMP
+#include <omp.h>
+#define ORACLE_PARALLEL_FOR _Pragma("omp parallel for schedule(dynamic, 16)")
+#else
+#define ORACLE_PARALLEL_FOR
+#endif
+
+/* Threads of the OpenMP build (1 without OpenMP). */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 enum { ACT_IDENTITY = 0, ACT_RELU = 1, ACT_SILU = 2, ACT_GELU_TANH = 3 };
 enum { LAYOUT_KN = 0, LAYOUT_NK = 1 };
@@ -254,6 +278,19 @@ static void elem(const int64_t *idx_m, const int64_t *idx_n, int64_t N,
     }
 }
 
+/* 0 when every requested (m, n) lies inside the M x N output, -1 otherwise
+ * (checked before any work, so the element loops below never stop early). */
+static int elems_ok(const int64_t *idx_m, const int64_t *idx_n, int64_t M, int64_t N,
+                    int64_t count)
+{
+    if (!idx_m)
+        return count == M * N ? 0 : -1;
+    for (int64_t i = 0; i < count; ++i)
+        if (idx_m[i] < 0 || idx_m[i] >= M || idx_n[i] < 0 || idx_n[i] >= N)
+            return -1;
+    return 0;
+}
+
 static void emit(int64_t i, double v, uint16_t *out_bf16, double *out_f64)
 {
     if (out_bf16)
@@ -282,13 +319,12 @@ int oracle_gemm_epilogue(const uint16_t *A, const uint16_t *B, int layout,
 {
     if (M < 0 || N < 0 || K < 0 || (layout != LAYOUT_KN && layout != LAYOUT_NK))
         return -1;
-    if (!idx_m && count != M * N)
+    if (elems_ok(idx_m, idx_n, M, N, count) != 0)
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t i = 0; i < count; ++i) {
         int64_t m, n;
         elem(idx_m, idx_n, N, i, &m, &n);
-        if (m < 0 || m >= M || n < 0 || n >= N)
-            return -1;
         double acc = dot_ab(A, B, layout, N, K, m, n);
         if (unfused)
             acc = oracle_bf16_to_f64(oracle_bf16_from_f64(acc));
@@ -311,13 +347,12 @@ int oracle_swiglu(const uint16_t *x, const uint16_t *w_gate,
 {
     if (M < 0 || N < 0 || K < 0 || (layout != LAYOUT_KN && layout != LAYOUT_NK))
         return -1;
-    if (!idx_m && count != M * N)
+    if (elems_ok(idx_m, idx_n, M, N, count) != 0)
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t i = 0; i < count; ++i) {
         int64_t m, n;
         elem(idx_m, idx_n, N, i, &m, &n);
-        if (m < 0 || m >= M || n < 0 || n >= N)
-            return -1;
         double g = dot_ab(x, w_gate, layout, N, K, m, n);
         double u = dot_ab(x, w_up, layout, N, K, m, n);
         if (unfused) {
@@ -345,13 +380,12 @@ int oracle_w4a16(const uint16_t *A, const uint8_t *Wq, const uint16_t *scales,
 {
     if (M < 0 || N < 0 || K < 0 || G <= 0 || N % 2 != 0 || K % G != 0)
         return -1;
-    if (!idx_m && count != M * N)
+    if (elems_ok(idx_m, idx_n, M, N, count) != 0)
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t i = 0; i < count; ++i) {
         int64_t m, n;
         elem(idx_m, idx_n, N, i, &m, &n);
-        if (m < 0 || m >= M || n < 0 || n >= N)
-            return -1;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k)
             acc += oracle_bf16_to_f64(A[m * K + k]) * w4_at(Wq, scales, G, N, k, n);
@@ -373,13 +407,12 @@ int oracle_wq_gemm(int kind, const uint16_t *A, const uint8_t *Wq, const void *s
 {
     if (M < 0 || !wq_args_ok(kind, G, N, K))
         return -1;
-    if (!idx_m && count != M * N)
+    if (elems_ok(idx_m, idx_n, M, N, count) != 0)
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t i = 0; i < count; ++i) {
         int64_t m, n;
         elem(idx_m, idx_n, N, i, &m, &n);
-        if (m < 0 || m >= M || n < 0 || n >= N)
-            return -1;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k)
             acc += oracle_bf16_to_f64(A[m * K + k]) * wq_at(kind, Wq, scales, G, N, k, n);
@@ -395,6 +428,7 @@ int oracle_wq_dequant(int kind, const uint8_t *Wq, const void *scales, int64_t G
 {
     if (!wq_args_ok(kind, G, N, K))
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t k = 0; k < K; ++k)
         for (int64_t n = 0; n < N; ++n)
             w_out[k * N + n] = oracle_bf16_from_f64(wq_at(kind, Wq, scales, G, N, k, n));
@@ -408,6 +442,7 @@ int oracle_dequant_int4(const uint8_t *Wq, const uint16_t *scales, int64_t G,
 {
     if (K < 0 || N < 0 || G <= 0 || N % 2 != 0 || K % G != 0)
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t k = 0; k < K; ++k)
         for (int64_t n = 0; n < N; ++n)
             w_out[k * N + n] = oracle_bf16_from_f64(w4_at(Wq, scales, G, N, k, n));
@@ -423,6 +458,7 @@ int oracle_pointwise_epilogue(const uint16_t *D, const uint16_t *C,
 {
     if (M < 0 || N < 0)
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n)
             out_bf16[m * N + n] = oracle_bf16_from_f64(
@@ -439,6 +475,7 @@ int oracle_swiglu_pointwise(const uint16_t *g, const uint16_t *u,
 {
     if (M < 0 || N < 0)
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n) {
             double h = oracle_act(act, alpha * oracle_bf16_to_f64(g[m * N + n])) *
@@ -461,6 +498,7 @@ int oracle_add_rmsnorm(const uint16_t *a, const uint16_t *x, const uint16_t *w, 
 {
     if (M < 0 || N <= 0 || eps < 0.0)
         return -1;
+    ORACLE_PARALLEL_FOR
     for (int64_t m = 0; m < M; ++m) {
         double ss = 0.0;
         for (int64_t j = 0; j < N; ++j) {

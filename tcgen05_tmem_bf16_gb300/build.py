@@ -33,7 +33,8 @@ def nvcc() -> str:
 
 def _inputs_mtime() -> float:
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    files += [os.path.join(ROOT, "include", "gbfuse.h"), os.path.abspath(__file__)]
+    files += [os.path.join(ROOT, "include", h) for h in ("gbfuse.h", "gbfuse_debug.h")]
+    files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 
 

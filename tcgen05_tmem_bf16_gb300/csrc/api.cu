@@ -1,4 +1,5 @@
-// api.cu -- the C ABI declared in include/gbfuse.h: argument validation,
+// api.cu -- the C ABI declared in include/gbfuse.h (and the test and tuning
+// hooks of include/gbfuse_debug.h): argument validation,
 // TMA tensor-map encoding, kernel-family selection by shape, launch, and
 // status codes.  Nothing here allocates device memory.
 #include <cuda.h>
@@ -13,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/gbfuse.h"
+#include "../../include/gbfuse_debug.h"
 #include "internal.h"
 
 namespace gbf {
@@ -32,70 +34,126 @@ std::atomic<size_t> g_prof_bytes{0};
 constexpr int kMaxDevices = 64;
 
 struct DevState {
-  std::once_flag once;
+  std::mutex mu;
+  std::atomic<bool> ready{false};
   DeviceInfo info;
   unsigned* err = nullptr;
-  cudaError_t status = cudaSuccess;
 };
 DevState g_dev[kMaxDevices];
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
+std::mutex g_encode_mu;
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode{nullptr};
 
-// Current device, its properties and the address of its error word.
+// Current device, its properties and the address of its error word.  The
+// lookup is made once per device; only a successful one is kept, so a call
+// made before the device could answer (e.g. during a failed context set-up)
+// does not disable the library on that device: the next call tries again.
 gbf_status_t current_device(const DeviceInfo** info, unsigned** err) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return GBF_ERR_NO_DEVICE;
   DevState& d = g_dev[dev];
-  std::call_once(d.once, [&d, dev]() {
-    int sms = 0, major = 0, minor = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    if (e == cudaSuccess) {
+  if (!d.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(d.mu);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+      int sms = 0, major = 0, minor = 0;
       void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_gbf_error_word);
+      cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+      if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_gbf_error_word);
+      if (e != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();  // not sticky: leave no error behind for the caller
+        return GBF_ERR_CUDA;
+      }
       d.err = static_cast<unsigned*>(p);
+      d.info.sms = sms;
+      d.info.pairs = (major == 10 && minor == 3) ? max_active_pairs() : 0;
+      if (d.info.pairs <= 0) d.info.pairs = sms / 2;
+      d.info.cc_major = major;
+      d.info.cc_minor = minor;
+      d.ready.store(true, std::memory_order_release);
     }
-    d.info.sms = sms;
-    if (e == cudaSuccess && major == 10 && minor == 3) d.info.pairs = max_active_pairs();
-    if (d.info.pairs <= 0) d.info.pairs = sms / 2;
-    d.info.cc_major = major;
-    d.info.cc_minor = minor;
-    d.status = e;
-  });
-  if (d.status != cudaSuccess) return GBF_ERR_CUDA;
+  }
   if (d.info.cc_major != 10 || d.info.cc_minor != 3) return GBF_ERR_NO_DEVICE;
   *info = &d.info;
   *err = d.err;
   return GBF_OK;
 }
 
-bool encoder() {
-  std::call_once(g_encode_once, []() {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode != nullptr;
+// The driver's tensor-map encoder (looked up until a lookup succeeds).
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = g_encode.load(std::memory_order_acquire);
+  if (fn) return fn;
+  std::lock_guard<std::mutex> lock(g_encode_mu);
+  fn = g_encode.load(std::memory_order_relaxed);
+  if (fn) return fn;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && p) {
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    g_encode.store(fn, std::memory_order_release);
+  } else {
+    (void)cudaGetLastError();
+  }
+  return fn;
 }
 
 // Row-major 2-D tensor [outer][inner] with `row_bytes` between rows.
+//
+// Encoded maps are kept in a small per-thread cache keyed by every argument:
+// a descriptor is a pure function of them, and a model calls the same layer
+// shapes on the same buffers step after step, so an un-graphed call then
+// skips the host-side encode.
+struct TmapKey {
+  const void* base;
+  uint64_t inner, outer, row_bytes;
+  uint32_t box_inner, box_outer;
+  int dt, swz;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && row_bytes == o.row_bytes &&
+           box_inner == o.box_inner && box_outer == o.box_outer && dt == o.dt && swz == o.swz;
+  }
+};
+struct TmapEntry {
+  CUtensorMap map;
+  TmapKey key;
+  bool valid;
+};
+constexpr int kTmapCacheSize = 32;
+thread_local TmapEntry t_tmap_cache[kTmapCacheSize];
+thread_local int t_tmap_next = 0;
+
 bool tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner,
              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
              CUtensorMapSwizzle swz) {
-  if (!encoder()) return false;
+  const TmapKey key{base, inner, outer, row_bytes, box_inner, box_outer, static_cast<int>(dt),
+                    static_cast<int>(swz)};
+  for (int i = 0; i < kTmapCacheSize; ++i) {
+    const TmapEntry& e = t_tmap_cache[i];
+    if (e.valid && e.key == key) {
+      *m = e.map;
+      return true;
+    }
+  }
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
+  if (!encode) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  TmapEntry& slot = t_tmap_cache[t_tmap_next];
+  t_tmap_next = (t_tmap_next + 1) % kTmapCacheSize;
+  slot.map = *m;
+  slot.key = key;
+  slot.valid = true;
+  return true;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -303,6 +361,15 @@ double plan_time(const GemmPlan& p, bool dual, const DeviceInfo& dev) {
 }
 
 }  // namespace
+
+int check_gemm_call(const void* A, const void* B, int b_layout, const void* C, const void* bias,
+                    const void* residual, const void* out, int64_t M, int64_t N, int64_t K,
+                    int act) {
+  gbf_status_t st = check_common(M, N, K, act);
+  if (st != GBF_OK) return st;
+  if (b_layout != GBF_B_KN && b_layout != GBF_B_NK) return GBF_ERR_INVALID_ARG;
+  return check_ptrs({A, B, out}, {C, bias, residual});
+}
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const DeviceInfo& dev) {
   GemmPlan p;

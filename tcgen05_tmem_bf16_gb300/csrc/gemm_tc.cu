@@ -557,7 +557,10 @@ __global__ void __launch_bounds__(256, 2)
         }
       }
       if (epi && nq > 0) {
-        wait_bar(recvb, 0, ctl, kSiteEpiAccFull);
+        // Not cut short by the abort flag: every peer issues its copies after
+        // the cluster barrier above whatever its state, so this wait ends
+        // (bounded by the timeout) and the final barrier then follows them.
+        wait_bar(recvb, 0, ctl, kSiteEpiAccFull, /*honor_abort=*/false);
         const float4* in = reinterpret_cast<const float4*>(recv);
 #pragma unroll 1
         for (int g = qa; g < qa + nq; ++g) {

@@ -52,6 +52,13 @@ struct DeviceInfo {
   int cc_minor = 0;
 };
 
+// ---- argument checks (api.cu) -------------------------------------------------
+// The status gemm_epilogue / gemm_epilogue_unfused return for these arguments
+// before any workspace or device check (a GBF_* code; 0 = acceptable).
+int check_gemm_call(const void* A, const void* B, int b_layout, const void* C, const void* bias,
+                    const void* residual, const void* out, int64_t M, int64_t N, int64_t K,
+                    int act);
+
 // ---- planning (api.cu) -------------------------------------------------------
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const DeviceInfo& dev);
 GemmPlan plan_w4a16(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);

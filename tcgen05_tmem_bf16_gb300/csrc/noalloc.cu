@@ -14,7 +14,8 @@
 // process exits.  In host code its name is only a host-side stand-in, so the
 // device address is looked up with cudaGetSymbolAddress once per device, on
 // the first call made while that device is current; that first call should
-// therefore come before any stream capture.
+// therefore come before any stream capture.  A lookup that fails is not
+// remembered: the call returns GBF_ERR_CUDA and the next call tries again.
 //
 // All calls share the one array and it keeps the last call's contents.
 // Nothing in it has to start at zero: the GEMM writes every element of the
@@ -24,9 +25,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/gbfuse.h"
+#include "internal.h"
 
 namespace {
 
@@ -37,11 +40,26 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) __nv_bfloat16 g_noalloc_scratch[kNoAllocMaxElems];
 
 struct ScratchSlot {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t status = cudaSuccess;
+  std::mutex mu;
+  std::atomic<void*> ptr{nullptr};
 };
 ScratchSlot g_slots[kMaxDevices];
+
+// Device address of the scratch array on the current device (null on failure).
+void* scratch_address(int dev) {
+  ScratchSlot& slot = g_slots[dev];
+  void* p = slot.ptr.load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(slot.mu);
+  p = slot.ptr.load(std::memory_order_relaxed);
+  if (p) return p;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();  // not sticky: leave no error behind for the caller
+    return nullptr;
+  }
+  slot.ptr.store(p, std::memory_order_release);
+  return p;
+}
 
 }  // namespace
 
@@ -49,16 +67,16 @@ extern "C" gbf_status_t gemm_epilogue_unfused_noalloc(
     const void* A, const void* B, int b_layout, const void* C, const void* bias,
     const void* residual, void* out, int64_t M, int64_t N, int64_t K, float alpha, float beta,
     int act, gbf_stream_t stream) {
-  if (M < 0 || N < 0 || K < 0) return GBF_ERR_INVALID_ARG;
+  // the same argument checks, in the same order, as the workspace entry point;
+  // the size limit takes the place of its workspace check
+  const gbf_status_t st = gbf::check_gemm_call(A, B, b_layout, C, bias, residual, out, M, N, K, act);
+  if (st != GBF_OK) return st;
   if (M != 0 && N > kNoAllocMaxElems / M) return GBF_ERR_WORKSPACE;  // M*N beyond the array
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return GBF_ERR_NO_DEVICE;
-  ScratchSlot& slot = g_slots[dev];
-  std::call_once(slot.once, [&slot]() {
-    slot.status = cudaGetSymbolAddress(&slot.ptr, g_noalloc_scratch);
-  });
-  if (slot.status != cudaSuccess || slot.ptr == nullptr) return GBF_ERR_CUDA;
+  void* scratch = scratch_address(dev);
+  if (!scratch) return GBF_ERR_CUDA;
   return gemm_epilogue_unfused(A, B, b_layout, C, bias, residual, out, M, N, K, alpha, beta, act,
-                               slot.ptr, kNoAllocBytes, stream);
+                               scratch, kNoAllocBytes, stream);
 }

@@ -11,11 +11,13 @@ import tcgen05_tmem_bf16_gb300 as gbf
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gbfuse.h")
+DEBUG_HEADER = os.path.join(ROOT, "include", "gbfuse_debug.h")
 
 
-def declared_symbols():
-    text = open(HEADER).read()
-    text = text.split("#define GBF_API")[-1].split("\n", 1)[1]
+def declared_symbols(path=HEADER):
+    text = open(path).read()
+    if "#define GBF_API" in text:
+        text = text.split("#define GBF_API")[-1].split("\n", 1)[1]
     return sorted(set(re.findall(r"^GBF_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)))
 
 
@@ -32,13 +34,32 @@ def test_header_declares_the_boundary():
                  "swiglu_dual_gemm_unfused", "w4a16_gemm_unfused", "gbf_workspace_size",
                  "gbf_check_device_error", "gbf_status_string"):
         assert name in syms
-    assert set(syms) == set(gbf.EXPORTS)
+    hooks = declared_symbols(DEBUG_HEADER)
+    # the product boundary holds no test or tuning hook; the hooks live in
+    # their own header, and the binding names exactly the union of the two
+    assert not any(n.startswith("gbf_debug_") for n in syms)
+    assert hooks and all(n.startswith("gbf_debug_") for n in hooks)
+    assert not set(syms) & set(hooks)
+    assert set(syms) | set(hooks) == set(gbf.EXPORTS)
 
 
 def test_library_exports_every_declared_symbol(lib):
-    for name in declared_symbols():
+    for name in declared_symbols() + declared_symbols(DEBUG_HEADER):
         assert hasattr(lib, name), name
         assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_library_exports_nothing_undeclared(lib):
+    import subprocess
+    from tcgen05_tmem_bf16_gb300 import build
+    r = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("nm unavailable")
+    exported = {line.split()[-1] for line in r.stdout.splitlines()
+                if len(line.split()) == 3 and line.split()[1] == "T"}
+    ours = {n for n in exported if n.startswith(("gbf_", "gemm_", "swiglu_", "w4a16_",
+                                                  "w8a16_", "add_rmsnorm", "mlp_"))}
+    assert ours == set(declared_symbols()) | set(declared_symbols(DEBUG_HEADER))
 
 
 def test_status_strings_and_version(lib):

@@ -7,6 +7,11 @@ arithmetic, or an invariant.  A plausible mistake in the oracle (a dropped
 term, a wrong sign, a transposed operand, the other nibble order, a wrong
 group index, a wrong GELU constant, round-half-up) fails at least one of
 them.  CPU only.
+
+Every pin runs twice: against the single-threaded build of the oracle and
+against its OpenMP build (the same C file, the loop over output elements
+shared among threads), and the two builds are also compared bit for bit on
+the five workloads' shapes in miniature.
 """
 import json
 import math
@@ -20,6 +25,13 @@ import oracle
 from workloads import to_bf16_bits
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(autouse=True, params=["serial", "openmp"])
+def oracle_build(request):
+    prev = oracle.set_parallel(request.param == "openmp")
+    yield request.param
+    oracle.set_parallel(prev)
 
 
 def _golden(name):
@@ -577,3 +589,64 @@ def test_nvfp4_alpha_is_the_per_tensor_scale():
     vals = np.array([oracle.fp4_e2m1_to_f64(c) for c in range(16)])[codes]
     sv = np.array([oracle.fp8_e4m3_to_f64(c) for c in range(256)])[S].repeat(16, axis=0)
     assert np.array_equal(oracle.bf16_bits_to_f64(w), vals * sv)
+
+
+# ---------------------------------------------------------------- the two builds
+
+def _both(fn):
+    prev = oracle.set_parallel(False)
+    try:
+        a = fn()
+        oracle.set_parallel(True)
+        b = fn()
+    finally:
+        oracle.set_parallel(prev)
+    return a, b
+
+
+def test_openmp_build_runs_on_several_threads(oracle_build):
+    if oracle_build != "openmp":
+        pytest.skip("checked once")
+    prev = oracle.set_parallel(False)
+    try:
+        assert oracle.threads() == 1
+        with oracle.all_cores():
+            n = oracle.threads()
+    finally:
+        oracle.set_parallel(prev)
+    assert 1 <= n <= (os.cpu_count() or 1)
+    if (os.cpu_count() or 1) > 1 and "OMP_NUM_THREADS" not in os.environ:
+        assert n > 1
+
+
+@pytest.mark.parametrize("what", ["gemm", "gemm_unfused", "swiglu", "w4a16", "fp8", "nvfp4",
+                                  "rmsnorm"])
+def test_serial_and_openmp_builds_agree_bit_for_bit(oracle_build, what):
+    if oracle_build != "serial":
+        pytest.skip("checked once")
+    import workloads
+    if what.startswith("gemm"):
+        w = workloads.make("sweep", M=37, shape=dict(N=136, K=200))
+        fn = lambda: oracle.gemm_epilogue(w["A"], w["B"], "kn", w["C"], w["bias"], None,
+                                          M=37, N=136, K=200, alpha=w["alpha"], beta=w["beta"],
+                                          act=w["act"], unfused=what.endswith("unfused"),
+                                          want_f64=True)
+    elif what == "swiglu":
+        w = workloads.make("swiglu", shape=dict(M=19, N=72, K=96))
+        fn = lambda: oracle.swiglu(w["x"], w["w_gate"], w["w_up"], "nk", M=19, N=72, K=96,
+                                   want_f64=True)
+    elif what == "w4a16":
+        w = workloads.make("w4a16", shape=dict(M=5, N=96, K=256))
+        fn = lambda: oracle.w4a16(w["A"], w["Wq"], w["scales"], 128, M=5, N=96, K=256,
+                                  want_f64=True)
+    elif what in ("fp8", "nvfp4"):
+        name = "w8a16_fp8" if what == "fp8" else "w4a16_nvfp4"
+        w = workloads.make(name, shape=dict(M=3, N=64, K=128))
+        fn = lambda: oracle.wq_gemm(what, w["A"], w["Wq"], w["scales"], w["group"], M=3, N=64,
+                                    K=128, alpha=w["alpha"], want_f64=True)
+    else:
+        w = workloads.make("add_rmsnorm", shape=dict(M=9, N=64))
+        fn = lambda: oracle.add_rmsnorm(w["a"], w["x"], w["weight"], M=9, N=64, eps=w["eps"])
+    a, b = _both(fn)
+    for x, y in zip(a, b):
+        assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))

@@ -110,6 +110,10 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib, M):
     A = rand_bf16(31, (M, K))
     B = rand_bf16(32, (N, K), std=K ** -0.5)
     out = poison_bf16(M, N)
+    if M <= 128:
+        # the swapped kernel with a split-K exchange: an aborted rank must
+        # still wait for its peers' copies before it leaves
+        assert cuda_lib.gbf_kernel_path("gemm_epilogue", M, N, K, "nk")[1] > 1
     cuda_lib.gbf_set_wait_timeout_ns(20_000_000)  # 20 ms
     cuda_lib.gbf_debug_inject_timeout(True)
     try:
@@ -139,11 +143,11 @@ def test_stream_argument_is_honoured(cuda_lib):
 
 @pytest.mark.parametrize("M", [16, 32])
 def test_weight_only_kernel_timeout_is_reported_and_recoverable(cuda_lib, M):
-    # the weight-only kernel at M <= 16 issues its MMAs from the transform
-    # warps (group barriers), at M = 32 from one issuer warp; a withheld
-    # accumulator-ready signal must end in GBF_ERR_TIMEOUT on both, and the
-    # next call on the same context must be correct
+    # a withheld accumulator-ready signal must end in GBF_ERR_TIMEOUT, with
+    # the split-K exchange pushing partials (M = 16) or pulling them (M = 32),
+    # and the next call on the same context must be correct
     N, K, G = 1024, 1024, 128
+    assert cuda_lib.gbf_kernel_path("w4a16", M, N, K)[1] > 1
     w = workloads.make("w4a16", shape=dict(M=M, N=N, K=K, group=G))
     out = poison_bf16(M, N)
     cuda_lib.gbf_set_wait_timeout_ns(50_000_000)
