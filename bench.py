@@ -3,23 +3,30 @@
 
 One step = one pass of the hot path over one batch of synthetic input: a
 single fused call (TMA staging -> tcgen05 main loop -> fused epilogue ->
-one store).  Default workload: the prefill projection with a bias +
-residual ending, A[4096x4096] * W[4096x4096]^T + bias + residual, bf16 in,
-fp32 accumulate, bf16 out.  Other workloads (--workload) are the gate/up
-SwiGLU GEMM, the W4A16 decode GEMM, the epilogue sweep (sweep-<M>) and the
-tiny case.
+one store).  The default run (--workload all) measures every workload: the
+JSON line's headline (value, roofline, e2e, cpu_baseline) is the largest one,
+the epilogue sweep at M = 8192 (out = gelu_tanh(0.75*A*B + 0.25*C + bias),
+A[8192x8192], B[8192x8192], bf16 in, fp32 accumulate, bf16 out), and the key
+"configs" holds one record per other workload (the tiny case, the prefill
+projection, the gate/up SwiGLU GEMM, the W4A16 decode GEMM, the sweep at
+M = 1, 16, 128 and 1024, and the FP8 / NVFP4 weight-only GEMMs, fused
+add + RMSNorm, the level-1 SwiGLU ending and the MLP block at decode), each
+with its value, roofline fractions against both the tensor and the HBM peak,
+recorded DRAM traffic and fused-vs-unfused speedup.  --workload NAME runs one
+workload alone.
 
-Prints ONE JSON line.  ``value`` is whole-job TFLOP/s (FLOPs of every rank's
-steps / max over ranks of the timed region).  Inputs are resident in HBM;
-rotating input sets (>= 2x L2 in total) keep consecutive steps from reading
-each other's data out of L2.  CUDA events on the launching stream bracket the
-timed region; a step is one kernel launch, so region / steps is the kernel's
-average launch duration used for the roofline fraction.  Extra keys:
-roofline, cpu_baseline (the fp64 oracle timed on a bounded sample on the host
-cores), e2e (the same metric with host buffers and
-host<->device copies inside the timed region), clocks (nvidia-smi samples taken
-during the timed region), the unfused composition's time and the
-fused-vs-unfused speedup.
+Prints ONE JSON line.  ``value`` is whole-job throughput (the workload's
+metric: TFLOP/s when tensor-bound, GB/s of algorithmic bytes when HBM-bound,
+summed over ranks / max over ranks of the timed region).  Inputs are
+resident in HBM; rotating input sets (>= 2x L2 in total) keep consecutive
+steps from reading each other's data out of L2.  CUDA events on the launching
+stream bracket the timed region; a step is one kernel launch, so region /
+steps is the kernel's average launch duration used for the roofline
+fraction.  Extra keys: roofline, cpu_baseline (the fp64 oracle timed on a
+bounded sample on all host cores, with the single-threaded build beside it),
+e2e (the same metric with host buffers and host<->device copies inside the
+timed region), clocks (nvidia-smi samples taken during the timed region),
+the unfused composition's time and the fused-vs-unfused speedup.
 
 --impl reference times the fp64 CPU oracle (the only reference this path
 has) on the same workload, each step a bounded sample of output elements.
@@ -50,6 +57,11 @@ if ROOT not in sys.path:
 METRIC = "fused GEMM+epilogue TFLOP/s or GB/s as % of roofline; fused vs unfused speedup"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
+
+HEADLINE = "sweep-8192"
+SUB_WORKLOADS = ("tiny", "prefill", "swiglu", "w4a16", "sweep-1", "sweep-16", "sweep-128",
+                 "sweep-1024", "w8a16_fp8", "w4a16_nvfp4", "add_rmsnorm", "swiglu_pointwise",
+                 "mlp_decode")
 
 WORKLOAD_TEXT = {
     "add_rmsnorm": "fused residual add + RMSNorm, a,x[4096x4096] bf16, eps 1e-5",
@@ -227,8 +239,16 @@ def describe(w: dict) -> dict:
     return d
 
 
+def workload_text(name: str) -> str:
+    if name.startswith("sweep-"):
+        M = int(name.split("-")[1])
+        return (f"epilogue sweep M={M}: gelu_tanh(0.75*A*B + 0.25*C + bias), A[{M}x8192], "
+                f"B[8192x8192] (K x N), C[{M}x8192], bf16")
+    return WORKLOAD_TEXT.get(name, name)
+
+
 def config_of(name: str, w: dict, world: int) -> dict:
-    return {"workload": WORKLOAD_TEXT.get(name, name), "name": name, **describe(w),
+    return {"workload": workload_text(name), "name": name, **describe(w),
             "parallelism": f"replicas x{world}"}
 
 
@@ -539,27 +559,58 @@ def metric_per_element(w: dict):
     return c.fused_bytes * per / 1e9, "GB/s"
 
 
-def cpu_baseline(w: dict, seconds: float = 12.0) -> dict:
-    """The oracle as it stands (single-threaded C, fp64) on seeded output
-    elements of the same workload, for about `seconds` of CPU time."""
-    import numpy as np
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_sample(w: dict, seconds: float, parallel: bool):
+    """(output elements, seconds, threads) of the oracle on seeded positions
+    of the workload for about `seconds`."""
+    import oracle
     import workloads
-    rows, cols = workloads.sample_indices(w["M"], w["N"], 1 << 20, seed=0xBEEF)
-    pos, done, t0, batch = 0, 0, time.perf_counter(), 64
-    while True:
-        done += oracle_elements(w, rows[pos:pos + batch], cols[pos:pos + batch])
-        pos += batch
-        el = time.perf_counter() - t0
-        if el >= seconds or pos + batch > rows.size:
-            break
-        batch = min(batch * 2, 4096)
+    rows, cols = workloads.sample_indices(w["M"], w["N"], 1 << 21, seed=0xBEEF)
+    prev = oracle.set_parallel(parallel)
+    try:
+        threads = oracle.threads()
+        pos, done, t0, batch = 0, 0, time.perf_counter(), 64
+        cap = 4096 * max(1, threads)
+        while True:
+            done += oracle_elements(w, rows[pos:pos + batch], cols[pos:pos + batch])
+            pos += batch
+            el = time.perf_counter() - t0
+            if el >= seconds or pos + batch > rows.size:
+                break
+            batch = min(batch * 2, cap)
+    finally:
+        oracle.set_parallel(prev)
+    return done, el, threads
+
+
+def cpu_baseline(w: dict, seconds: float = 10.0) -> dict:
+    """The oracle as it stands (fp64 C) on seeded output elements of the same
+    workload, for about `seconds` each: the OpenMP build on all host cores
+    (the record's value) and the single-threaded build beside it."""
     per, unit = metric_per_element(w)
-    return {"value": done * per / el, "unit": unit, "cores": 1, "kind": "oracle",
-            "sample": f"{done} output elements of the "
-                      + (f"{w['M']}x{w['D']}x{w['F']}" if w["op"] == "mlp"
-                         else f"{w['M']}x{w['N']}x{w['K']}")
-                      + f" workload at seeded positions ({el:.1f} s, single-threaded fp64 C "
-                        f"oracle)"}
+    shape = (f"{w['M']}x{w['D']}x{w['F']}" if w["op"] == "mlp"
+             else f"{w['M']}x{w['N']}x{w['K']}")
+    n1, t1, _ = _oracle_sample(w, seconds, parallel=False)
+    nn, tn, threads = _oracle_sample(w, seconds, parallel=True)
+    return {"value": nn * per / tn, "unit": unit, "cores": threads, "kind": "oracle",
+            "cpu": cpu_model(), "host_cores": os.cpu_count(),
+            "sample": f"{nn} output elements of the {shape} workload at seeded positions "
+                      f"({tn:.1f} s, OpenMP build of the fp64 C oracle, {threads} threads)",
+            "single_thread": {"value": n1 * per / t1, "unit": unit, "cores": 1,
+                              "kind": "oracle",
+                              "sample": f"{n1} output elements, same positions ({t1:.1f} s, "
+                                        f"single-threaded build)"}}
 
 
 def run_reference(args, workload_name):
@@ -567,14 +618,20 @@ def run_reference(args, workload_name):
     computes a bounded sample of output elements."""
     import numpy as np
     import workloads
+    import oracle
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if workload_name == "all":
+        workload_name = HEADLINE
     w = (workloads.make("sweep", M=int(workload_name.split("-")[1]))
          if workload_name.startswith("sweep-") else workloads.make(workload_name))
-    rows, cols = workloads.sample_indices(w["M"], w["N"], 1 << 16, seed=0xFACE)
+    rows, cols = workloads.sample_indices(w["M"], w["N"], 1 << 20, seed=0xFACE)
+    oracle.set_parallel(True)  # the OpenMP build: every host core
+    threads = oracle.threads()
+    oracle_elements(w, rows[:threads], cols[:threads])  # thread pool start-up
     t0 = time.perf_counter()
-    n0 = oracle_elements(w, rows[:32], cols[:32])
+    n0 = oracle_elements(w, rows[:32 * threads], cols[:32 * threads])
     per_elem = max((time.perf_counter() - t0) / n0, 1e-9)
     budget = 90.0 / max(1, args.steps + args.warmup)
     per_step = int(max(1, min(rows.size // 2, budget / per_elem)))
@@ -601,14 +658,14 @@ def run_reference(args, workload_name):
     shape = (f"{w['M']}x{w['D']}x{w['F']}" if w["op"] == "mlp"
              else f"{w['M']}x{w['N']}x{w['K']}")
     sample = (f"{done // args.steps} output elements per step at seeded positions of the "
-              f"{shape} workload, single-threaded fp64 C oracle")
+              f"{shape} workload, fp64 C oracle (OpenMP build, {threads} threads)")
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
             "config": config_of(workload_name, w, max(1, args.gpus)),
-            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                             "cpu": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -678,20 +735,171 @@ def mlp_gate_up_kernel_time(wl, stream, steps: int):
 
 
 
+def measure(name: str, args, dev, stream, peaks, peak_src, world: int, headline: bool) -> dict:
+    """Time one workload: the fused call (value and roofline of its dominant
+    kernel), the unfused composition (speedup), and the end-to-end call with
+    host buffers.  Returns the workload's record; frees its device memory."""
+    import torch
+
+    import tcgen05_tmem_bf16_gb300 as gbf
+    from tcgen05_tmem_bf16_gb300 import roofline as rf
+
+    wl = Workload(name, dev)
+    # warm-up (also checks the launch works)
+    for i in range(args.warmup):
+        wl.fused(i)
+    torch.cuda.synchronize()
+    if wl.op == "mlp":
+        wl.capture()  # the block is replayed from CUDA graphs from here on
+        for i in range(args.warmup):
+            wl.fused(i)
+        torch.cuda.synchronize()
+    steps = args.steps
+    if steps is None:
+        t_cal, _ = time_loop(wl.fused, 20, stream, per_launch=False)
+        steps = int(min(50000, max(200, 1.5 / max(t_cal / 20, 1e-6))))
+        if world > 1:
+            import torch.distributed as dist
+            k = torch.tensor([steps], dtype=torch.int64, device=dev)
+            dist.all_reduce(k, op=dist.ReduceOp.MIN)
+            steps = int(k.item())
+    if gbf.gbf_check_device_error() != 0:
+        raise SystemExit(f"{name}: kernel reported a timeout during warm-up")
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    # One event pair around the region; a step is exactly one kernel launch
+    # (two for the MLP block), so the kernel's average launch duration is
+    # region / steps (conservative: gaps between launches count against it).
+    region, _ = time_loop(wl.fused, steps, stream, per_launch=False)
+    per_launch = region / steps
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    bnd = rf.bound(wl.counts, peaks["bf16_tflops"], peaks["hbm_gbs"])
+    # the workload's metric: TFLOP/s when tensor-bound, GB/s of algorithmic
+    # bytes when HBM-bound
+    per_step, vscale, vunit = ((wl.counts.flops, 1e12, "TFLOP/s") if bnd == "tensor"
+                               else (wl.counts.fused_bytes, 1e9, "GB/s"))
+    max_region, total_units = aggregate(region, per_step * steps, world)
+    if gbf.gbf_check_device_error() != 0:
+        raise SystemExit(f"{name}: kernel reported a timeout in the timed region")
+    value = total_units / max_region / vscale
+
+    # unfused composition, same workload, same rotation of input sets.  The
+    # speedup is taken from alternating blocks of fused and unfused steps of
+    # equal length (about 0.1 s each), so that both see the same clock and
+    # power-cap state; the median block ratio is reported.
+    for i in range(3):
+        wl.unfused(i)
+    torch.cuda.synchronize()
+    block = max(3, min(args.unfused_steps, int(0.1 / max(per_launch, 1e-6))))
+    ratios, un_times, fu_times = [], [], []
+    for _ in range(args.speedup_rounds):
+        f_reg, _ = time_loop(wl.fused, block, stream, per_launch=False)
+        u_reg, _ = time_loop(wl.unfused, block, stream, per_launch=False)
+        ratios.append(u_reg / f_reg)
+        un_times.append(u_reg / block * 1e3)
+        fu_times.append(f_reg / block * 1e3)
+
+    # end to end through the public API with host buffers
+    wl.e2e_run(2, stream)
+    torch.cuda.synchronize()
+    e2e_region = wl.e2e_run(args.e2e_steps, stream)
+    e2e_max, e2e_units = aggregate(e2e_region, per_step * args.e2e_steps, world)
+
+    # MLP block: per-step latency of each way of issuing it, and the
+    # dominant kernel (the gate/up GEMM) timed on its own
+    extra = {}
+    per_launch_dom = per_launch
+    dom_counts = wl.counts
+    if wl.op == "mlp":
+        extra["latency_us"] = mlp_latency(wl, stream)
+        per_launch_dom, dom_counts = mlp_gate_up_kernel_time(wl, stream, steps)
+
+    # roofline of the dominant kernel of the step, against both peaks
+    long_loop = region > 0.5
+    tpeak = peaks["bf16_tflops_sustained"] if long_loop else peaks["bf16_tflops"]
+    ach_tf = dom_counts.flops / per_launch_dom / 1e12
+    ach_gb = dom_counts.fused_bytes / per_launch_dom / 1e9
+    if bnd == "tensor":
+        achieved, peak, unit = ach_tf, tpeak, "TFLOP/s"
+    else:
+        achieved, peak, unit = ach_gb, peaks["hbm_gbs"], "GB/s"
+    kname = {"persistent": "gemm_persistent_kernel", "swap_splitk": "gemm_swap_kernel",
+             "w4a16": "wq_gemm_kernel", "pair": "gemm_pair_kernel",
+             "add_rmsnorm": "add_rmsnorm_kernel",
+             "swiglu_pointwise": "swiglu_pointwise_kernel"}.get(wl.path, wl.path)
+    tpeak_name = ("bf16_tflops_sustained (back-to-back loop)" if long_loop
+                  else "bf16_tflops (burst)")
+    roof = {"bound": bnd, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": recorded_traffic(name, kname),
+            "peak_source": f"{peak_src}: " + (tpeak_name if bnd == "tensor" else "hbm_gbs"),
+            "kernel": kname,
+            "splits": wl.splits,
+            "kernel_ms": per_launch_dom * 1e3,
+            "algorithmic_flops": dom_counts.flops, "algorithmic_bytes": dom_counts.fused_bytes,
+            # both sides of the roofline (the slower of the two is the bound)
+            "achieved_tflops": ach_tf, "achieved_gbs": ach_gb,
+            "frac_tensor": ach_tf / tpeak, "frac_hbm": ach_gb / peaks["hbm_gbs"],
+            "tensor_peak": tpeak, "tensor_peak_source": f"{peak_src}: {tpeak_name}",
+            "hbm_peak": peaks["hbm_gbs"],
+            "roofline_ms": rf.roofline_seconds(dom_counts, peaks["bf16_tflops"],
+                                               peaks["hbm_gbs"]) * 1e3}
+    roof["frac_of_roofline"] = roof["roofline_ms"] / roof["kernel_ms"]
+    if bnd == "tensor":
+        roof["frac_of_burst_peak"] = ach_tf / peaks["bf16_tflops"]
+    if wl.op == "mlp":
+        chain_gbs = wl.counts.fused_bytes / per_launch / 1e9
+        roof["kernel"] = f"{roof['kernel']} (gate/up GEMM, the larger of the block's two)"
+        roof["chain"] = {"achieved": chain_gbs, "unit": "GB/s",
+                         "frac": chain_gbs / peaks["hbm_gbs"],
+                         "ms": per_launch * 1e3, "algorithmic_bytes": wl.counts.fused_bytes}
+    rec = {
+        "value": value, "unit": vunit, "steps": steps, "ms_per_step": max_region / steps * 1e3,
+        "config": config_of(name, wl.w, world),
+        "l2": f"{wl.n_sets} rotating input sets of {wl.set_bytes / 2**20:.0f} MiB (> 2x L2)",
+        "roofline": roof,
+        "unfused_ms_per_step": statistics.median(un_times),
+        "unfused_kind": wl.unfused_kind(),
+        "speedup_vs_unfused": statistics.median(ratios),
+        "speedup_method": (f"median over {args.speedup_rounds} alternating blocks of {block} "
+                           f"fused and {block} unfused steps (fused block "
+                           f"{statistics.median(fu_times):.4f} ms/step)"),
+        "e2e": {"value": e2e_units / e2e_max / vscale, "unit": vunit,
+                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes,
+                "method": (f"{args.e2e_steps} steps: inputs copied from pinned host memory "
+                           "into one of two device sets, the call, the result copied back; "
+                           "copies on their own streams overlap the neighbouring steps")},
+        "gpu_launches": steps * wl.launches_per_step(),
+        "clocks": clocks,
+        **extra,
+    }
+    w = wl.w
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec, w
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: enough for about 1.5 s of timed work)")
+                    help="timed steps per workload (default: enough for about 1.5 s of work)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="prefill",
-                    help="prefill | swiglu | w4a16 | tiny | sweep-<M>")
+    ap.add_argument("--workload", default="all",
+                    help="all (default: every workload, headline sweep-8192) | prefill | "
+                         "swiglu | w4a16 | tiny | sweep-<M> | w8a16_fp8 | w4a16_nvfp4 | "
+                         "add_rmsnorm | swiglu_pointwise | mlp_decode")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--unfused-steps", type=int, default=200,
                     help="upper bound on the steps of one block of the fused/unfused comparison")
     ap.add_argument("--speedup-rounds", type=int, default=5)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -719,149 +927,39 @@ def main(argv=None):
     gbf.load()
 
     dev = torch.device("cuda", local)
-    wl = Workload(args.workload, dev)
     stream = torch.cuda.current_stream()
     peaks, peak_src = load_peaks()
 
-    # warm-up (also checks the launch works)
-    for i in range(args.warmup):
-        wl.fused(i)
-    torch.cuda.synchronize()
-    if wl.op == "mlp":
-        wl.capture()  # the block is replayed from CUDA graphs from here on
-        for i in range(args.warmup):
-            wl.fused(i)
-        torch.cuda.synchronize()
-    if args.steps is None:
-        t_cal, _ = time_loop(wl.fused, 20, stream, per_launch=False)
-        args.steps = int(min(50000, max(200, 1.5 / max(t_cal / 20, 1e-6))))
-        if world > 1:
-            import torch.distributed as dist
-            k = torch.tensor([args.steps], dtype=torch.int64, device=dev)
-            dist.all_reduce(k, op=dist.ReduceOp.MIN)
-            args.steps = int(k.item())
-    if gbf.gbf_check_device_error() != 0:
-        raise SystemExit("kernel reported a timeout during warm-up")
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    # One event pair around the region; a step is exactly one kernel launch, so
-    # the kernel's average launch duration is region / steps (conservative:
-    # gaps between launches count against it).  The unfused leg is timed the
-    # same way, so the speedup compares like with like.
-    region, _ = time_loop(wl.fused, args.steps, stream, per_launch=False)
-    per_launch = region / args.steps
-    torch.cuda.synchronize()
-    barrier(world)
-    clocks = sampler.stop()
-    from tcgen05_tmem_bf16_gb300 import roofline as rf
-    bnd = rf.bound(wl.counts, peaks["bf16_tflops"], peaks["hbm_gbs"])
-    # the workload's metric: TFLOP/s when tensor-bound, GB/s of algorithmic
-    # bytes when HBM-bound
-    per_step, vscale, vunit = ((wl.counts.flops, 1e12, "TFLOP/s") if bnd == "tensor"
-                               else (wl.counts.fused_bytes, 1e9, "GB/s"))
-    max_region, total_units = aggregate(region, per_step * args.steps, world)
-    if gbf.gbf_check_device_error() != 0:
-        raise SystemExit("kernel reported a timeout in the timed region")
-    value = total_units / max_region / vscale
-
-    # unfused composition, same workload, same rotation of input sets.  The
-    # speedup is taken from alternating blocks of fused and unfused steps of
-    # equal length (about 0.1 s each), so that both see the same clock and
-    # power-cap state; the median block ratio is reported.
-    for i in range(3):
-        wl.unfused(i)
-    torch.cuda.synchronize()
-    fu_ms = max_region / args.steps * 1e3
-    block = max(3, min(args.unfused_steps, int(0.1 / max(per_launch, 1e-6))))
-    ratios, un_times, fu_times = [], [], []
-    for _ in range(args.speedup_rounds):
-        f_reg, _ = time_loop(wl.fused, block, stream, per_launch=False)
-        u_reg, _ = time_loop(wl.unfused, block, stream, per_launch=False)
-        ratios.append(u_reg / f_reg)
-        un_times.append(u_reg / block * 1e3)
-        fu_times.append(f_reg / block * 1e3)
-    un_ms = statistics.median(un_times)
-    speedup = statistics.median(ratios)
-
-    # end to end through the public API with host buffers
-    wl.e2e_run(2, stream)
-    torch.cuda.synchronize()
-    e2e_region = wl.e2e_run(args.e2e_steps, stream)
-    e2e_max, e2e_units = aggregate(e2e_region, per_step * args.e2e_steps, world)
-
-    # MLP block: per-step latency of each way of issuing it, and the
-    # dominant kernel (the gate/up GEMM) timed on its own
-    extra = {}
-    per_launch_dom = per_launch
-    dom_counts = wl.counts
-    if wl.op == "mlp":
-        extra["latency_us"] = mlp_latency(wl, stream)
-        per_launch_dom, dom_counts = mlp_gate_up_kernel_time(wl, stream, args.steps)
-
-    # roofline of the dominant kernel of the step
-    long_loop = region > 0.5
-    if bnd == "tensor":
-        achieved = dom_counts.flops / per_launch_dom / 1e12
-        peak = peaks["bf16_tflops_sustained"] if long_loop else peaks["bf16_tflops"]
-        unit = "TFLOP/s"
-    else:
-        achieved = dom_counts.fused_bytes / per_launch_dom / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-    kname = {"persistent": "gemm_persistent_kernel", "swap_splitk": "gemm_swap_kernel",
-             "w4a16": "wq_gemm_kernel", "pair": "gemm_pair_kernel",
-             "add_rmsnorm": "add_rmsnorm_kernel",
-             "swiglu_pointwise": "swiglu_pointwise_kernel"}.get(wl.path, wl.path)
-    roof = {"bound": bnd, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": recorded_traffic(args.workload, kname),
-            "peak_source": (f"{peak_src}: " + ("bf16_tflops_sustained (back-to-back loop)"
-                                               if bnd == "tensor" and long_loop else
-                                               ("bf16_tflops (burst)" if bnd == "tensor"
-                                                else "hbm_gbs"))),
-            "kernel": kname,
-            "splits": wl.splits,
-            "kernel_ms": per_launch_dom * 1e3,
-            "algorithmic_flops": dom_counts.flops, "algorithmic_bytes": dom_counts.fused_bytes,
-            "roofline_ms": rf.roofline_seconds(wl.counts, peaks["bf16_tflops"],
-                                               peaks["hbm_gbs"]) * 1e3}
-    if bnd == "tensor":
-        roof["frac_of_burst_peak"] = achieved / peaks["bf16_tflops"]
-    if wl.op == "mlp":
-        chain_gbs = wl.counts.fused_bytes / per_launch / 1e9
-        roof["kernel"] = f"{roof['kernel']} (gate/up GEMM, the larger of the block's two)"
-        roof["chain"] = {"achieved": chain_gbs, "unit": "GB/s", "frac": chain_gbs / peak,
-                         "ms": per_launch * 1e3, "algorithmic_bytes": wl.counts.fused_bytes}
+    head_name = HEADLINE if args.workload == "all" else args.workload
+    head, head_w = measure(head_name, args, dev, stream, peaks, peak_src, world, headline=True)
+    configs = {}
+    if args.workload == "all":
+        for name in SUB_WORKLOADS:
+            rec, _ = measure(name, args, dev, stream, peaks, peak_src, world, headline=False)
+            configs[name] = rec
 
     line = {
-        "metric": METRIC, "value": value, "unit": vunit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": fu_ms,
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+        "steps": head["steps"], "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {**config_of(args.workload, wl.w, world),
-                   "l2": f"{wl.n_sets} rotating input sets of {wl.set_bytes / 2**20:.0f} MiB "
-                         f"(> 2x L2)"},
+        "config": head["config"],
+        "l2": head["l2"],
         "impl": "gbfuse",
-        "roofline": roof,
-        "unfused_ms_per_step": un_ms,
-        "unfused_kind": wl.unfused_kind(),
-        "speedup_vs_unfused": speedup,
-        "speedup_method": (f"median over {args.speedup_rounds} alternating blocks of {block} fused "
-                           f"and {block} unfused steps (fused block {statistics.median(fu_times):.4f}"
-                           f" ms/step)"),
-        "e2e": {"value": e2e_units / e2e_max / vscale, "unit": vunit,
-                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes,
-                "method": (f"{args.e2e_steps} steps: inputs copied from pinned host memory "
-                           "into one of two device sets, the call, the result copied back; "
-                           "copies on their own streams overlap the neighbouring steps")},
-        "gpu_launches": args.steps * wl.launches_per_step(),
-        "clocks": clocks,
-        **extra,
+        "roofline": head["roofline"],
+        "unfused_ms_per_step": head["unfused_ms_per_step"],
+        "unfused_kind": head["unfused_kind"],
+        "speedup_vs_unfused": head["speedup_vs_unfused"],
+        "speedup_method": head["speedup_method"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        **{k: v for k, v in head.items() if k == "latency_us"},
     }
+    if configs:
+        line["configs"] = configs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl.w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(head_w, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
