@@ -755,9 +755,14 @@ def measure(name: str, args, dev, stream, peaks, peak_src, world: int, headline:
             wl.fused(i)
         torch.cuda.synchronize()
     steps = args.steps
-    if steps is None:
+    if steps is None or not headline:
         t_cal, _ = time_loop(wl.fused, 20, stream, per_launch=False)
-        steps = int(min(50000, max(200, 1.5 / max(t_cal / 20, 1e-6))))
+        if steps is None:
+            steps = int(min(50000, max(200, 1.5 / max(t_cal / 20, 1e-6))))
+        else:
+            # the other workloads' records: at least ~30 ms of timed work, so
+            # that the average per launch of a short kernel is well formed
+            steps = int(min(5000, max(steps, 0.03 / max(t_cal / 20, 1e-6))))
         if world > 1:
             import torch.distributed as dist
             k = torch.tensor([steps], dtype=torch.int64, device=dev)
