@@ -253,11 +253,18 @@ gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, 
                            w_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return GBF_ERR_CUDA;
   }
-  if (pair)
-    return cuda_status(launch_gemm_pair(plan, kn, dual, tmA, tmW, tmW2, ep, static_cast<int>(M),
+  // the output for the TMA stores of the persistent kernels' epilogues
+  CUtensorMap tmO{};
+  if (plan.path != kPathSwap &&
+      !tmap_2d(&tmO, ep.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, N, M, N * 2, 32, 32,
+               CU_TENSOR_MAP_SWIZZLE_64B))
+    return GBF_ERR_CUDA;
+  if (pair) {
+    return cuda_status(launch_gemm_pair(plan, kn, dual, tmA, tmW, tmW2, tmO, ep, static_cast<int>(M),
                                         static_cast<int>(N), static_cast<int>(K),
                                         make_ctl(err, plan_ctas(plan)), stream));
-  return cuda_status(launch_gemm(plan, kn, dual, tmA, tmW, tmW2, ep, static_cast<int>(M),
+  }
+  return cuda_status(launch_gemm(plan, kn, dual, tmA, tmW, tmW2, tmO, ep, static_cast<int>(M),
                                  static_cast<int>(N), static_cast<int>(K),
                                  make_ctl(err, plan_ctas(plan)), stream));
 }

@@ -95,6 +95,82 @@ __device__ __forceinline__ void epi_row32(const uint32_t (&acc)[32], const uint3
   }
 }
 
+// The ending of 32 consecutive output columns of one row, packed as 16
+// bf16x2 words (column pairs), for the staged store below.  Columns past N
+// see zero operands; the store does not write them.
+template <int ACT, bool DUAL>
+__device__ __forceinline__ void epi_row32_pack(const uint32_t (&acc)[32], const uint32_t (&up)[32],
+                                               const RowLoads& L, const EpiParams& e,
+                                               uint32_t (&w)[16]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float x[8];
+    if constexpr (DUAL) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        x[i] = act_apply<ACT>(e.alpha * __uint_as_float(acc[v * 8 + i])) *
+               (e.alpha * __uint_as_float(up[v * 8 + i]));
+      if (e.C) {
+        float c[8];
+        unpack8(L.c[v], c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = fmaf(e.beta, c[i], x[i]);
+      }
+    } else {
+      float c[8], b[8], r[8];
+      unpack8(L.c[v], c);
+      unpack8(L.b[v], b);
+      unpack8(L.r[v], r);
+      const float beta = e.C ? e.beta : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        x[i] = act_apply<ACT>(fmaf(beta, c[i], e.alpha * __uint_as_float(acc[v * 8 + i])) + b[i]) +
+               r[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[v * 4 + i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+  }
+}
+
+// Coalesced output through shared memory: each epilogue warp owns two 2 KB
+// staging buffers; one buffer holds a 32-row x 32-column bf16 chunk, rows of
+// 64 bytes in the tensor map's 64-byte swizzle (16-byte unit u of row r at
+// u ^ ((r >> 1) & 3)), so a quarter-warp's 16-byte stores fall on distinct
+// banks.  Lane 0 writes the chunk to global memory with one TMA store, which
+// covers whole rows of 64 bytes instead of 32 separate 16-byte pieces.
+constexpr int kStageChunkBytes = 32 * 64;
+
+__device__ __forceinline__ void stage_row32(uint8_t* buf, int r, const uint32_t (&w)[16]) {
+  const uint32_t base = smem_u32(buf) + static_cast<uint32_t>(r) * 64u;
+  const uint32_t sw = static_cast<uint32_t>((r >> 1) & 3);
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + ((u ^ sw) << 4)),
+                 "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                 : "memory");
+}
+
+// One warp's chunk (rows row0 .. row0+31, columns col0 .. col0+31) from the
+// thread-per-row registers `w` to global memory through staging buffer
+// `bufs[*flip]`.  The buffer's previous store (two chunks earlier) must have
+// finished reading it first.
+__device__ __forceinline__ void store_chunk32(uint8_t* bufs, int& flip, const uint32_t (&w)[16],
+                                              const CUtensorMap* out_map, int64_t row0,
+                                              int col0, int M, int N, uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  uint8_t* buf = bufs + flip * kStageChunkBytes;
+  if (lane == 0) bulk_wait_read<1>();
+  __syncwarp();
+  stage_row32(buf, lane, w);
+  fence_proxy_async_smem();  // the generic-proxy writes before the async-proxy read
+  __syncwarp();
+  if (lane == 0) {
+    if (row0 < M && col0 < N) tma_store_2d(out_map, buf, col0, static_cast<int32_t>(row0), pol);
+    bulk_commit();
+  }
+  flip ^= 1;
+}
+
 // Persistent tile raster: groups of `group` M-tiles (kGroupM by default);
 // inside a group the N-tile index varies slowest, so the CTAs working at the
 // same time share weight panels (and activation panels) in L2.

@@ -63,7 +63,11 @@ template <int BN>
 struct PairCfg {
   static constexpr int kBBytes = (BN / 2) * kBK * 2;
   static constexpr int kStageBytes = kQStreams * kQABytes + kBBytes;  // A0 | A1 | B
-  static constexpr int kSmem = 1024 + kQStages * kStageBytes + 256;
+  // ring | barriers (1 KB) | output staging: 8 epilogue warps x 2 buffers of 2 KB
+  static constexpr int kBarBytes = 1024;
+  static constexpr int kStagingBytes = 8 * 2 * kStageChunkBytes;
+  static constexpr int kSmem = 1024 + kQStages * kStageBytes + kBarBytes + kStagingBytes;
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   static constexpr int kChunks = BN / 32;             // 32-column epilogue chunks
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN <= 256, "tile width");
@@ -85,7 +89,8 @@ __device__ __forceinline__ void settle_after_abort() {
 template <bool W_KN, bool DUAL, int BN>
 __global__ void __launch_bounds__(kQThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                     const __grid_constant__ CUtensorMap tmW2, const PairArgs a) {
+                     const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmO,
+                     const PairArgs a) {
   using Cfg = PairCfg<BN>;
   static_assert(!(W_KN || DUAL) || BN == 256, "narrow tiles only for K-contiguous single B");
   extern __shared__ uint8_t smem_raw[];
@@ -98,6 +103,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint64_t* done = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  uint8_t* staging = smem + kQStages * Cfg::kStageBytes + Cfg::kBarBytes;  // 1024-aligned
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -121,6 +127,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
     if (DUAL) tma_prefetch_desc(&tmW2);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 2) {
     tmem_alloc_pair(tmem_holder, 512);
@@ -249,6 +256,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int c_end = half == 0 ? kFirst : kChunks;
     const uint32_t tempty_leader[kQStreams] = {mapa_shared(smem_u32(&tempty[0]), 0),
                                                mapa_shared(smem_u32(&tempty[1]), 0)};
+    uint8_t* my_staging = staging + (warp - 4) * 2 * kStageChunkBytes;
+    int flip = 0;
     // tile l of the pair: super tile pair + (l / 2) * npairs, M-tile l % 2 of it
     for (int local = 0; pair + (local / kQStreams) * npairs < num_super; ++local) {
       const int st = local % kQStreams;
@@ -282,18 +291,19 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
         const RowLoads cur = L;
         if (c + 1 < c_end) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep, pol);
-        if (row < a.M) {
-          switch (a.ep.act) {
-            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
-            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
-            case kActGeluTanh:
-              epi_row32<kActGeluTanh, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol);
-              break;
-            default: epi_row32<kActIdentity, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
-          }
+        uint32_t w[16];
+        switch (a.ep.act) {
+          case kActRelu: epi_row32_pack<kActRelu, DUAL>(acc, up, cur, a.ep, w); break;
+          case kActSilu: epi_row32_pack<kActSilu, DUAL>(acc, up, cur, a.ep, w); break;
+          case kActGeluTanh: epi_row32_pack<kActGeluTanh, DUAL>(acc, up, cur, a.ep, w); break;
+          default: epi_row32_pack<kActIdentity, DUAL>(acc, up, cur, a.ep, w); break;
         }
+        store_chunk32(my_staging, flip, w, &tmO, row - lane, col0, a.M, a.N, pol);
       }
     }
+    // every staged chunk written to global memory before the CTA may exit
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
 
   if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
@@ -310,7 +320,8 @@ namespace {
 
 template <bool W_KN, bool DUAL, int BN>
 cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                     const CUtensorMap& tmW2, const PairArgs& args, cudaStream_t stream) {
+                     const CUtensorMap& tmW2, const CUtensorMap& tmO, const PairArgs& args,
+                     cudaStream_t stream) {
   static std::atomic<uint64_t> mask{0};
   auto kernel = gemm_pair_kernel<W_KN, DUAL, BN>;
   constexpr int kQSmem = PairCfg<BN>::kSmem;
@@ -339,7 +350,7 @@ cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMa
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, tmW2, args);
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, tmW2, tmO, args);
 }
 
 }  // namespace
@@ -369,15 +380,15 @@ int max_active_pairs() {
 
 cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
                              const CUtensorMap& tmW, const CUtensorMap& tmW2,
-                             const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
-                             cudaStream_t stream) {
+                             const CUtensorMap& tmO, const EpiParams& ep, int M, int N, int K,
+                             const KernelCtl& ctl, cudaStream_t stream) {
   PairArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
   if (w_kn)
-    return dual ? run_pair<true, true, 256>(plan, tmA, tmW, tmW2, args, stream)
-                : run_pair<true, false, 256>(plan, tmA, tmW, tmW2, args, stream);
-  if (dual) return run_pair<false, true, 256>(plan, tmA, tmW, tmW2, args, stream);
-  return plan.bn == 224 ? run_pair<false, false, 224>(plan, tmA, tmW, tmW2, args, stream)
-                        : run_pair<false, false, 256>(plan, tmA, tmW, tmW2, args, stream);
+    return dual ? run_pair<true, true, 256>(plan, tmA, tmW, tmW2, tmO, args, stream)
+                : run_pair<true, false, 256>(plan, tmA, tmW, tmW2, tmO, args, stream);
+  if (dual) return run_pair<false, true, 256>(plan, tmA, tmW, tmW2, tmO, args, stream);
+  return plan.bn == 224 ? run_pair<false, false, 224>(plan, tmA, tmW, tmW2, tmO, args, stream)
+                        : run_pair<false, false, 256>(plan, tmA, tmW, tmW2, tmO, args, stream);
 }
 
 }  // namespace gbf

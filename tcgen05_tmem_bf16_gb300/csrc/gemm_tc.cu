@@ -49,7 +49,10 @@ constexpr int kPABytes = kBM * kBK * 2;             // 16 KB
 constexpr int kPBBytes = kPersistBN * kBK * 2;      // 32 KB
 constexpr int kPStageBytes = kPABytes + kPBBytes;   // 48 KB
 constexpr int kPThreads = 384;  // warps 0-3 roles, warps 4-11 epilogue (two warpgroups)
-constexpr int kPSmem = 1024 + kPStages * kPStageBytes + 256;
+// ring | barriers (1 KB) | output staging: 8 epilogue warps x 2 buffers of 2 KB
+constexpr int kPBarBytes = 1024;
+constexpr int kPSmem = 1024 + kPStages * kPStageBytes + kPBarBytes + 8 * 2 * kStageChunkBytes;
+static_assert(kPSmem <= 227 * 1024, "shared memory per CTA");
 
 struct PersistArgs {
   int M, N, K;
@@ -62,7 +65,8 @@ template <bool W_KN, bool DUAL>
 __global__ void __launch_bounds__(kPThreads, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmW,
-                           const __grid_constant__ CUtensorMap tmW2, const PersistArgs a) {
+                           const __grid_constant__ CUtensorMap tmW2,
+                           const __grid_constant__ CUtensorMap tmO, const PersistArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
@@ -73,6 +77,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* done = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  uint8_t* staging = smem + kPStages * kPStageBytes + kPBarBytes;  // 1024-aligned
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -92,6 +97,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW);
     if (DUAL) tma_prefetch_desc(&tmW2);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 2) {
     tmem_alloc(tmem_holder, 512);
@@ -213,6 +219,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint64_t pol = l2_evict_first_policy();
     constexpr int kChunks = (DUAL ? 128 : 256) / 32;
     constexpr int kMine = kChunks / 2;
+    uint8_t* my_staging = staging + (warp - 4) * 2 * kStageChunkBytes;
+    int flip = 0;
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
       int mb, nb;
@@ -240,18 +248,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         const RowLoads cur = L;
         if (cc + 1 < kMine) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep, pol);
-        if (row < a.M) {
-          switch (a.ep.act) {
-            case kActRelu: epi_row32<kActRelu, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
-            case kActSilu: epi_row32<kActSilu, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
-            case kActGeluTanh:
-              epi_row32<kActGeluTanh, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol);
-              break;
-            default: epi_row32<kActIdentity, DUAL>(acc, up, cur, row, col0, a.N, a.ep, pol); break;
-          }
+        uint32_t w[16];
+        switch (a.ep.act) {
+          case kActRelu: epi_row32_pack<kActRelu, DUAL>(acc, up, cur, a.ep, w); break;
+          case kActSilu: epi_row32_pack<kActSilu, DUAL>(acc, up, cur, a.ep, w); break;
+          case kActGeluTanh: epi_row32_pack<kActGeluTanh, DUAL>(acc, up, cur, a.ep, w); break;
+          default: epi_row32_pack<kActIdentity, DUAL>(acc, up, cur, a.ep, w); break;
         }
+        store_chunk32(my_staging, flip, w, &tmO, row - lane, col0, a.M, a.N, pol);
       }
     }
+    // every staged chunk written to global memory before the CTA may exit
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
 
   if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
@@ -720,13 +729,13 @@ cudaError_t ensure_smem_attr(K kernel, int bytes, std::atomic<uint64_t>& mask) {
 
 template <bool W_KN, bool DUAL>
 cudaError_t run_persistent(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                           const CUtensorMap& tmW2, const PersistArgs& args,
-                           cudaStream_t stream) {
+                           const CUtensorMap& tmW2, const CUtensorMap& tmO,
+                           const PersistArgs& args, cudaStream_t stream) {
   static std::atomic<uint64_t> mask{0};
   auto kernel = gemm_persistent_kernel<W_KN, DUAL>;
   cudaError_t e = ensure_smem_attr(kernel, kPSmem, mask);
   if (e != cudaSuccess) return e;
-  kernel<<<p.grid, kPThreads, kPSmem, stream>>>(tmA, tmW, tmW2, args);
+  kernel<<<p.grid, kPThreads, kPSmem, stream>>>(tmA, tmW, tmW2, tmO, args);
   return cudaGetLastError();
 }
 
@@ -780,16 +789,16 @@ cudaError_t run_swap_mpad(const GemmPlan& p, bool dual, const CUtensorMap& tmA,
 }  // namespace
 
 cudaError_t launch_gemm(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
-                        const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                        const CUtensorMap& tmW, const CUtensorMap& tmW2, const CUtensorMap& tmO,
                         const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
                         cudaStream_t stream) {
   if (plan.path == kPathPersistent) {
     PersistArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
     if (w_kn)
-      return dual ? run_persistent<true, true>(plan, tmA, tmW, tmW2, args, stream)
-                  : run_persistent<true, false>(plan, tmA, tmW, tmW2, args, stream);
-    return dual ? run_persistent<false, true>(plan, tmA, tmW, tmW2, args, stream)
-                : run_persistent<false, false>(plan, tmA, tmW, tmW2, args, stream);
+      return dual ? run_persistent<true, true>(plan, tmA, tmW, tmW2, tmO, args, stream)
+                  : run_persistent<true, false>(plan, tmA, tmW, tmW2, tmO, args, stream);
+    return dual ? run_persistent<false, true>(plan, tmA, tmW, tmW2, tmO, args, stream)
+                : run_persistent<false, false>(plan, tmA, tmW, tmW2, tmO, args, stream);
   }
   if (plan.path == kPathSwap) {
     SwapArgs args{M, N, K, plan.num_kb, plan.splits, ep, ctl};

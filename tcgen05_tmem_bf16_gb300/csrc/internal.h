@@ -65,17 +65,21 @@ GemmPlan plan_w4a16(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 
 // ---- launchers ---------------------------------------------------------------
 // Dense bf16 GEMM with fused ending (gemm_tc.cu).  tmA: activations [M][K];
-// tmW / tmW2: weights (tmW2 = up weights of the dual GEMM).
+// tmW / tmW2: weights (tmW2 = up weights of the dual GEMM); tmO: the output
+// [M][N] in boxes of 32 x 32 with the 64-byte swizzle (used by the
+// persistent kernel's TMA stores; the swapped kernel writes directly).
 cudaError_t launch_gemm(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
-                        const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                        const CUtensorMap& tmW, const CUtensorMap& tmW2, const CUtensorMap& tmO,
                         const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
                         cudaStream_t stream);
 
-// The same on CTA pairs with tcgen05.mma.cta_group::2 (gemm_pair.cu).
+// The same on CTA pairs with tcgen05.mma.cta_group::2 (gemm_pair.cu).  tmO:
+// the output [M][N] bf16 in boxes of 32 x 32 with the 64-byte swizzle (the
+// epilogue writes it with TMA stores).
 cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
                              const CUtensorMap& tmW, const CUtensorMap& tmW2,
-                             const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
-                             cudaStream_t stream);
+                             const CUtensorMap& tmO, const EpiParams& ep, int M, int N, int K,
+                             const KernelCtl& ctl, cudaStream_t stream);
 int max_active_pairs();
 
 // Weight-only quantised GEMM (wq_gemm.cu).  tmA: activations; tmQ: the

@@ -86,19 +86,31 @@ struct W4Cfg {
   static constexpr int kStages = FMT == kWqFp8 ? 3 : (MPAD <= 16 ? 5 : 4);
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
   static constexpr uint32_t kTmemCols = 256;
-  // Accumulator sets: the 16-deep K steps alternate between kSets copies of
-  // the four region accumulators, so that 4*kSets independent accumulation
-  // chains are in flight (a narrow MMA's time is set by its accumulator's
-  // read-after-write chain); the epilogue adds the sets, set 0 first.
-  static constexpr int kSets = MPAD <= 16 ? 2 : 1;
-  // MMA issuing threads.  tcgen05.mma instructions from one thread complete
-  // one after another (about 150 cycles each on this part, whatever their N),
-  // while those of different threads overlap; with two accumulator sets, set
-  // g is fed by its own issuer from transform group g's operand buffer.
-  static constexpr int kIssuers = kSets;
-  static constexpr uint32_t kColA = kSets * kW4Regions * MPAD;  // D(set e, region r) at (4e+r)*MPAD
-  // A buffer of group g at kColA + 64g; region r at +16r (16 columns = 32 k).
-  static_assert(kColA + 128 <= kTmemCols, "TMEM budget");
+  // Tensor-memory pipeline between the transform warps and the MMAs.
+  //
+  // Accumulators: kSets copies of the four region accumulators, D(set e,
+  // region r) at columns (4e + r) * MPAD.  With one set the two MMA issuers
+  // split the regions (issuer i owns regions 2i and 2i+1, every K step);
+  // with two sets issuer i owns set i and takes every other operand unit.
+  // Either way every accumulator has exactly one writer, and the epilogue
+  // adds the sets, set 0 first.
+  //
+  // Operand units: the dequantised weights of kUnitRows k-rows (all four
+  // regions, kUnitRows / 2 columns each) are one hand-over from a transform
+  // group to the MMAs.  The units of consecutive stages go round a ring of
+  // kBufs tensor-memory buffers, so a transform group refills a buffer while
+  // the MMAs still read the previous ones; a buffer is released when every
+  // MMA that reads it has completed.
+  static constexpr int kSets = 1;
+  static constexpr int kUnitRows = 32;
+  static constexpr int kIssuers = 2;
+  static constexpr int kUnits = kBK / kUnitRows;        // units per stage (2 per group or 1)
+  static constexpr int kUnitCols = 2 * kUnitRows;       // 4 regions x kUnitRows / 2 columns
+  static constexpr uint32_t kColA = kSets * kW4Regions * MPAD;
+  static constexpr int kBufs = (kTmemCols - kColA) / kUnitCols;
+  static_assert(kBufs >= 2 && kBufs <= 8, "operand ring of two to eight buffers");
+  static_assert(kColA + kBufs * kUnitCols <= kTmemCols, "TMEM budget");
+  static_assert(kUnits % 2 == 0, "each transform group fills whole units");
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static_assert(kStages * kStageBytes >= 128 * kW4Regions * MPAD * 4, "reduction buffer");
   static_assert(kSmem <= 115 * 1024, "two CTAs per SM");
@@ -151,6 +163,50 @@ __device__ __forceinline__ void deq_rowpair(uint32_t x0, uint32_t x1, uint32_t c
       : "r"(x0), "r"(x1), "r"(c136), "r"(s0), "r"(s1), "r"(s2), "r"(s3));
 }
 
+// The same with one fused multiply-add per bf16x2 pair, for scales with
+// |s| < 2^-5.  (x & 0x000F000F) read as bf16x2 is the pair of subnormals
+// (q * 2^-133), exactly; with sp = s * 2^133 (exact: no overflow for such s)
+// and c = -8 s (exact), fma(q * 2^-133, sp, c) = q*s - 8*s computed exactly
+// and rounded once, i.e. bf16_rne((q - 8) * s) as the definition asks.
+// 12 instructions per k-row pair instead of 16.
+__device__ __forceinline__ void deq_rowpair_fma(uint32_t x0, uint32_t x1, uint32_t sp0,
+                                                uint32_t sp1, uint32_t sp2, uint32_t sp3,
+                                                uint32_t c0, uint32_t c1, uint32_t c2,
+                                                uint32_t c3, uint32_t& o0, uint32_t& o1,
+                                                uint32_t& o2, uint32_t& o3) {
+  asm("{\n\t"
+      ".reg .b32 x, t0, t1, t2, t3;\n\t"
+      "prmt.b32 x, %4, %5, 0x5410;\n\t"
+      "shr.b32 t0, x, 4;\n\t"
+      "shr.b32 t2, x, 12;\n\t"
+      "shr.b32 t3, x, 8;\n\t"
+      "and.b32 t0, t0, 0x000F000F;\n\t"
+      "and.b32 t1, x, 0x000F000F;\n\t"
+      "and.b32 t2, t2, 0x000F000F;\n\t"
+      "and.b32 t3, t3, 0x000F000F;\n\t"
+      "fma.rn.bf16x2 %0, t0, %6, %10;\n\t"
+      "fma.rn.bf16x2 %1, t1, %7, %11;\n\t"
+      "fma.rn.bf16x2 %2, t2, %8, %12;\n\t"
+      "fma.rn.bf16x2 %3, t3, %9, %13;\n\t"
+      "}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(x0), "r"(x1), "r"(sp0), "r"(sp1), "r"(sp2), "r"(sp3), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3));
+}
+
+// bf16x2 a * b (round to nearest even).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// |value| of a bf16x2 (s, s) pair below the bf16 `limit_bits` (NaN and
+// infinity are not).
+__device__ __forceinline__ bool bf16_abs_below(uint32_t pair, uint32_t limit_bits) {
+  return (pair & 0x7FFFu) < limit_bits;
+}
+
 // FP8 k-row pair: x0, x1 = the 32-bit loads (bytes = columns 4t..4t+3) of
 // rows k and k+1.  Region r: prmt puts byte r of each row into bytes 1 and 3
 // (the high byte of each half), the magnitude bits move down by 4 into the
@@ -189,6 +245,40 @@ __device__ __forceinline__ void deq_fp8_rowpair(uint32_t x0, uint32_t x1, uint32
       "}"
       : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
       : "r"(x0), "r"(x1), "r"(s0), "r"(s1), "r"(s2), "r"(s3), "r"(kBf16x2Pow120));
+}
+
+// The same with the two multiplies fused, for scales with |s| < 2^8: with
+// sp = s * 2^120 (exact), code * 2^-120 * sp is the exact product e4m3 * s,
+// rounded once.  20 instructions per k-row pair instead of 24.
+__device__ __forceinline__ void deq_fp8_rowpair_fused(uint32_t x0, uint32_t x1, uint32_t sp0,
+                                                      uint32_t sp1, uint32_t sp2, uint32_t sp3,
+                                                      uint32_t& o0, uint32_t& o1, uint32_t& o2,
+                                                      uint32_t& o3) {
+  asm("{\n\t"
+      ".reg .b32 y, u;\n\t"
+      "prmt.b32 y, %4, %5, 0x4400;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 %0, u, %6;\n\t"
+      "prmt.b32 y, %4, %5, 0x5511;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 %1, u, %7;\n\t"
+      "prmt.b32 y, %4, %5, 0x6622;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 %2, u, %8;\n\t"
+      "prmt.b32 y, %4, %5, 0x7733;\n\t"
+      "and.b32 u, y, 0x7F007F00;\n\t"
+      "shr.b32 u, u, 4;\n\t"
+      "lop3.b32 u, u, y, 0x80008000, 0xF8;\n\t"
+      "mul.rn.bf16x2 %3, u, %9;\n\t"
+      "}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(x0), "r"(x1), "r"(sp0), "r"(sp1), "r"(sp2), "r"(sp3));
 }
 
 // Four E4M3 scale bytes (columns 4t..4t+3) -> four bf16x2 (s, s) pairs, exact.
@@ -339,9 +429,9 @@ __global__ void __launch_bounds__(kW4Threads, 2)
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kStages * Cfg::kStageBytes);
   uint64_t* empty = full + Cfg::kStages;
-  uint64_t* afull = empty + Cfg::kStages;  // [2]: transform group g -> MMA
-  uint64_t* aempty = afull + 2;            // [2]: MMA -> transform group g
-  uint64_t* dfull = aempty + 2;
+  uint64_t* afull = empty + Cfg::kStages;  // [kBufs]: operand buffer written
+  uint64_t* aempty = afull + Cfg::kBufs;   // [kBufs]: operand buffer read by the MMAs
+  uint64_t* dfull = aempty + Cfg::kBufs;
   uint64_t* done = dfull + 1;
   uint64_t* recvb = done + 1;  // split-K partials pushed here by the other ranks
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(recvb + 1);
@@ -361,9 +451,9 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 8 + Cfg::kIssuers);  // 8 transform warps + the MMA commits
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&afull[i], 4);
-      mbar_init(&aempty[i], 1);
+    for (int i = 0; i < Cfg::kBufs; ++i) {
+      mbar_init(&afull[i], 4);                              // the writing group's 4 warps
+      mbar_init(&aempty[i], Cfg::kSets == 1 ? 2 : 1);       // the commits of its readers
     }
     mbar_init(dfull, Cfg::kIssuers);
     mbar_init(done, Cfg::kIssuers);
@@ -437,45 +527,56 @@ __global__ void __launch_bounds__(kW4Threads, 2)
         if (fills[i]) wait_bar(&full[i], (fills[i] - 1) & 1, ctl, kSiteDrain, false);
     }
     __syncwarp();
-  } else if (warp == 1 || (warp == 3 && Cfg::kIssuers == 2)) {
+  } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------ MMA issuers
-    // one issuer: both groups' buffers, K steps alternating over the sets;
-    // two issuers: issuer i takes group i's buffer into accumulator set i
+    // The operand units of the CTA's K range in order h = 0, 1, ...; unit h
+    // sits in buffer h % kBufs.  One set: both issuers read every unit, each
+    // into its own two regions.  Two sets: issuer i reads units h % 2 == i,
+    // all four regions, into set i.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kBM, MPAD, false, false);
+      constexpr int kSteps = Cfg::kUnitRows / 16;   // 16-deep K steps per unit
+      constexpr int kRegionCols = Cfg::kUnitRows / 2;
       const int issuer = warp == 1 ? 0 : 1;
-      const int g0 = Cfg::kIssuers == 2 ? issuer : 0;
-      const int g1 = Cfg::kIssuers == 2 ? issuer + 1 : 2;
+      const int r0 = Cfg::kSets == 1 ? 2 * issuer : 0;
+      const int r1 = Cfg::kSets == 1 ? r0 + 2 : kW4Regions;
+      const uint32_t dset = tmem_base + (Cfg::kSets == 1 ? 0 : issuer) * kW4Regions * MPAD;
       int s = 0;
       uint32_t ph = 0;
+      int b = 0;          // buffer of unit h
+      uint32_t bph = 0;   // parity of unit h's use of that buffer
+      int h = 0;
       bool ok = true;
       for (int kb = kb0; kb < kb1 && ok; ++kb) {
-        const uint32_t gph = (kb - kb0) & 1;
         if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
           ok = false;
           break;
         }
         const uint32_t x0 = smem_u32(stages + s * Cfg::kStageBytes + Cfg::kQBytes);
-        for (int g = g0; g < g1; ++g) {
-          if (!wait_bar(&afull[g], gph, ctl, kSiteMmaOperand)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t abuf = tmem_base + Cfg::kColA + 64 * g;
+        for (int uu = 0; uu < Cfg::kUnits; ++uu, ++h) {
+          if (Cfg::kSets == 1 || (h & 1) == issuer) {
+            if (!wait_bar(&afull[b], bph, ctl, kSiteMmaOperand)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t abuf = tmem_base + Cfg::kColA + Cfg::kUnitCols * b;
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const uint64_t bd = sdesc_sw128(x0 + (2 * g + k) * 32, 16, 1024);
-            const int j = (kb - kb0) * 4 + 2 * g + k;  // K step within this CTA's range
-            const int e = Cfg::kIssuers == 2 ? issuer : j % Cfg::kSets;
-            const uint32_t accum =
-                Cfg::kIssuers == 2 ? ((kb > kb0 || k > 0) ? 1u : 0u) : (j >= Cfg::kSets ? 1u : 0u);
+            for (int k = 0; k < kSteps; ++k) {
+              // activation rows of k-rows [uu * kUnitRows + 16 k, +16) of the stage
+              const uint64_t bd = sdesc_sw128(x0 + (uu * kSteps + k) * 32, 16, 1024);
+              // the first K step into an accumulator overwrites it
+              const uint32_t accum = (h >= Cfg::kSets || k > 0) ? 1u : 0u;
 #pragma unroll
-            for (int r = 0; r < kW4Regions; ++r)
-              mma_ts(tmem_base + (e * kW4Regions + r) * MPAD, abuf + 16 * r + 8 * k, bd, idesc,
-                     accum);
+              for (int r = r0; r < r1; ++r)
+                mma_ts(dset + r * MPAD, abuf + kRegionCols * r + 8 * k, bd, idesc, accum);
+            }
+            mma_commit(&aempty[b]);
           }
-          mma_commit(&aempty[g]);
+          if (++b == Cfg::kBufs) {
+            b = 0;
+            bph ^= 1;
+          }
         }
         if (!ok) break;
         mma_commit(&empty[s]);
@@ -495,18 +596,60 @@ __global__ void __launch_bounds__(kW4Threads, 2)
     const int q = warp & 3;                 // TMEM lane quarter
     const int t = q * 32 + lane;            // TMEM lane = owner of packed bytes 2t, 2t+1
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t abuf = tmem_base + lane_off + Cfg::kColA + 64 * g;
+    const uint32_t lane_base = tmem_base + lane_off + Cfg::kColA;
+    constexpr int kHalvesPerUnit = Cfg::kUnitRows / 16;  // 16-row halves of a unit
+    constexpr int kRegionCols = Cfg::kUnitRows / 2;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    // The operand buffer is waited for only once the first half's weights
-    // are dequantised in registers, so that work overlaps the MMAs still
-    // reading the buffer.
+    // Each 16-row half of the group's 32 rows is dequantised in registers
+    // first; only then is the unit's buffer waited for, so that this work
+    // overlaps the MMAs still reading the buffer's previous unit.
     for (int kb = kb0; kb < kb1 && ok; ++kb) {
-      const uint32_t gph = (kb - kb0) & 1;
       if (!wait_bar(&full[s], ph, ctl, kSiteXformFull)) break;
+      const int j = kb - kb0;
       const uint8_t* sq = stages + s * Cfg::kStageBytes;
       const uint8_t* ssc = sq + Cfg::kQBytes + Cfg::kXBytes;
+      int cur = 0;         // buffer of the unit being filled
+      uint32_t ubuf = 0;   // its TMEM address in this warp's lane quarter
+      // wait until the unit holding half `hh` of this group's rows has a free buffer
+      auto acquire = [&](int hh) -> bool {
+        const int h = Cfg::kUnits * j + (Cfg::kUnits / 2) * g + hh / kHalvesPerUnit;
+        cur = h % Cfg::kBufs;
+        const uint32_t use = static_cast<uint32_t>(h / Cfg::kBufs);
+        if (!wait_bar(&aempty[cur], (use & 1) ^ 1, ctl, kSiteXformEmpty)) return false;
+        tc_fence_after();
+        ubuf = lane_base + Cfg::kUnitCols * cur;
+        return true;
+      };
+      // store half `hh` (eight bf16x2 k-row pairs of each region)
+      auto put = [&](int hh, const uint32_t (&o0)[8], const uint32_t (&o1)[8],
+                     const uint32_t (&o2)[8], const uint32_t (&o3)[8]) {
+        const uint32_t c = 8 * (hh % kHalvesPerUnit);
+        tmem_st8(ubuf + c, o0);
+        tmem_st8(ubuf + kRegionCols + c, o1);
+        tmem_st8(ubuf + 2 * kRegionCols + c, o2);
+        tmem_st8(ubuf + 3 * kRegionCols + c, o3);
+        if (hh % kHalvesPerUnit == kHalvesPerUnit - 1) {  // the unit is complete
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull[cur]);
+        }
+      };
+      // one 16-row half: dequantise its 8 k-row pairs with `deq`
+      // (x0, x1 -> four bf16x2), then hand it to the unit's buffer
+      auto half = [&](int hh, const uint8_t* rows, int row_bytes, auto deq) -> bool {
+        uint32_t o0[8], o1[8], o2[8], o3[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int row = 16 * hh + 2 * p;
+          deq(rows + row * row_bytes, rows + (row + 1) * row_bytes, o0[p], o1[p], o2[p], o3[p]);
+        }
+        if (hh % kHalvesPerUnit == 0 && !acquire(hh)) return false;
+        put(hh, o0, o1, o2, o3);
+        return true;
+      };
       if constexpr (FMT == kWqFp8) {
         // bytes 4t..4t+3 of each k-row: box half t/64, word t%64
         const uint2 sc = *reinterpret_cast<const uint2*>(ssc + 8 * t);
@@ -515,81 +658,89 @@ __global__ void __launch_bounds__(kW4Threads, 2)
         const uint32_t s2 = __byte_perm(sc.y, 0, 0x1010);
         const uint32_t s3 = __byte_perm(sc.y, 0, 0x3232);
         const uint8_t* rows = sq + (t >> 6) * (kBK * 256) + (32 * g) * 256 + 4 * (t & 63);
+        // |s| < 2^8 on every lane: one multiply by s * 2^120 per pair
+        constexpr uint32_t kLimit = 0x4380u;  // bf16 2^8
+        if (__all_sync(0xffffffffu, bf16_abs_below(s0, kLimit) && bf16_abs_below(s1, kLimit) &&
+                                        bf16_abs_below(s2, kLimit) && bf16_abs_below(s3, kLimit))) {
+          const uint32_t p0 = bf16x2_mul(s0, kBf16x2Pow120), p1 = bf16x2_mul(s1, kBf16x2Pow120);
+          const uint32_t p2 = bf16x2_mul(s2, kBf16x2Pow120), p3 = bf16x2_mul(s3, kBf16x2Pow120);
+          auto deq = [=](const uint8_t* r0, const uint8_t* r1, uint32_t& a0, uint32_t& a1,
+                         uint32_t& a2, uint32_t& a3) {
+            deq_fp8_rowpair_fused(*reinterpret_cast<const uint32_t*>(r0),
+                                  *reinterpret_cast<const uint32_t*>(r1), p0, p1, p2, p3, a0, a1,
+                                  a2, a3);
+          };
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t o0[8], o1[8], o2[8], o3[8];
+          for (int hh = 0; hh < 2 && ok; ++hh) ok = half(hh, rows, 256, deq);
+        } else {
+          auto deq = [=](const uint8_t* r0, const uint8_t* r1, uint32_t& a0, uint32_t& a1,
+                         uint32_t& a2, uint32_t& a3) {
+            deq_fp8_rowpair(*reinterpret_cast<const uint32_t*>(r0),
+                            *reinterpret_cast<const uint32_t*>(r1), s0, s1, s2, s3, a0, a1, a2,
+                            a3);
+          };
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const int row = 16 * h + 2 * p;
-            const uint32_t x0 = *reinterpret_cast<const uint32_t*>(rows + row * 256);
-            const uint32_t x1 = *reinterpret_cast<const uint32_t*>(rows + (row + 1) * 256);
-            deq_fp8_rowpair(x0, x1, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
-          }
-          if (h == 0) {
-            if (!wait_bar(&aempty[g], gph ^ 1, ctl, kSiteXformEmpty)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          tmem_st8(abuf + 0 + 8 * h, o0);
-          tmem_st8(abuf + 16 + 8 * h, o1);
-          tmem_st8(abuf + 32 + 8 * h, o2);
-          tmem_st8(abuf + 48 + 8 * h, o3);
+          for (int hh = 0; hh < 2 && ok; ++hh) ok = half(hh, rows, 256, deq);
+        }
+      } else if constexpr (FMT == kWqInt4) {
+        const uint8_t* rows = sq + (32 * g) * Cfg::kRowBytes + 2 * t;
+        const uint2 sc = *reinterpret_cast<const uint2*>(ssc + 8 * t);
+        const uint32_t s0 = __byte_perm(sc.x, 0, 0x1010);  // bf16x2 (s, s), column 4t
+        const uint32_t s1 = __byte_perm(sc.x, 0, 0x3232);  // column 4t+1
+        const uint32_t s2 = __byte_perm(sc.y, 0, 0x1010);  // column 4t+2
+        const uint32_t s3 = __byte_perm(sc.y, 0, 0x3232);  // column 4t+3
+        // regions: 0 = high nibble of byte 2t, 1 = low of 2t, 2 = high of 2t+1,
+        // 3 = low of 2t+1
+        constexpr uint32_t kLimit = 0x3D00u;  // bf16 2^-5
+        if (__all_sync(0xffffffffu, bf16_abs_below(s0, kLimit) && bf16_abs_below(s1, kLimit) &&
+                                        bf16_abs_below(s2, kLimit) && bf16_abs_below(s3, kLimit))) {
+          // s * 2^133 = s * 2^126 * 2^7 (exact), and -8 s (exact)
+          constexpr uint32_t kPow126 = 0x7E807E80u, kPow7 = 0x43004300u, kMinus8 = 0xC100C100u;
+          const uint32_t p0 = bf16x2_mul(bf16x2_mul(s0, kPow126), kPow7);
+          const uint32_t p1 = bf16x2_mul(bf16x2_mul(s1, kPow126), kPow7);
+          const uint32_t p2 = bf16x2_mul(bf16x2_mul(s2, kPow126), kPow7);
+          const uint32_t p3 = bf16x2_mul(bf16x2_mul(s3, kPow126), kPow7);
+          const uint32_t c0 = bf16x2_mul(s0, kMinus8), c1 = bf16x2_mul(s1, kMinus8);
+          const uint32_t c2 = bf16x2_mul(s2, kMinus8), c3 = bf16x2_mul(s3, kMinus8);
+          auto deq = [=](const uint8_t* r0, const uint8_t* r1, uint32_t& a0, uint32_t& a1,
+                         uint32_t& a2, uint32_t& a3) {
+            deq_rowpair_fma(*reinterpret_cast<const uint16_t*>(r0),
+                            *reinterpret_cast<const uint16_t*>(r1), p0, p1, p2, p3, c0, c1, c2,
+                            c3, a0, a1, a2, a3);
+          };
+#pragma unroll
+          for (int hh = 0; hh < 2 && ok; ++hh) ok = half(hh, rows, Cfg::kRowBytes, deq);
+        } else {
+          auto deq = [=](const uint8_t* r0, const uint8_t* r1, uint32_t& a0, uint32_t& a1,
+                         uint32_t& a2, uint32_t& a3) {
+            deq_rowpair(*reinterpret_cast<const uint16_t*>(r0),
+                        *reinterpret_cast<const uint16_t*>(r1), 0x43084308u, s0, s1, s2, s3, a0,
+                        a1, a2, a3);
+          };
+#pragma unroll
+          for (int hh = 0; hh < 2 && ok; ++hh) ok = half(hh, rows, Cfg::kRowBytes, deq);
         }
       } else {
         const uint8_t* rows = sq + (32 * g) * Cfg::kRowBytes + 2 * t;
-        uint32_t s0, s1, s2, s3;
-        if constexpr (FMT == kWqInt4) {
-          const uint2 sc = *reinterpret_cast<const uint2*>(ssc + 8 * t);
-          s0 = __byte_perm(sc.x, 0, 0x1010);  // bf16x2 (s, s), column 4t
-          s1 = __byte_perm(sc.x, 0, 0x3232);  // column 4t+1
-          s2 = __byte_perm(sc.y, 0, 0x1010);  // column 4t+2
-          s3 = __byte_perm(sc.y, 0, 0x3232);  // column 4t+3
-        }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if constexpr (FMT == kWqNvfp4) {
-            // the E4M3 block scale of k-rows [32g + 16h, +16): block row 2g + h
-            const uint32_t b = *reinterpret_cast<const uint32_t*>(
-                ssc + (t >> 6) * 1024 + (2 * g + h) * 256 + 4 * (t & 63));
-            e4m3x4_to_bf16x2_dup(b, s0, s1, s2, s3);
-          }
-          uint32_t o0[8], o1[8], o2[8], o3[8];
-#pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const int row = 16 * h + 2 * p;
-            const uint32_t x0 = *reinterpret_cast<const uint16_t*>(rows + row * Cfg::kRowBytes);
-            const uint32_t x1 =
-                *reinterpret_cast<const uint16_t*>(rows + (row + 1) * Cfg::kRowBytes);
-            // regions: 0 = high nibble of byte 2t, 1 = low of 2t, 2 = high of 2t+1,
-            // 3 = low of 2t+1
-            if constexpr (FMT == kWqInt4)
-              deq_rowpair(x0, x1, 0x43084308u, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
-            else
-              deq_fp4_rowpair(x0, x1, s0, s1, s2, s3, o0[p], o1[p], o2[p], o3[p]);
-          }
-          if (h == 0) {
-            if (!wait_bar(&aempty[g], gph ^ 1, ctl, kSiteXformEmpty)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          tmem_st8(abuf + 0 + 8 * h, o0);
-          tmem_st8(abuf + 16 + 8 * h, o1);
-          tmem_st8(abuf + 32 + 8 * h, o2);
-          tmem_st8(abuf + 48 + 8 * h, o3);
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          // the E4M3 block scale of k-rows [32g + 16hh, +16): block row 2g + hh
+          uint32_t s0, s1, s2, s3;
+          const uint32_t sb = *reinterpret_cast<const uint32_t*>(
+              ssc + (t >> 6) * 1024 + (2 * g + hh) * 256 + 4 * (t & 63));
+          e4m3x4_to_bf16x2_dup(sb, s0, s1, s2, s3);
+          auto deq = [=](const uint8_t* r0, const uint8_t* r1, uint32_t& a0, uint32_t& a1,
+                         uint32_t& a2, uint32_t& a3) {
+            deq_fp4_rowpair(*reinterpret_cast<const uint16_t*>(r0),
+                            *reinterpret_cast<const uint16_t*>(r1), s0, s1, s2, s3, a0, a1, a2,
+                            a3);
+          };
+          ok = half(hh, rows, Cfg::kRowBytes, deq);
         }
       }
       if (!ok) break;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&afull[g]);
-        mbar_arrive(&empty[s]);
-      }
+      __syncwarp();  // every lane's shared-memory reads of the stage are done
+      if (lane == 0) mbar_arrive(&empty[s]);
       if (++s == Cfg::kStages) {
         s = 0;
         ph ^= 1;

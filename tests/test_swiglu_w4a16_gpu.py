@@ -183,3 +183,67 @@ def test_w4a16_all_eights_gives_the_ending_alone(cuda_lib):
     assert cuda_lib.gbf_check_device_error() == 0
     ref = oracle.w4a16(A, Wq, s, G, C, bias, M=M, N=N, K=K, alpha=1.0, beta=2.0, act="silu")
     assert_parity(down(out), ref, "all eights")
+
+
+@pytest.mark.parametrize("scales", ["small", "large", "mixed", "tiny_and_negative"])
+def test_w4a16_dequantised_operand_is_bit_exact(cuda_lib, scales):
+    # One-hot activation rows pick single k-rows, so out[m][n] is the
+    # dequantised weight bf16((q - 8) * s) itself (one non-zero product, exact
+    # in fp32).  Every code appears in those rows, with scales of general
+    # mantissas: below 2^-5 (the kernel's fused multiply-add path), above it
+    # (the separate subtract and multiply), both within one warp's columns,
+    # and negative and subnormal ones.  The result must equal the oracle's
+    # dequantised weight bit for bit.
+    M, N, K, G = 16, 1024, 512, 128
+    rng = np.random.Generator(np.random.PCG64(77))
+    Wq = rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+    ks = np.array([0, 1, 63, 64, 127, 128, 200, 255, 256, 300, 383, 384, 450, 500, 510, 511])
+    for i, k in enumerate(ks):  # every byte value appears in the picked rows
+        Wq[k, :256] = np.arange(256, dtype=np.uint8)
+    if scales == "small":
+        sv = rng.uniform(0.001, 0.031, size=(K // G, N))
+    elif scales == "large":
+        sv = rng.uniform(0.04, 3.0, size=(K // G, N))
+    elif scales == "mixed":
+        sv = rng.uniform(0.001, 0.031, size=(K // G, N))
+        sv[:, ::37] = rng.uniform(0.04, 3.0, size=sv[:, ::37].shape)
+    else:
+        sv = rng.uniform(-0.03, 0.03, size=(K // G, N))
+        sv[:, ::11] = np.float32(3e-39)  # bf16 subnormal scales
+    s = workloads.to_bf16_bits(sv.astype(np.float32))
+    A = np.zeros((M, K), dtype=np.uint16)
+    A[np.arange(M), ks] = 0x3F80  # 1.0
+    out = poison_bf16(M, N)
+    cuda_lib.w4a16_gemm(up(A), up(Wq), up(s), G, None, None, None, out, M, N, K)
+    assert cuda_lib.gbf_check_device_error() == 0
+    w = oracle.bf16_bits_to_f64(oracle.dequant_int4(Wq, s, G, K=K, N=N)[ks])
+    got = oracle.bf16_bits_to_f64(down(out))
+    # weights that are themselves bf16 subnormals are left out of the bit-wise
+    # comparison (what the tensor cores do with subnormal operands is not the
+    # dequantisation's concern); subnormal scales still feed normal weights
+    normal = (w == 0) | (np.abs(w) >= 2.0 ** -126)
+    assert normal.mean() > 0.9
+    assert np.array_equal(got[normal], w[normal])
+
+
+@pytest.mark.parametrize("scales", ["small", "large"])
+def test_fp8_dequantised_operand_is_bit_exact(cuda_lib, scales):
+    # As above for FP8 weights: scales below 2^8 take the fused multiply,
+    # larger ones the two-step one.
+    M, N, K, G = 16, 512, 256, 128
+    rng = np.random.Generator(np.random.PCG64(78))
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    Wq = rng.choice(codes, size=(K, N)).astype(np.uint8)
+    ks = np.arange(0, K, K // M)
+    sv = (rng.uniform(0.001, 200.0, size=(K // G, N)) if scales == "small"
+          else rng.uniform(300.0, 3000.0, size=(K // G, N)))
+    s = workloads.to_bf16_bits(sv.astype(np.float32))
+    A = np.zeros((M, K), dtype=np.uint16)
+    A[np.arange(M), ks] = 0x3F80
+    out = poison_bf16(M, N)
+    cuda_lib.w8a16_fp8_gemm(up(A), up(Wq), up(s), G, None, None, None, out, M, N, K)
+    assert cuda_lib.gbf_check_device_error() == 0
+    w = oracle.dequant_wq("fp8", Wq, s, G, K=K, N=N)
+    got = down(out)
+    ok = np.isfinite(oracle.bf16_bits_to_f64(w[ks]))
+    assert np.array_equal(oracle.bf16_bits_to_f64(got)[ok], oracle.bf16_bits_to_f64(w[ks])[ok])
