@@ -5,7 +5,8 @@ The swapped kernel and the weight-only kernel split K across a cluster of
 
 - push: the output rows are shared out among the ranks, and each rank
   bulk-copies the other ranks' rows to them.
-- pull: for larger tiles, each rank loads the other partials of its chunks
+- pull: for larger tiles (the swapped kernel at M > 64, the weight-only
+  kernel at M > 16), each rank loads the other partials of its chunks
   through distributed shared memory.
 
 The split count normally follows from the shape, so these tests force every
@@ -36,7 +37,7 @@ def forced(cuda_lib):
 
 
 @pytest.mark.parametrize("splits", [2, 3, 4, 5, 6, 7, 8])
-@pytest.mark.parametrize("M", [1, 13, 16, 32, 64, 128])
+@pytest.mark.parametrize("M", [1, 13, 16, 32, 64, 100, 128])
 def test_swapped_gemm_every_split_count(cuda_lib, forced, M, splits):
     N, K = 264, 1024  # 3 weight tiles, the last one ragged; 16 K blocks
     A = rand_bf16(100 + M, (M, K))

@@ -104,7 +104,7 @@ def test_unfused_rejects_a_small_workspace(cuda_lib):
     assert st == 4
 
 
-@pytest.mark.parametrize("M", [8, 256, 512])
+@pytest.mark.parametrize("M", [8, 128, 256, 512])
 def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib, M):
     N, K = 256, 128
     A = rand_bf16(31, (M, K))
