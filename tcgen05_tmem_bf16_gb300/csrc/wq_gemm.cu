@@ -164,26 +164,29 @@ __device__ __forceinline__ void deq_rowpair(uint32_t x0, uint32_t x1, uint32_t c
 }
 
 // The same with one fused multiply-add per bf16x2 pair, for scales with
-// |s| < 2^-5.  (x & 0x000F000F) read as bf16x2 is the pair of subnormals
-// (q * 2^-133), exactly; with sp = s * 2^133 (exact: no overflow for such s)
-// and c = -8 s (exact), fma(q * 2^-133, sp, c) = q*s - 8*s computed exactly
-// and rounded once, i.e. bf16_rne((q - 8) * s) as the definition asks.
-// 12 instructions per k-row pair instead of 16.
+// |s| < 2^-5.  A bf16 bit pattern p < 0x100 (exponent field 0 or 1) has the
+// value p * 2^-133 exactly, so a nibble masked in place is already a bf16
+// multiple of q: bits 0-3 give q * 2^-133, bits 4-7 give q * 2^-129.  With
+// sp = s * 2^133 or s * 2^129 (exact: no overflow for such s) and c = -8 s
+// (exact), fma(nibble, sp, c) = q*s - 8*s computed exactly and rounded once,
+// i.e. bf16_rne((q - 8) * s) as the definition asks.  Regions 1 and 0 (low
+// and high nibble of byte 2t) are masked in place, regions 3 and 2 after
+// one shift by 8 (bits 8-15 of each half; the high half's upper byte that
+// the shift brings into the low half is masked off).  10 instructions per
+// k-row pair instead of 16.  sp0, sp2: s * 2^129; sp1, sp3: s * 2^133.
 __device__ __forceinline__ void deq_rowpair_fma(uint32_t x0, uint32_t x1, uint32_t sp0,
                                                 uint32_t sp1, uint32_t sp2, uint32_t sp3,
                                                 uint32_t c0, uint32_t c1, uint32_t c2,
                                                 uint32_t c3, uint32_t& o0, uint32_t& o1,
                                                 uint32_t& o2, uint32_t& o3) {
   asm("{\n\t"
-      ".reg .b32 x, t0, t1, t2, t3;\n\t"
+      ".reg .b32 x, y, t0, t1, t2, t3;\n\t"
       "prmt.b32 x, %4, %5, 0x5410;\n\t"
-      "shr.b32 t0, x, 4;\n\t"
-      "shr.b32 t2, x, 12;\n\t"
-      "shr.b32 t3, x, 8;\n\t"
-      "and.b32 t0, t0, 0x000F000F;\n\t"
+      "shr.b32 y, x, 8;\n\t"
+      "and.b32 t0, x, 0x00F000F0;\n\t"
       "and.b32 t1, x, 0x000F000F;\n\t"
-      "and.b32 t2, t2, 0x000F000F;\n\t"
-      "and.b32 t3, t3, 0x000F000F;\n\t"
+      "and.b32 t2, y, 0x00F000F0;\n\t"
+      "and.b32 t3, y, 0x000F000F;\n\t"
       "fma.rn.bf16x2 %0, t0, %6, %10;\n\t"
       "fma.rn.bf16x2 %1, t1, %7, %11;\n\t"
       "fma.rn.bf16x2 %2, t2, %8, %12;\n\t"
@@ -694,11 +697,13 @@ __global__ void __launch_bounds__(kW4Threads, 2)
         constexpr uint32_t kLimit = 0x3D00u;  // bf16 2^-5
         if (__all_sync(0xffffffffu, bf16_abs_below(s0, kLimit) && bf16_abs_below(s1, kLimit) &&
                                         bf16_abs_below(s2, kLimit) && bf16_abs_below(s3, kLimit))) {
-          // s * 2^133 = s * 2^126 * 2^7 (exact), and -8 s (exact)
-          constexpr uint32_t kPow126 = 0x7E807E80u, kPow7 = 0x43004300u, kMinus8 = 0xC100C100u;
-          const uint32_t p0 = bf16x2_mul(bf16x2_mul(s0, kPow126), kPow7);
+          // s * 2^129 for the high nibbles, s * 2^133 for the low ones
+          // (products of exact power-of-two factors), and -8 s (exact)
+          constexpr uint32_t kPow126 = 0x7E807E80u, kPow3 = 0x41004100u, kPow7 = 0x43004300u;
+          constexpr uint32_t kMinus8 = 0xC100C100u;
+          const uint32_t p0 = bf16x2_mul(bf16x2_mul(s0, kPow126), kPow3);
           const uint32_t p1 = bf16x2_mul(bf16x2_mul(s1, kPow126), kPow7);
-          const uint32_t p2 = bf16x2_mul(bf16x2_mul(s2, kPow126), kPow7);
+          const uint32_t p2 = bf16x2_mul(bf16x2_mul(s2, kPow126), kPow3);
           const uint32_t p3 = bf16x2_mul(bf16x2_mul(s3, kPow126), kPow7);
           const uint32_t c0 = bf16x2_mul(s0, kMinus8), c1 = bf16x2_mul(s1, kMinus8);
           const uint32_t c2 = bf16x2_mul(s2, kMinus8), c3 = bf16x2_mul(s3, kMinus8);
