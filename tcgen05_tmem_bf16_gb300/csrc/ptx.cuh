@@ -84,6 +84,18 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Prefetch of a 2-D tile into L2 (no shared-memory destination, no
+// completion).  L2 is where this GPU's accesses meet, so a later read sees
+// any write made after the prefetch: prefetching an operand that the
+// previous kernel may still be writing is safe, it only warms the cache.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0,
+                                                   int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // 2-D tiled store shared -> global (bulk async-group of this thread), with an
 // L2 eviction-priority policy.  Parts of the box outside the tensor are not
 // written.  c0 (the innermost coordinate) x element size must be a multiple
