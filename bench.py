@@ -833,7 +833,8 @@ def measure(name: str, args, dev, stream, peaks, peak_src, world: int, headline:
         achieved, peak, unit = ach_tf, tpeak, "TFLOP/s"
     else:
         achieved, peak, unit = ach_gb, peaks["hbm_gbs"], "GB/s"
-    kname = {"persistent": "gemm_persistent_kernel", "swap_splitk": "gemm_swap_kernel",
+    kname = {"persistent": "gemm_persistent_kernel", "persistent_splitk": "gemm_persistent_kernel",
+             "swap_splitk": "gemm_swap_kernel",
              "w4a16": "wq_gemm_kernel", "pair": "gemm_pair_kernel",
              "add_rmsnorm": "add_rmsnorm_kernel",
              "swiglu_pointwise": "swiglu_pointwise_kernel"}.get(wl.path, wl.path)

@@ -316,8 +316,10 @@ GBF_API gbf_status_t gbf_set_wait_timeout_ns(uint64_t ns);
  * Returns 1 = persistent 128x256-tile kernel, 2 = small-M swapped kernel
  * with cluster split-K (also the gate/up GEMM at M <= 32), 3 = weight-only
  * kernel (int4, FP8, NVFP4), 4 = persistent kernel on CTA pairs (chosen over 1
- * when its 512-row units fill the GPU better),
- * 0 = no launch (empty output), -1 = the arguments would be rejected.
+ * when its 512-row units fill the GPU better), 5 = the persistent kernel's
+ * split-K form (two CTAs per tile, chosen when the tiles fill at most half
+ * of the SMs), 0 = no launch (empty output), -1 = the arguments would be
+ * rejected.
  * `*splits` (may be NULL) receives the split-K cluster size.
  *
  * Kernels of families 2, 3 and 4 are launched with programmatic stream

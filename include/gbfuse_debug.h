@@ -38,10 +38,12 @@ GBF_API gbf_status_t gbf_debug_set_profile(void *counters, size_t bytes);
 GBF_API gbf_status_t gbf_debug_force_splits(int splits);
 
 /* Tuning hook: for the dense product (and the gate/up GEMM) at M above the
- * swapped kernel's range, run the persistent kernel (1) or the CTA-pair
- * kernel (4) for later launches instead of the automatic choice (0, the
- * default).  Other values return GBF_ERR_INVALID_ARG.  Changes which kernel
- * computes the result, not the result beyond the order of rounding. */
+ * swapped kernel's range, run the persistent kernel (1), its split-K form
+ * over two CTAs per tile (5; the single product only, the gate/up GEMM takes
+ * 1) or the CTA-pair kernel (4) for later launches instead of the automatic
+ * choice (0, the default).  Other values return GBF_ERR_INVALID_ARG.
+ * Changes which kernel computes the result, not the result beyond the order
+ * of rounding. */
 GBF_API gbf_status_t gbf_debug_force_path(int path);
 
 #ifdef __cplusplus

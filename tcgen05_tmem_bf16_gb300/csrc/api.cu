@@ -341,14 +341,29 @@ GemmPlan pair_plan(int64_t M, int64_t N, bool dual, bool kn, const DeviceInfo& d
 }
 
 // The one-SM persistent kernel: 128 x 256 tiles (128 x 128 of each product
-// for the gate/up GEMM).
-GemmPlan persistent_plan(int64_t M, int64_t N, bool dual, const DeviceInfo& dev) {
+// for the gate/up GEMM).  When the tiles fill at most half of the SMs, the
+// single product runs in its split-K form instead: a cluster of two CTAs per
+// tile, each over half of K (`split` true; needs enough K blocks to pay for
+// the exchange of the partial sums).
+GemmPlan persistent_plan(int64_t M, int64_t N, int64_t K, bool dual, bool split,
+                         const DeviceInfo& dev) {
   GemmPlan p;
   p.path = kPathPersistent;
   p.m_tiles = ceil_div(M, kBM);
   p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
+  p.num_kb = ceil_div(K, kBK);
   p.grid = std::min(p.m_tiles * p.n_tiles, std::max(1, dev.sms));
+  if (split && !dual && p.num_kb >= 2) {
+    p.path = kPathPersistentSplit;
+    p.splits = 2;
+    p.grid = 2 * p.m_tiles * p.n_tiles;
+  }
   return p;
+}
+
+bool split_pays(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo& dev) {
+  const int64_t tiles = static_cast<int64_t>(ceil_div(M, kBM)) * ceil_div(N, kPersistBN);
+  return !dual && 2 * tiles <= dev.sms && ceil_div(K, kBK) >= 8;
 }
 
 // Relative time of a plan: rounds of units times the MMA area of a unit per
@@ -357,6 +372,8 @@ GemmPlan persistent_plan(int64_t M, int64_t N, bool dual, const DeviceInfo& dev)
 // about 0.8 of the rate of the pair kernel's two streams (measured: ~8.7
 // against ~11 TFLOP/s per SM).
 double plan_time(const GemmPlan& p, bool dual, const DeviceInfo& dev) {
+  if (p.path == kPathPersistentSplit)  // one round, half of K per SM, plus the exchange
+    return 0.55 * 128.0 * 256.0 / 0.8;
   if (p.path == kPathPair) {
     const int64_t units = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
     const int64_t rounds = (units + dev.pairs - 1) / dev.pairs;
@@ -394,9 +411,10 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const De
   // time (the pair kernel's 512-row units leave most SMs idle when there are
   // few of them), unless a tuning hook forces one.
   const int force = g_force_path.load();
-  GemmPlan pp = persistent_plan(M, N, dual, dev);
-  pp.num_kb = ceil_div(K, kBK);
-  if (dev.pairs <= 0 || force == kPathPersistent) return pp;
+  if (force == kPathPersistentSplit && !dual) return persistent_plan(M, N, K, dual, true, dev);
+  if (force == kPathPersistent) return persistent_plan(M, N, K, dual, false, dev);
+  GemmPlan pp = persistent_plan(M, N, K, dual, split_pays(M, N, K, dual, dev), dev);
+  if (dev.pairs <= 0) return pp;
   GemmPlan qp = pair_plan(M, N, dual, kn, dev);
   qp.num_kb = pp.num_kb;
   if (force == kPathPair) return qp;
@@ -832,7 +850,8 @@ gbf_status_t gbf_debug_force_splits(int splits) {
 }
 
 gbf_status_t gbf_debug_force_path(int path) {
-  if (path != 0 && path != kPathPersistent && path != kPathPair) return GBF_ERR_INVALID_ARG;
+  if (path != 0 && path != kPathPersistent && path != kPathPair && path != kPathPersistentSplit)
+    return GBF_ERR_INVALID_ARG;
   g_force_path.store(path);
   return GBF_OK;
 }

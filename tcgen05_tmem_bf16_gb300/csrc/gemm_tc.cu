@@ -61,7 +61,16 @@ struct PersistArgs {
   KernelCtl ctl;
 };
 
-template <bool W_KN, bool DUAL>
+// Split-K form (SPLIT): a cluster of two CTAs computes one tile, each over
+// half of the K range; each then parks the partial sums of the other CTA's
+// half of the columns in its (now idle) stage memory as [column][row] fp32
+// (64 KB), sends them to that CTA with bulk copies, and applies the ending
+// to its own 128 columns as rank 0's partial + rank 1's partial.
+constexpr int kPSplitHalf = kPersistBN / 2;                     // columns each rank finishes
+constexpr int kPSplitBytes = kPSplitHalf * kBM * 4;             // 64 KB of fp32 partials
+static_assert(2 * kPSplitBytes <= kPStages * kPStageBytes, "partials fit in the ring");
+
+template <bool W_KN, bool DUAL, bool SPLIT>
 __global__ void __launch_bounds__(kPThreads, 1)
     gemm_persistent_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmW,
@@ -75,12 +84,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* tfull = empty + kPStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* recvb = done + 1;  // split-K: the peer's partial sums have landed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(recvb + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   uint8_t* staging = smem + kPStages * kPStageBytes + kPBarBytes;  // 1024-aligned
+  static_assert(!(SPLIT && DUAL), "split-K form for the single product only");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // split-K: rank r of the cluster takes k blocks [kb0, kb1) of its cluster's tile
+  const uint32_t rank = SPLIT ? (cluster_ctarank() & 1u) : 0u;
+  const int tile0 = SPLIT ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = SPLIT ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int kb0 = SPLIT ? static_cast<int>((static_cast<int64_t>(rank) * a.num_kb) / 2) : 0;
+  const int kb1 =
+      SPLIT ? static_cast<int>((static_cast<int64_t>(rank + 1) * a.num_kb) / 2) : a.num_kb;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
@@ -92,6 +110,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&tempty[i], 8);  // one arrive per epilogue warp
     }
     mbar_init(done, 1);
+    if (SPLIT) {
+      mbar_init(recvb, 1);
+      mbar_arrive_expect_tx(recvb, kPSplitBytes);  // the peer's 128 x 128 partials
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -105,13 +127,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (SPLIT) cluster_sync_all();  // both CTAs' barriers exist before any copy between them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
   const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
   const long long t_start = clock64();
   const int num_tiles = a.m_tiles * a.n_tiles;
-  const int num_kb = a.num_kb;
   const int out_bn = DUAL ? 128 : 256;
 
   if (warp == 0) {
@@ -123,10 +145,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = tile0; t < num_tiles && ok; t += tile_step) {
         int mb, nb;
         tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -175,13 +197,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       uint32_t ph = 0;
       int local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+      for (int t = tile0; t < num_tiles && ok; t += tile_step, ++local) {
         const int buf = local & 1;
         const uint32_t aph = (local >> 1) & 1;
         if (!wait_bar(&tempty[buf], aph ^ 1, ctl, kSiteMmaAccEmpty)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * 256;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
             ok = false;
             break;
@@ -194,7 +216,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = W_KN ? sdesc_sw128(b0 + k * 2048, 8192, 1024)
                                      : sdesc_sw128(b0 + k * 32, 16, 1024);
-            mma_ss(d, ad, bd, idesc, (kb | k) != 0);
+            mma_ss(d, ad, bd, idesc, (kb > kb0 || k != 0) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
           if (++s == kPStages) {
@@ -209,7 +231,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       wait_bar(done, 0, ctl, kSiteDrain, false);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (!SPLIT && warp >= 4) {
     // ------------------------------------------------------------ epilogue
     // Warps 4-7 and 8-11 read the same TMEM lanes (warp % 4 selects the lane
     // quarter); the first warpgroup takes the left half of the tile's
@@ -222,7 +244,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     uint8_t* my_staging = staging + (warp - 4) * 2 * kStageChunkBytes;
     int flip = 0;
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+    for (int t = tile0; t < num_tiles; t += tile_step, ++local) {
       int mb, nb;
       tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
       const int buf = local & 1;
@@ -261,6 +283,86 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // every staged chunk written to global memory before the CTA may exit
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
+  }
+
+  if constexpr (SPLIT) {
+    // ------------------------------------------------------------ split-K exchange + ending
+    // (one tile per cluster: the launch has two CTAs per tile)
+    const bool epi = warp >= 4;
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;      // warpgroup: chunks 2*half, 2*half + 1 of a half-tile
+    const int rl = q * 32 + lane;          // row within the tile = TMEM lane
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);  // accumulator 0
+    float* park = reinterpret_cast<float*>(stages);                 // [column][row], 64 KB
+    float* recv = reinterpret_cast<float*>(stages + kPSplitBytes);  // the peer's, same layout
+    const int t = tile0;
+    int mb = 0, nb = 0;
+    if (t < num_tiles) tile_coords(t, a.m_tiles, a.n_tiles, mb, nb);
+    const uint64_t pol = l2_evict_first_policy();
+    const int64_t row = static_cast<int64_t>(mb) * kBM + rl;
+    const int mine = static_cast<int>(rank) * kPSplitHalf;       // first column this rank finishes
+    const int theirs = kPSplitHalf - mine;                       // the peer's first column
+    if (epi) {
+      wait_bar(&tfull[0], 0, ctl, kSiteEpiAccFull);
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
+        uint32_t v[32];
+        tmem_ld32(tb + theirs + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) park[(c * 32 + j) * kBM + rl] = __uint_as_float(v[j]);
+      }
+      fence_proxy_async_smem();  // the bulk copies read what these threads wrote
+    }
+    cluster_sync_all();  // both ranks parked
+    if (threadIdx.x == 128) {
+      const uint32_t peer = rank ^ 1u;
+      constexpr int kPiece = kPSplitBytes / 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        bulk_copy_to_peer(mapa_shared(smem_u32(stages + kPSplitBytes + i * kPiece), peer),
+                          smem_u32(stages + i * kPiece), kPiece,
+                          mapa_shared(smem_u32(recvb), peer));
+    }
+    if (epi) {
+      uint8_t* my_staging = staging + (warp - 4) * 2 * kStageChunkBytes;
+      int flip = 0;
+      // not cut short by the abort flag: the peer sends whatever its state
+      wait_bar(recvb, 0, ctl, kSiteEpiAccFull, /*honor_abort=*/false);
+      RowLoads L;
+      epi_row_prefetch(L, row, nb * 256 + mine + 2 * half * 32, a.M, a.N, a.ep, pol);
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
+        const int col0 = nb * 256 + mine + c * 32;
+        uint32_t own[32], sum[32];
+        tmem_ld32(tb + mine + c * 32, own);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float o = __uint_as_float(own[j]);
+          const float p = recv[(c * 32 + j) * kBM + rl];
+          // rank 0's partial first, in both ranks
+          sum[j] = __float_as_uint(rank == 0 ? o + p : p + o);
+        }
+        const RowLoads cur = L;
+        if (cc == 0) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep, pol);
+        uint32_t w[16];
+        switch (a.ep.act) {
+          case kActRelu: epi_row32_pack<kActRelu, false>(sum, sum, cur, a.ep, w); break;
+          case kActSilu: epi_row32_pack<kActSilu, false>(sum, sum, cur, a.ep, w); break;
+          case kActGeluTanh: epi_row32_pack<kActGeluTanh, false>(sum, sum, cur, a.ep, w); break;
+          default: epi_row32_pack<kActIdentity, false>(sum, sum, cur, a.ep, w); break;
+        }
+        if (t < num_tiles) store_chunk32(my_staging, flip, w, &tmO, row - lane, col0, a.M, a.N, pol);
+      }
+      if (lane == 0) bulk_wait<0>();
+      __syncwarp();
+    }
+    // no rank leaves while copies into or out of its shared memory may be in flight
+    cluster_sync_all();
   }
 
   if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
@@ -751,11 +853,35 @@ cudaError_t run_persistent(const GemmPlan& p, const CUtensorMap& tmA, const CUte
                            const CUtensorMap& tmW2, const CUtensorMap& tmO,
                            const PersistArgs& args, cudaStream_t stream) {
   static std::atomic<uint64_t> mask{0};
-  auto kernel = gemm_persistent_kernel<W_KN, DUAL>;
+  auto kernel = gemm_persistent_kernel<W_KN, DUAL, false>;
   cudaError_t e = ensure_smem_attr(kernel, kPSmem, mask);
   if (e != cudaSuccess) return e;
   kernel<<<p.grid, kPThreads, kPSmem, stream>>>(tmA, tmW, tmW2, tmO, args);
   return cudaGetLastError();
+}
+
+// Split-K form: clusters of two CTAs, one cluster per tile.
+template <bool W_KN>
+cudaError_t run_persistent_split(const GemmPlan& p, const CUtensorMap& tmA,
+                                 const CUtensorMap& tmW, const CUtensorMap& tmO,
+                                 const PersistArgs& args, cudaStream_t stream) {
+  static std::atomic<uint64_t> mask{0};
+  auto kernel = gemm_persistent_kernel<W_KN, false, true>;
+  cudaError_t e = ensure_smem_attr(kernel, kPSmem, mask);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid, 1, 1);
+  cfg.blockDim = dim3(kPThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmW, tmW, tmO, args);
 }
 
 template <int MPAD, bool W_KN, bool DUAL>
@@ -811,6 +937,11 @@ cudaError_t launch_gemm(const GemmPlan& plan, bool w_kn, bool dual, const CUtens
                         const CUtensorMap& tmW, const CUtensorMap& tmW2, const CUtensorMap& tmO,
                         const EpiParams& ep, int M, int N, int K, const KernelCtl& ctl,
                         cudaStream_t stream) {
+  if (plan.path == kPathPersistentSplit && !dual) {
+    PersistArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
+    return w_kn ? run_persistent_split<true>(plan, tmA, tmW, tmO, args, stream)
+                : run_persistent_split<false>(plan, tmA, tmW, tmO, args, stream);
+  }
   if (plan.path == kPathPersistent) {
     PersistArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
     if (w_kn)

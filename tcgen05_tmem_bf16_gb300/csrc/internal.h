@@ -32,7 +32,14 @@ struct KernelCtl {
 constexpr int kProfSlots = 32;  // [2*site] cycles waited, [2*site+1] waits; [31] CTA cycles
 
 // Kernel families (gbf_kernel_path codes).
-enum Path { kPathNone = 0, kPathPersistent = 1, kPathSwap = 2, kPathW4 = 3, kPathPair = 4 };
+enum Path {
+  kPathNone = 0,
+  kPathPersistent = 1,
+  kPathSwap = 2,
+  kPathW4 = 3,
+  kPathPair = 4,
+  kPathPersistentSplit = 5,  // the one-SM persistent kernel, K split over a CTA pair per tile
+};
 
 struct GemmPlan {
   int path = kPathNone;

@@ -84,9 +84,13 @@ def test_workspace_sizes(lib):
 
 def test_kernel_path_planning(lib):
     assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096) == ("pair", 1)
-    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096) == ("persistent", 1)
-    # mid-size M: the pair kernel's 512 x 256 units would leave most SMs idle
-    assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 4096) == ("persistent", 1)
+    # mid-size M: the pair kernel's 512 x 256 units would leave most SMs idle,
+    # and 128 x 256 tiles fill at most half of them: two CTAs per tile (split K)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096) == ("persistent_splitk", 2)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 4096) == ("persistent_splitk", 2)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 4096, 4096) == ("persistent", 1)
+    # too little K to pay for the exchange of the partial sums
+    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 256) == ("persistent", 1)
     assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 8192, 8192, "kn") == ("pair", 1)
     path, splits = gbf.gbf_kernel_path("gemm_epilogue", 16, 8192, 8192, "kn")
     assert path == "swap_splitk" and 1 <= splits <= 8
@@ -159,7 +163,11 @@ def test_force_path_hook(lib):
 
 @pytest.mark.parametrize("op,M,N,K,layout,want", [
     # measured on a GB300 with both kernels forced (TFLOP/s pair / one-SM):
-    ("gemm_epilogue", 512, 4096, 4096, "nk", "persistent"),    # 414 / 644
+    # the one-SM kernel's split-K form when its tiles fill at most half of the
+    # SMs (same box, pair / one-SM / split: 410 / 526 / 737; 256 x 8192^2
+    # 428 / 620 / 913)
+    ("gemm_epilogue", 512, 4096, 4096, "nk", "persistent_splitk"),
+    ("gemm_epilogue", 256, 8192, 8192, "kn", "persistent_splitk"),
     ("gemm_epilogue", 1024, 4096, 4096, "nk", "persistent"),   # 812 / 1112
     ("gemm_epilogue", 1536, 4096, 4096, "nk", "pair"),         # 1203 / 956
     ("gemm_epilogue", 4096, 4096, 4096, "nk", "pair"),         # 1595 / 1354

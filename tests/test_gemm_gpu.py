@@ -77,6 +77,42 @@ def test_persistent_kernel(cuda_lib, layout, M, N, K):
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,N,K", [(129, 136, 72), (300, 520, 1000), (511, 264, 200),
+                                   (1030, 1048, 136), (1300, 2056, 256), (256, 4096, 4096)])
+def test_persistent_splitk_kernel(cuda_lib, layout, M, N, K):
+    # two CTAs per tile, each over half of K (ragged halves included), the
+    # partial sums of the other CTA's 128 columns exchanged by bulk copies;
+    # more clusters than fit at once in the last case but one
+    run_and_check(cuda_lib, M, N, K, layout, "gelu_tanh", 0.75, -0.5, seed=M + 5 * N + K,
+                  expect_path="persistent_splitk", force_path="persistent_splitk")
+
+
+@pytest.mark.parametrize("act", ["identity", "relu", "silu", "gelu_tanh"])
+@pytest.mark.parametrize("opts", [(False, False, False), (True, True, True)])
+def test_persistent_splitk_every_ending(cuda_lib, act, opts):
+    c, bias, res = opts
+    run_and_check(cuda_lib, 200, 392, 384, "nk", act, 1.25, 0.5, seed=33, c=c, bias=bias,
+                  res=res, expect_path="persistent_splitk", force_path="persistent_splitk")
+
+
+def test_persistent_splitk_in_place_residual(cuda_lib):
+    M, N, K = 300, 264, 512
+    A, B, C, bi, r = case(M, N, K, "nk", 810)
+    out = up(r)  # residual == out
+    assert cuda_lib.gbf_debug_force_path("persistent_splitk") == 0
+    try:
+        assert cuda_lib.gbf_kernel_path("gemm_epilogue", M, N, K, "nk")[0] == "persistent_splitk"
+        cuda_lib.gemm_epilogue(up(A), up(B), "nk", up(C), up(bi), out, out, M, N, K, 0.5, 1.0,
+                               "silu")
+    finally:
+        cuda_lib.gbf_debug_force_path(None)
+    assert cuda_lib.gbf_check_device_error() == 0
+    ref = oracle.gemm_epilogue(A, B, "nk", C, bi, r, M=M, N=N, K=K, alpha=0.5, beta=1.0,
+                               act="silu")
+    assert_parity(down(out), ref, "split-K in-place residual")
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("M,N,K", [(512, 256, 64), (515, 264, 256), (1030, 1048, 136),
                                    (777, 520, 328), (2048, 1024, 512), (129, 264, 128),
                                    (300, 520, 200), (400, 1048, 136)])
