@@ -318,7 +318,8 @@ GBF_API gbf_status_t gbf_set_wait_timeout_ns(uint64_t ns);
  * kernel (int4, FP8, NVFP4), 4 = persistent kernel on CTA pairs (chosen over 1
  * when its 512-row units fill the GPU better), 5 = the persistent kernel's
  * split-K form (two CTAs per tile, chosen when the tiles fill at most half
- * of the SMs), 0 = no launch (empty output), -1 = the arguments would be
+ * of the SMs), 6 = the CTA-pair kernel with one MMA stream (units of 256
+ * rows), 0 = no launch (empty output), -1 = the arguments would be
  * rejected.
  * `*splits` (may be NULL) receives the split-K cluster size.
  *

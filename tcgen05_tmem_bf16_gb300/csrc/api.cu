@@ -237,7 +237,7 @@ gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, 
   const GemmPlan plan = plan_gemm(M, N, K, dual, kn, dev);
   CUtensorMap tmA, tmW, tmW2;
   const uint32_t a_rows = plan.path == kPathSwap ? plan.mpad : kBM;
-  const bool pair = plan.path == kPathPair;
+  const bool pair = plan.path == kPathPair || plan.path == kPathPairOne;
   if (!tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, kBK, a_rows,
                CU_TENSOR_MAP_SWIZZLE_128B))
     return GBF_ERR_CUDA;
@@ -315,13 +315,21 @@ gbf_status_t check_nvfp4(int64_t M, int64_t N, int64_t K, int act) {
 namespace {
 
 // The CTA-pair kernel: pairs of 256-row M-tiles share each B tile (a unit of
-// 512 x bn per pair of SMs), persistent over the units.
-GemmPlan pair_plan(int64_t M, int64_t N, bool dual, bool kn, const DeviceInfo& dev) {
+// 512 x bn per pair of SMs), persistent over the units.  With one stream
+// (single product only) a unit is one 256-row M-tile x 256 columns.
+GemmPlan pair_plan(int64_t M, int64_t N, bool dual, bool kn, const DeviceInfo& dev,
+                   int streams = 2) {
   GemmPlan p;
   p.path = kPathPair;
   p.m_tiles = ceil_div(M, 2 * kBM);
   p.n_tiles = ceil_div(N, dual ? 128 : kPersistBN);
   p.bn = 256;
+  if (streams == 1 && !dual) {
+    p.path = kPathPairOne;
+    p.streams = 1;
+    p.grid = 2 * std::min(p.m_tiles * p.n_tiles, dev.pairs);
+    return p;
+  }
   if (!dual && !kn) {
     // A 224-wide tile when it wastes less of the last round of tiles:
     // compare useful area / (rounds * pairs * tile area).
@@ -379,6 +387,11 @@ double plan_time(const GemmPlan& p, bool dual, const DeviceInfo& dev) {
     const int64_t rounds = (units + dev.pairs - 1) / dev.pairs;
     return static_cast<double>(rounds) * 512.0 * (dual ? 256 : p.bn) / 2.0;
   }
+  if (p.path == kPathPairOne) {  // one MMA stream: about 0.9 of the two streams' rate
+    const int64_t units = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int64_t rounds = (units + dev.pairs - 1) / dev.pairs;
+    return static_cast<double>(rounds) * 256.0 * p.bn / 2.0 / 0.9;
+  }
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   const int64_t rounds = (tiles + std::max(1, dev.sms) - 1) / std::max(1, dev.sms);
   return static_cast<double>(rounds) * 128.0 * 256.0 / 0.8;
@@ -418,7 +431,14 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const De
   GemmPlan qp = pair_plan(M, N, dual, kn, dev);
   qp.num_kb = pp.num_kb;
   if (force == kPathPair) return qp;
-  return plan_time(qp, dual, dev) < plan_time(pp, dual, dev) ? qp : pp;
+  GemmPlan best = plan_time(qp, dual, dev) < plan_time(pp, dual, dev) ? qp : pp;
+  if (!dual) {
+    GemmPlan op = pair_plan(M, N, dual, kn, dev, 1);
+    op.num_kb = pp.num_kb;
+    if (force == kPathPairOne) return op;
+    if (plan_time(op, dual, dev) < plan_time(best, dual, dev)) best = op;
+  }
+  return best;
 }
 
 GemmPlan plan_w4a16(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
@@ -850,7 +870,8 @@ gbf_status_t gbf_debug_force_splits(int splits) {
 }
 
 gbf_status_t gbf_debug_force_path(int path) {
-  if (path != 0 && path != kPathPersistent && path != kPathPair && path != kPathPersistentSplit)
+  if (path != 0 && path != kPathPersistent && path != kPathPair && path != kPathPersistentSplit &&
+      path != kPathPairOne)
     return GBF_ERR_INVALID_ARG;
   g_force_path.store(path);
   return GBF_OK;

@@ -47,8 +47,7 @@
 
 namespace gbf {
 
-constexpr int kQStages = 4;
-constexpr int kQStreams = 2;                   // MMA streams = M-tiles per stage
+
 // Raster group of M-tile pairs: the ~152 tiles in flight then span about 16
 // M-tiles x 9 N-tiles, whose A and B panels (K = 8192: 64 + 40 MB) stay in L2.
 constexpr int kQGroup = 8;
@@ -59,18 +58,28 @@ constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
 // Tile width BN (MMA N) of the pair: 256, or 224 when that fills the last
 // round of tiles better (the planner picks it for K-contiguous weights).
 // Each CTA holds BN/2 rows of the B tile.
-template <int BN>
+//
+// STREAMS: M-tiles of 256 rows per unit of work.  Two (the default): a unit
+// is an M-tile pair whose two tiles share each B tile and are computed by two
+// MMA streams into the two accumulators.  One: a unit is one M-tile, a
+// single MMA stream alternates between the two accumulators so that the
+// ending of a tile overlaps the main loop of the next; twice as many units
+// of half the size, for shapes whose M-tile pairs are fewer than the SM pairs.
+template <int BN, int STREAMS = 2>
 struct PairCfg {
+  static constexpr int kStreams = STREAMS;
   static constexpr int kBBytes = (BN / 2) * kBK * 2;
-  static constexpr int kStageBytes = kQStreams * kQABytes + kBBytes;  // A0 | A1 | B
+  static constexpr int kStageBytes = STREAMS * kQABytes + kBBytes;  // A0 (| A1) | B
+  static constexpr int kStages = STREAMS == 2 ? 4 : 6;
   // ring | barriers (1 KB) | output staging: 8 epilogue warps x 2 buffers of 2 KB
   static constexpr int kBarBytes = 1024;
   static constexpr int kStagingBytes = 8 * 2 * kStageChunkBytes;
-  static constexpr int kSmem = 1024 + kQStages * kStageBytes + kBarBytes + kStagingBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kStagingBytes;
   static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   static constexpr int kChunks = BN / 32;             // 32-column epilogue chunks
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN <= 256, "tile width");
+  static_assert(STREAMS == 1 || STREAMS == 2, "one or two streams");
 };
 
 struct PairArgs {
@@ -86,12 +95,14 @@ __device__ __forceinline__ void settle_after_abort() {
   while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
 }
 
-template <bool W_KN, bool DUAL, int BN>
+template <bool W_KN, bool DUAL, int BN, int STREAMS>
 __global__ void __launch_bounds__(kQThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmO,
                      const PairArgs a) {
-  using Cfg = PairCfg<BN>;
+  using Cfg = PairCfg<BN, STREAMS>;
+  constexpr int kQStages = Cfg::kStages;
+  constexpr int kQStreams = Cfg::kStreams;
   static_assert(!(W_KN || DUAL) || BN == 256, "narrow tiles only for K-contiguous single B");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -117,7 +128,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kQStreams);  // both issuers' commits
     }
-    for (int i = 0; i < kQStreams; ++i) {
+    for (int i = 0; i < 2; ++i) {  // the two accumulators
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 16);  // 8 epilogue warps in each CTA of the pair
     }
@@ -140,8 +151,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   const WaitCtl ctl{a.ctl.err, a.ctl.timeout_ns, abort_flag, prof_slots(a.ctl.prof)};
   const long long t_start = clock64();
-  const int m_pairs = (a.m_tiles + 1) / 2;      // M-tile pairs (the last may be half empty)
-  const int num_super = m_pairs * a.n_tiles;     // a super tile = an M-tile pair x one N-tile
+  // units: STREAMS M-tiles (the last unit's second tile may be empty) x one N-tile
+  const int m_pairs = (a.m_tiles + kQStreams - 1) / kQStreams;
+  const int num_super = m_pairs * a.n_tiles;
   const int num_kb = a.num_kb;
   const int out_bn = DUAL ? 128 : BN;
   if (threadIdx.x == 0) griddep_launch_dependents();
@@ -173,7 +185,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
           for (int i = 0; i < kQStreams; ++i)  // rows past M read as zeros
             tma_load_2d_pair(sa + i * kQABytes, &tmA, bar, kb * kBK,
-                             (2 * mp + i) * kQTileM + static_cast<int>(rank) * kBM);
+                             (kQStreams * mp + i) * kQTileM + static_cast<int>(rank) * kBM);
           const CUtensorMap* wmap = (DUAL && rank) ? &tmW2 : &tmW;
           const int n0 = DUAL ? nb * 128 : nb * BN + static_cast<int>(rank) * (BN / 2);
           if constexpr (W_KN) {
@@ -200,19 +212,23 @@ __global__ void __launch_bounds__(kQThreads, 1)
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers (even CTA)
-    // warp 1 lane 0 issues stream 0 (the pair's even M-tile), warp 2 lane 0
-    // stream 1 (the odd one) from the same stages; warp 2 also allocates and
-    // frees the tensor memory, outside this loop
-    if (lane == 0 && leader) {
+    // The pair's tiles in order l = 0, 1, ...: tile l is M-tile l % STREAMS
+    // of unit l / STREAMS, accumulated in accumulator l & 1.  With two streams
+    // warp 1 lane 0 issues the even tiles and warp 2 lane 0 the odd ones from
+    // the same stages (each stream keeps its accumulator); with one stream
+    // warp 1 issues every tile, alternating accumulators.  Warp 2 also
+    // allocates and frees the tensor memory, outside this loop.
+    const int st = warp - 1;
+    if (lane == 0 && leader && st < kQStreams) {
       constexpr uint32_t idesc = idesc_bf16(kQTileM, BN, false, W_KN);
-      const int st = warp - 1;
-      const uint32_t d = tmem_base + st * 256;
       int s = 0;
       uint32_t ph = 0;
-      int local = 0;
+      int l = st;
       bool ok = true;
-      for (int t = pair; t < num_super && ok; t += npairs, ++local) {
-        if (!wait_bar(&tempty[st], (local & 1) ^ 1, ctl, kSiteMmaAccEmpty)) break;
+      for (int t = pair; t < num_super && ok; t += npairs, l += kQStreams) {
+        const int acc = l & 1;
+        const uint32_t d = tmem_base + acc * 256;
+        if (!wait_bar(&tempty[acc], ((l >> 1) & 1) ^ 1, ctl, kSiteMmaAccEmpty)) break;
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
         }
         if (!ok) break;
-        if (!(a.ctl.inject && st == 0 && local == 0)) mma_commit_pair(&tfull[st], 0x3);
+        if (!(a.ctl.inject && l == 0)) mma_commit_pair(&tfull[acc], 0x3);
       }
       mma_commit_pair(done, 0x1);
       wait_bar(done, 0, ctl, kSiteDrain, false);
@@ -254,17 +270,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
     constexpr int kFirst = (kChunks + 1) / 2;  // chunks of warpgroup 0; the rest go to 1
     const int c_begin = half == 0 ? 0 : kFirst;
     const int c_end = half == 0 ? kFirst : kChunks;
-    const uint32_t tempty_leader[kQStreams] = {mapa_shared(smem_u32(&tempty[0]), 0),
-                                               mapa_shared(smem_u32(&tempty[1]), 0)};
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
+                                       mapa_shared(smem_u32(&tempty[1]), 0)};
     uint8_t* my_staging = staging + (warp - 4) * 2 * kStageChunkBytes;
     int flip = 0;
-    // tile l of the pair: super tile pair + (l / 2) * npairs, M-tile l % 2 of it
+    // tile l of the pair: unit pair + (l / STREAMS) * npairs, M-tile l % STREAMS
+    // of it, in accumulator l & 1 (use (l >> 1) of that accumulator)
     for (int local = 0; pair + (local / kQStreams) * npairs < num_super; ++local) {
-      const int st = local % kQStreams;
+      const int st = local & 1;  // accumulator
       int mp, nb;
       tile_coords(pair + (local / kQStreams) * npairs, m_pairs, a.n_tiles, mp, nb, kQGroup);
-      const int mb = 2 * mp + st;
-      const uint32_t aph = (local / kQStreams) & 1;
+      const int mb = kQStreams * mp + local % kQStreams;
+      const uint32_t aph = (local >> 1) & 1;
       const int64_t row =
           static_cast<int64_t>(mb) * kQTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
       epi_row_l2_prefetch(row, nb * out_bn + c_begin * 32, nb * out_bn + c_end * 32, a.M, a.N,
@@ -318,13 +335,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 namespace {
 
-template <bool W_KN, bool DUAL, int BN>
+template <bool W_KN, bool DUAL, int BN, int STREAMS = 2>
 cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
                      const CUtensorMap& tmW2, const CUtensorMap& tmO, const PairArgs& args,
                      cudaStream_t stream) {
   static std::atomic<uint64_t> mask{0};
-  auto kernel = gemm_pair_kernel<W_KN, DUAL, BN>;
-  constexpr int kQSmem = PairCfg<BN>::kSmem;
+  auto kernel = gemm_pair_kernel<W_KN, DUAL, BN, STREAMS>;
+  constexpr int kQSmem = PairCfg<BN, STREAMS>::kSmem;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -369,7 +386,7 @@ int max_active_pairs() {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto kernel = gemm_pair_kernel<false, false, 256>;
+  auto kernel = gemm_pair_kernel<false, false, 256, 2>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return 0;
@@ -383,6 +400,9 @@ cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const C
                              const CUtensorMap& tmO, const EpiParams& ep, int M, int N, int K,
                              const KernelCtl& ctl, cudaStream_t stream) {
   PairArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
+  if (plan.streams == 1 && !dual)  // one stream: units of one 256-row M-tile
+    return w_kn ? run_pair<true, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream)
+                : run_pair<false, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream);
   if (w_kn)
     return dual ? run_pair<true, true, 256>(plan, tmA, tmW, tmW2, tmO, args, stream)
                 : run_pair<true, false, 256>(plan, tmA, tmW, tmW2, tmO, args, stream);

@@ -39,6 +39,7 @@ enum Path {
   kPathW4 = 3,
   kPathPair = 4,
   kPathPersistentSplit = 5,  // the one-SM persistent kernel, K split over a CTA pair per tile
+  kPathPairOne = 6,          // the CTA-pair kernel with one MMA stream (units of one M-tile)
 };
 
 struct GemmPlan {
@@ -50,6 +51,7 @@ struct GemmPlan {
   int num_kb = 0;    // 64-wide K blocks
   int grid = 0;      // persistent kernels: CTAs
   int bn = 256;      // pair kernel: tile width (MMA N)
+  int streams = 2;   // pair kernel: M-tiles (MMA streams) per unit of work
 };
 
 struct DeviceInfo {

@@ -88,9 +88,9 @@ def test_kernel_path_planning(lib):
     # and 128 x 256 tiles fill at most half of them: two CTAs per tile (split K)
     assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096) == ("persistent_splitk", 2)
     assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 4096) == ("persistent_splitk", 2)
-    assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 4096, 4096) == ("persistent", 1)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 4096, 4096)[0] == "pair_1stream"
     # too little K to pay for the exchange of the partial sums
-    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 256) == ("persistent", 1)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 256)[0] != "persistent_splitk"
     assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 8192, 8192, "kn") == ("pair", 1)
     path, splits = gbf.gbf_kernel_path("gemm_epilogue", 16, 8192, 8192, "kn")
     assert path == "swap_splitk" and 1 <= splits <= 8
@@ -162,24 +162,26 @@ def test_force_path_hook(lib):
 
 
 @pytest.mark.parametrize("op,M,N,K,layout,want", [
-    # measured on a GB300 with both kernels forced (TFLOP/s pair / one-SM):
-    # the one-SM kernel's split-K form when its tiles fill at most half of the
-    # SMs (same box, pair / one-SM / split: 410 / 526 / 737; 256 x 8192^2
-    # 428 / 620 / 913)
-    ("gemm_epilogue", 512, 4096, 4096, "nk", "persistent_splitk"),
-    ("gemm_epilogue", 256, 8192, 8192, "kn", "persistent_splitk"),
-    ("gemm_epilogue", 1024, 4096, 4096, "nk", "persistent"),   # 812 / 1112
-    ("gemm_epilogue", 1536, 4096, 4096, "nk", "pair"),         # 1203 / 956
-    ("gemm_epilogue", 4096, 4096, 4096, "nk", "pair"),         # 1595 / 1354
-    ("gemm_epilogue", 512, 8192, 8192, "kn", "persistent"),    # 843 / 1267
-    ("gemm_epilogue", 768, 8192, 8192, "kn", "pair"),          # 1235 / 1057
-    ("gemm_epilogue", 1536, 8192, 8192, "kn", "persistent"),   # 1258 / 1438
-    ("gemm_epilogue", 3072, 8192, 8192, "kn", "pair"),         # 1648 / 1447
-    ("gemm_epilogue", 384, 14336, 4096, "nk", "pair"),         # 929 / 709
-    ("gemm_epilogue", 640, 14336, 4096, "nk", "persistent"),   # 814 / 1262
-    ("gemm_epilogue", 4096, 14336, 4096, "nk", "pair"),        # 1633 / 1489
-    ("swiglu", 512, 14336, 4096, "nk", "persistent"),          # 1347 / 1456
-    ("swiglu", 1024, 14336, 4096, "nk", "pair"),               # 1790 / 1581
+    # measured on one GB300 with every kernel forced, TFLOP/s
+    # (CTA pair / one-SM / one-SM split-K / CTA pair with one stream):
+    ("gemm_epilogue", 512, 4096, 4096, "nk", "persistent_splitk"),   # 408 / 523 / 707 / 614
+    ("gemm_epilogue", 640, 4096, 4096, "nk", "pair_1stream"),        # 508 / 655 / 547 / 752
+    ("gemm_epilogue", 1024, 4096, 4096, "nk", "pair_1stream"),       # 809 / 1044 / 802 / 1202
+    ("gemm_epilogue", 1536, 4096, 4096, "nk", "pair"),               # 1185 / 927 / 838 / 1049
+    ("gemm_epilogue", 2048, 4096, 4096, "nk", "pair"),               # 1564 / 1218 / 862 / 1395
+    ("gemm_epilogue", 256, 8192, 8192, "kn", "persistent_splitk"),   # 428 / 620 / 913 / -
+    ("gemm_epilogue", 512, 8192, 8192, "kn", "pair_1stream"),        # 845 / 1196 / 1051 / 1432
+    ("gemm_epilogue", 768, 8192, 8192, "kn", "pair"),                # 1240 / 1014 / 1095 / 1179
+    ("gemm_epilogue", 1536, 8192, 8192, "kn", "pair_1stream"),       # 1283 / 1360 / 1185 / 1587
+    ("gemm_epilogue", 384, 14336, 4096, "nk", "pair"),               # 1019 / 744 / 709 / 911
+    ("gemm_epilogue", 640, 14336, 4096, "nk", "persistent"),         # 925 / 1274 / 899 / 1070
+    ("gemm_epilogue", 1024, 14336, 4096, "nk", "pair_1stream"),      # 1453 / 1434 / 985 / 1590
+    # earlier measurements (pair / one-SM), still the planner's choice:
+    ("gemm_epilogue", 4096, 4096, 4096, "nk", "pair"),               # 1595 / 1354
+    ("gemm_epilogue", 3072, 8192, 8192, "kn", "pair"),               # 1648 / 1447
+    ("gemm_epilogue", 4096, 14336, 4096, "nk", "pair"),              # 1633 / 1489
+    ("swiglu", 512, 14336, 4096, "nk", "persistent"),                # 1347 / 1456
+    ("swiglu", 1024, 14336, 4096, "nk", "pair"),                     # 1790 / 1581
 ])
 def test_planner_picks_the_measured_faster_kernel(lib, op, M, N, K, layout, want):
     assert gbf.gbf_kernel_path(op, M, N, K, layout)[0] == want

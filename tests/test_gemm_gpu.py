@@ -121,6 +121,17 @@ def test_cta_pair_kernel(cuda_lib, layout, M, N, K):
                   expect_path="pair", force_path="pair")
 
 
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,N,K", [(257, 264, 136), (1030, 1048, 136), (640, 4096, 512),
+                                   (2048, 2560, 192), (4100, 520, 64)])
+def test_cta_pair_kernel_one_stream(cuda_lib, layout, M, N, K):
+    # units of one 256-row M-tile, one MMA stream alternating between the two
+    # accumulators; more units than pairs in the last two cases (the
+    # accumulators are reused across rounds)
+    run_and_check(cuda_lib, M, N, K, layout, "silu", 0.75, 0.5, seed=M + 7 * N + K,
+                  expect_path="pair_1stream", force_path="pair_1stream")
+
+
 @pytest.mark.parametrize("M,N,K", [(512, 4096, 256), (768, 2048, 192), (1024, 8192, 128),
                                    (3000, 1024, 64)])
 def test_automatic_kernel_choice(cuda_lib, M, N, K):
