@@ -330,7 +330,7 @@ GemmPlan pair_plan(int64_t M, int64_t N, bool dual, bool kn, const DeviceInfo& d
     p.grid = 2 * std::min(p.m_tiles * p.n_tiles, dev.pairs);
     return p;
   }
-  if (!dual && !kn) {
+  if (!dual) {
     // A 224-wide tile when it wastes less of the last round of tiles:
     // compare useful area / (rounds * pairs * tile area).
     // (a pair computes two M-tiles at a time: 512 x bn per round)

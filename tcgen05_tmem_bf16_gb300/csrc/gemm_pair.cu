@@ -68,7 +68,10 @@ constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
 template <int BN, int STREAMS = 2>
 struct PairCfg {
   static constexpr int kStreams = STREAMS;
-  static constexpr int kBBytes = (BN / 2) * kBK * 2;
+  // B region of a stage: room for 128 rows / columns of 64 k (16 KB); a
+  // 224-wide tile fills 112 of them (K-major rows), or two 64-column boxes of
+  // which the MMA reads the first 112 columns (N-major B[K][N])
+  static constexpr int kBBytes = 128 * kBK * 2;
   static constexpr int kStageBytes = STREAMS * kQABytes + kBBytes;  // A0 (| A1) | B
   static constexpr int kStages = STREAMS == 2 ? 4 : 6;
   // ring | barriers (1 KB) | output staging: 8 epilogue warps x 2 buffers of 2 KB
@@ -103,7 +106,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   using Cfg = PairCfg<BN, STREAMS>;
   constexpr int kQStages = Cfg::kStages;
   constexpr int kQStreams = Cfg::kStreams;
-  static_assert(!(W_KN || DUAL) || BN == 256, "narrow tiles only for K-contiguous single B");
+  // bytes the TMA engine writes into one CTA's stage
+  constexpr int kLoadBytes =
+      kQStreams * kQABytes + (W_KN ? 2 * 64 * kBK * 2 : (BN / 2) * kBK * 2);
+  static_assert(!DUAL || BN == 256, "narrow tiles only for the single product");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
@@ -181,7 +187,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           uint8_t* sa = stages + s * Cfg::kStageBytes;
           uint8_t* sb = sa + kQStreams * kQABytes;
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
-          if (leader) mbar_arrive_expect_tx(&full[s], 2 * Cfg::kStageBytes);
+          if (leader) mbar_arrive_expect_tx(&full[s], 2 * kLoadBytes);
 #pragma unroll
           for (int i = 0; i < kQStreams; ++i)  // rows past M read as zeros
             tma_load_2d_pair(sa + i * kQABytes, &tmA, bar, kb * kBK,
@@ -404,8 +410,9 @@ cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const C
     return w_kn ? run_pair<true, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream)
                 : run_pair<false, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream);
   if (w_kn)
-    return dual ? run_pair<true, true, 256>(plan, tmA, tmW, tmW2, tmO, args, stream)
-                : run_pair<true, false, 256>(plan, tmA, tmW, tmW2, tmO, args, stream);
+    return dual              ? run_pair<true, true, 256>(plan, tmA, tmW, tmW2, tmO, args, stream)
+           : plan.bn == 224 ? run_pair<true, false, 224>(plan, tmA, tmW, tmW2, tmO, args, stream)
+                            : run_pair<true, false, 256>(plan, tmA, tmW, tmW2, tmO, args, stream);
   if (dual) return run_pair<false, true, 256>(plan, tmA, tmW, tmW2, tmO, args, stream);
   return plan.bn == 224 ? run_pair<false, false, 224>(plan, tmA, tmW, tmW2, tmO, args, stream)
                         : run_pair<false, false, 256>(plan, tmA, tmW, tmW2, tmO, args, stream);

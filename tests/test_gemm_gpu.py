@@ -113,6 +113,16 @@ def test_persistent_splitk_in_place_residual(cuda_lib):
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,N,K", [(512, 2048, 256), (1000, 2000, 320)])
+def test_cta_pair_kernel_224_wide_tiles(cuda_lib, layout, M, N, K):
+    # shapes whose last round of 256-wide tiles is thin, so the planner takes
+    # 224-wide tiles (for B as [K][N] the MMA reads 112 of the 128 columns each
+    # CTA loads); N not a multiple of 224
+    run_and_check(cuda_lib, M, N, K, layout, "gelu_tanh", 0.75, 0.25, seed=M + 11 * N + K,
+                  expect_path="pair", force_path="pair")
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("M,N,K", [(512, 256, 64), (515, 264, 256), (1030, 1048, 136),
                                    (777, 520, 328), (2048, 1024, 512), (129, 264, 128),
                                    (300, 520, 200), (400, 1048, 136)])
