@@ -144,7 +144,8 @@ GBF_API gbf_status_t w4a16_gemm(const void *A, const uint8_t *Wq, const void *sc
  * w4a16_nvfp4_gemm -- the gemm_epilogue result with
  *   B~[k][n] = e2m1(q[k][n]) * e4m3(S[k/16][n])   (exact in bf16),
  *   NVFP4 weight-only quantisation with bf16 activations ("Fusion Thinking",
- *   Pattern 3: "INT4 / INT8 / NVFP4 weights, BF16 activations").
+ *   Pattern 3 lists NVFP4 among the weight-only formats used with bf16
+ *   activations).
  *   Wq     [K][N/2] bytes of OCP FP4 E2M1 codes, packed like w4a16_gemm's
  *          (column 2j in the HIGH nibble of byte j).
  *   scales [K/16][N] bytes, each an E4M3 factor for 16 consecutive k.
