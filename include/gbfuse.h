@@ -149,7 +149,8 @@ GBF_API gbf_status_t w4a16_gemm(const void *A, const uint8_t *Wq, const void *sc
  *   Wq     [K][N/2] bytes of OCP FP4 E2M1 codes, packed like w4a16_gemm's
  *          (column 2j in the HIGH nibble of byte j).
  *   scales [K/16][N] bytes, each an E4M3 factor for 16 consecutive k.
- *   The format's per-tensor factor is alpha (it multiplies the product).
+ *   The format's per-tensor factor is alpha (it multiplies the product);
+ *   a finite alpha with |alpha| >= 2^100 returns GBF_ERR_INVALID_ARG.
  *   Requires K % 16 == 0 and N % 32 == 0.  Workspace unused (NULL, 0).
  */
 GBF_API gbf_status_t w8a16_fp8_gemm(const void *A, const uint8_t *Wq, const void *scales,

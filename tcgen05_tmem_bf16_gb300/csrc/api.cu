@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -537,6 +538,9 @@ gbf_status_t w4a16_nvfp4_gemm(const void* A, const uint8_t* Wq, const uint8_t* s
   (void)workspace_bytes;
   gbf_status_t st = check_nvfp4(M, N, K, act);
   if (st != GBF_OK) return st;
+  // the kernel carries the product scaled by 2^-19 and restores it through
+  // alpha, which must leave room for that factor
+  if (std::fabs(alpha) >= 0x1p100f && std::fabs(alpha) != INFINITY) return GBF_ERR_INVALID_ARG;
   if ((st = check_ptrs({A, Wq, scales, out}, {C, bias, residual})) != GBF_OK) return st;
   const DeviceInfo* dev;
   unsigned* err;

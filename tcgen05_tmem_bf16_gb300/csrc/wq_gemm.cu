@@ -72,7 +72,6 @@ namespace gbf {
 constexpr int kW4Threads = 384;                 // warps 0-3 roles, 4-11 transform/epilogue
 constexpr int kW4Regions = 4;
 constexpr uint32_t kBf16x2Pow120 = 0x7B807B80u;  // bf16x2 (2^120, 2^120)
-constexpr uint32_t kBf16x2Pow126 = 0x7E807E80u;  // bf16x2 (2^126, 2^126)
 
 template <int FMT, int MPAD>
 struct W4Cfg {
@@ -314,14 +313,26 @@ __device__ __forceinline__ void e4m3x4_to_bf16x2_dup(uint32_t b, uint32_t& s0, u
       : "r"(b), "r"(kBf16x2Pow120));
 }
 
-// NVFP4 k-row pair: x0, x1 = the 16-bit loads of rows k and k+1 (packed bytes
-// 2t, 2t+1), joined into X.  Region r's nibble sits at bits 4/0/12/8 of each
-// half; its magnitude bits (EE.M) move to bf16 bits 6..8 and its sign bit to
-// bit 15; then x 2^126 and x s (both exact).
-__device__ __forceinline__ void deq_fp4_rowpair(uint32_t x0, uint32_t x1, uint32_t s0,
-                                                uint32_t s1, uint32_t s2, uint32_t s3,
-                                                uint32_t& o0, uint32_t& o1, uint32_t& o2,
-                                                uint32_t& o3) {
+// NVFP4 k-row pairs: x0, x1 = the 16-bit loads of rows k and k+1 (packed
+// bytes 2t, 2t+1), joined into X.  Region r's nibble sits at bits 4/0/12/8 of
+// each half; its magnitude bits (EE.M) move to bf16 bits 6..8 and its sign bit
+// to bit 15, which reads as e2m1 * 2^-126 (the code 0.5 as a bf16 subnormal).
+//
+// NVFP4 operand scaled by an exact power of two: with sp = s * 2^107 (exact:
+// s <= 448), one multiply gives e2m1 * s * 2^-19 instead of e2m1 * s (the code
+// read as bf16 is e2m1 * 2^-126; the product has at most 6 significant bits
+// and lies in [2^-29, 2^-7.6], so it is exact and a normal bf16).  The MMA
+// then accumulates the product scaled by 2^-19, which fp32 does exactly as
+// it would the unscaled one (a power-of-two factor commutes with every
+// rounding while nothing underflows), and the ending multiplies by 2^19
+// through alpha.  5 instructions per bf16 pair instead of 6.
+constexpr float kNvfp4OperandScale = 524288.0f;  // 2^19, restored in the ending
+constexpr uint32_t kBf16x2Pow107 = 0x75007500u;  // bf16x2 (2^107, 2^107)
+
+__device__ __forceinline__ void deq_fp4_rowpair_scaled(uint32_t x0, uint32_t x1, uint32_t sp0,
+                                                       uint32_t sp1, uint32_t sp2, uint32_t sp3,
+                                                       uint32_t& o0, uint32_t& o1, uint32_t& o2,
+                                                       uint32_t& o3) {
   asm("{\n\t"
       ".reg .b32 x, a, b;\n\t"
       "prmt.b32 x, %4, %5, 0x5410;\n\t"
@@ -329,28 +340,24 @@ __device__ __forceinline__ void deq_fp4_rowpair(uint32_t x0, uint32_t x1, uint32
       "shl.b32 b, x, 8;\n\t"
       "and.b32 a, a, 0x01C001C0;\n\t"
       "lop3.b32 a, a, b, 0x80008000, 0xF8;\n\t"
-      "mul.rn.bf16x2 a, a, %10;\n\t"
       "mul.rn.bf16x2 %0, a, %6;\n\t"
       "shl.b32 a, x, 6;\n\t"
       "shl.b32 b, x, 12;\n\t"
       "and.b32 a, a, 0x01C001C0;\n\t"
       "lop3.b32 a, a, b, 0x80008000, 0xF8;\n\t"
-      "mul.rn.bf16x2 a, a, %10;\n\t"
       "mul.rn.bf16x2 %1, a, %7;\n\t"
       "shr.b32 a, x, 6;\n\t"
       "and.b32 a, a, 0x01C001C0;\n\t"
       "lop3.b32 a, a, x, 0x80008000, 0xF8;\n\t"
-      "mul.rn.bf16x2 a, a, %10;\n\t"
       "mul.rn.bf16x2 %2, a, %8;\n\t"
       "shr.b32 a, x, 2;\n\t"
       "shl.b32 b, x, 4;\n\t"
       "and.b32 a, a, 0x01C001C0;\n\t"
       "lop3.b32 a, a, b, 0x80008000, 0xF8;\n\t"
-      "mul.rn.bf16x2 a, a, %10;\n\t"
       "mul.rn.bf16x2 %3, a, %9;\n\t"
       "}"
       : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
-      : "r"(x0), "r"(x1), "r"(s0), "r"(s1), "r"(s2), "r"(s3), "r"(kBf16x2Pow126));
+      : "r"(x0), "r"(x1), "r"(sp0), "r"(sp1), "r"(sp2), "r"(sp3));
 }
 
 // Epilogue of output columns n..n+3 for 8 rows m0..m0+7: operand loads
@@ -734,11 +741,14 @@ __global__ void __launch_bounds__(kW4Threads, 2)
           const uint32_t sb = *reinterpret_cast<const uint32_t*>(
               ssc + (t >> 6) * 1024 + (2 * g + hh) * 256 + 4 * (t & 63));
           e4m3x4_to_bf16x2_dup(sb, s0, s1, s2, s3);
+          // s * 2^107 (exact), for the operand scaled by 2^-19
+          const uint32_t p0 = bf16x2_mul(s0, kBf16x2Pow107), p1 = bf16x2_mul(s1, kBf16x2Pow107);
+          const uint32_t p2 = bf16x2_mul(s2, kBf16x2Pow107), p3 = bf16x2_mul(s3, kBf16x2Pow107);
           auto deq = [=](const uint8_t* r0, const uint8_t* r1, uint32_t& a0, uint32_t& a1,
                          uint32_t& a2, uint32_t& a3) {
-            deq_fp4_rowpair(*reinterpret_cast<const uint16_t*>(r0),
-                            *reinterpret_cast<const uint16_t*>(r1), s0, s1, s2, s3, a0, a1, a2,
-                            a3);
+            deq_fp4_rowpair_scaled(*reinterpret_cast<const uint16_t*>(r0),
+                                   *reinterpret_cast<const uint16_t*>(r1), p0, p1, p2, p3, a0,
+                                   a1, a2, a3);
           };
           ok = half(hh, rows, Cfg::kRowBytes, deq);
         }
@@ -1000,6 +1010,8 @@ cudaError_t launch_wq_gemm(int fmt, const GemmPlan& plan, const CUtensorMap& tmA
                            int M, int N, int K, int group, const KernelCtl& ctl,
                            cudaStream_t stream) {
   W4Args args{M, N, K, plan.num_kb, plan.splits, ep, ctl};
+  // the NVFP4 operand is the weight scaled by 2^-19 (deq_fp4_rowpair_scaled)
+  if (fmt == kWqNvfp4) args.ep.alpha *= kNvfp4OperandScale;
   switch (fmt) {
     case kWqInt4: return run_w4_fmt<kWqInt4>(plan, tmA, tmQ, tmS, args, group, stream);
     case kWqFp8: return run_w4_fmt<kWqFp8>(plan, tmA, tmQ, tmS, args, group, stream);

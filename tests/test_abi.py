@@ -139,6 +139,10 @@ def test_validation_errors_are_returned_before_any_launch(lib):
     assert s == 4
     s = gbf.swiglu_dual_gemm(a, a, None, 1, a, 8, 8, 8, stream=0, raise_on_error=False)
     assert s == 1
+    # the NVFP4 kernel restores its 2^-19 operand scale through alpha
+    nv = lambda alpha: gbf.w4a16_nvfp4_gemm(a, a, a, None, None, None, a, 8, 64, 64, alpha,
+                                            stream=0, raise_on_error=False)
+    assert nv(2.0 ** 100) == 1 and nv(-(2.0 ** 101)) == 1 and nv(3e38) == 1
 
 
 def test_timeout_setting_is_clamped(lib):

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_util import assert_parity, down, poison_bf16, up
+from gpu_util import assert_parity, down, poison_bf16, up, widen
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +72,20 @@ def test_nvfp4_fused(cuda_lib, M, N, K):
     w = nvfp4_inputs(M, N, K, seed=M + N)
     got, _ = run(cuda_lib, "w4a16_nvfp4", w, M, N, K)
     assert_parity(got, want("w4a16_nvfp4", w, M, N, K), f"nvfp4 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -40, 2.0 ** 40])
+def test_nvfp4_alpha_far_from_one(cuda_lib, scale):
+    """The NVFP4 kernel carries its operand scaled by 2^-19 and multiplies
+    alpha by 2^19; the result must not depend on where alpha sits."""
+    M, N, K = 16, 1024, 1024
+    w = nvfp4_inputs(M, N, K, seed=7)
+    got1, _ = run(cuda_lib, "w4a16_nvfp4", w, M, N, K)
+    assert_parity(got1, want("w4a16_nvfp4", w, M, N, K), "nvfp4")
+    got, _ = run(cuda_lib, "w4a16_nvfp4", w, M, N, K, alpha=w["alpha"] * scale)
+    # alpha * acc is one fp32 product, so a power-of-two factor on alpha
+    # scales every output exactly (nothing here leaves the normal range)
+    np.testing.assert_array_equal(widen(got), widen(got1) * scale)
 
 
 @pytest.mark.parametrize("kind", ["w8a16_fp8", "w4a16_nvfp4"])
