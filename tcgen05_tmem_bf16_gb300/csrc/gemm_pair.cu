@@ -408,7 +408,9 @@ cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const C
   PairArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
   if (plan.streams == 1 && !dual)  // one stream: units of one 256-row M-tile
     return w_kn ? run_pair<true, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream)
-                : run_pair<false, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream);
+           : plan.bn == 224
+               ? run_pair<false, false, 224, 1>(plan, tmA, tmW, tmW2, tmO, args, stream)
+               : run_pair<false, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream);
   if (w_kn)
     return dual              ? run_pair<true, true, 256>(plan, tmA, tmW, tmW2, tmO, args, stream)
            : plan.bn == 224 ? run_pair<true, false, 224>(plan, tmA, tmW, tmW2, tmO, args, stream)

@@ -142,6 +142,16 @@ def test_cta_pair_kernel_one_stream(cuda_lib, layout, M, N, K):
                   expect_path="pair_1stream", force_path="pair_1stream")
 
 
+@pytest.mark.parametrize("layout", ["nk"])
+@pytest.mark.parametrize("M,N,K", [(1024, 4096, 256), (700, 2000, 200)])
+def test_cta_pair_kernel_one_stream_224_wide_tiles(cuda_lib, layout, M, N, K):
+    # one-stream units whose 256-wide tiles leave SM pairs idle, so the
+    # planner takes 224-wide tiles for K-contiguous weights (16 -> 19
+    # N-tiles; N = 2000 ragged)
+    run_and_check(cuda_lib, M, N, K, layout, "gelu_tanh", 0.5, 0.75, seed=M + 5 * N + K,
+                  expect_path="pair_1stream", force_path="pair_1stream")
+
+
 @pytest.mark.parametrize("M,N,K", [(512, 4096, 256), (768, 2048, 192), (1024, 8192, 128),
                                    (3000, 1024, 64)])
 def test_automatic_kernel_choice(cuda_lib, M, N, K):
