@@ -523,7 +523,9 @@ __global__ void __launch_bounds__(256, 2)
       uint32_t fills[Cfg::kStages];
 #pragma unroll
       for (int i = 0; i < Cfg::kStages; ++i) fills[i] = 0;
-      // weight tiles of k block kb into stage s (read-only inputs)
+      // weight tiles of k block kb into stage s (read-only inputs, read once:
+      // evict-first, so that the ending's operands pulled into L2 stay)
+      const uint64_t wpol = policy_evict_first();
       auto load_w = [&](int s, int kb) {
         uint8_t* sw = stages + s * Cfg::kStageBytes;
 #pragma unroll
@@ -531,10 +533,10 @@ __global__ void __launch_bounds__(256, 2)
           const CUtensorMap* map = w == 0 ? &tmW : &tmW2;
           uint8_t* dst = sw + w * Cfg::kWTile;
           if constexpr (W_KN) {
-            tma_load_2d(dst, map, &full[s], nb * kSwapBN, kb * kBK);
-            tma_load_2d(dst + 8192, map, &full[s], nb * kSwapBN + 64, kb * kBK);
+            tma_load_2d_hint(dst, map, &full[s], nb * kSwapBN, kb * kBK, wpol);
+            tma_load_2d_hint(dst + 8192, map, &full[s], nb * kSwapBN + 64, kb * kBK, wpol);
           } else {
-            tma_load_2d(dst, map, &full[s], kb * kBK, nb * kSwapBN);
+            tma_load_2d_hint(dst, map, &full[s], kb * kBK, nb * kSwapBN, wpol);
           }
         }
       };
@@ -644,6 +646,21 @@ __global__ void __launch_bounds__(256, 2)
   bool have = false;
   const uint64_t pol = l2_evict_first_policy();
   const int n = nb * kSwapBN + tid;
+  // The ending's C and residual rows [r0, r0 + nr) of this warp's 32
+  // columns are pulled into L2 as soon as the previous kernel has finished,
+  // so that their loads after the main loop hit L2 (one 64-byte segment per
+  // row and operand; lane j takes rows j, j + 32, ...).
+  auto l2_rows = [&](int r0, int nr) {
+    const int n0 = nb * kSwapBN + q * 32;
+    if (n0 >= a.N) return;
+    for (int j = lane; j < nr; j += 32) {
+      const int64_t m = static_cast<int64_t>(mb) * MPAD + r0 + j;
+      if (m >= a.M) break;
+      if (a.ep.C) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.ep.C + m * a.N + n0));
+      if (a.ep.residual)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a.ep.residual + m * a.N + n0));
+    }
+  };
   bool pushed = false;
   if constexpr (Cfg::kPush) {
     if (S > 1) {
@@ -655,6 +672,7 @@ __global__ void __launch_bounds__(256, 2)
       uint8_t* recv = stages + Cfg::kQuads * Cfg::kQuadBytes;  // [sender][group][product][lane]
       ColLoads<4> L4;
       if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
+      if (epi) l2_rows(4 * qa, 4 * nq);
       if (epi && nq > 0)
         col_prefetch<4>(L4, static_cast<int64_t>(mb) * MPAD + 4 * qa, n, a.M, a.N, a.ep, pol);
       if (epi) {
@@ -745,6 +763,8 @@ __global__ void __launch_bounds__(256, 2)
   if (!pushed) {
     ColLoads<16> L;
     if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
+    if (epi)
+      for (int c = static_cast<int>(rank); c < kChunks; c += S) l2_rows(16 * c, 16);
     if (epi && static_cast<int>(rank) < kChunks)  // this rank's first chunk: operands early
       col_prefetch<16>(L, static_cast<int64_t>(mb) * MPAD + static_cast<int>(rank) * 16, n, a.M,
                      a.N, a.ep, pol);
