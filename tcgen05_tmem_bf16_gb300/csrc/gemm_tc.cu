@@ -635,8 +635,8 @@ __global__ void __launch_bounds__(256, 2)
   // that rank with one bulk copy, and each rank sums its own groups over
   // ranks 0..S-1 in that order (deterministic) from local shared memory.
   // Otherwise the 16-row chunks go to the ranks round-robin (chunk c to rank
-  // c % S) and each rank pulls the other partials of its chunks through
-  // distributed shared memory, again summing in rank order.
+  // c % S) and all eight warps of each rank pull the other partials of its
+  // chunks through distributed shared memory, again summing in rank order.
   const bool epi = warp >= 4;
   const int q = warp & 3;
   const int tid = threadIdx.x - 128;  // 0..127 for the epilogue warps = TMEM lane
@@ -760,64 +760,98 @@ __global__ void __launch_bounds__(256, 2)
       cluster_sync_all();
     }
   }
-  if (!pushed) {
+  if constexpr (!Cfg::kPush) {
+    if (S > 1) {
+      // Pull exchange (the single product at M > 64): 16-row chunks go to the
+      // ranks round-robin (chunk c to rank c % S).  After the park and a
+      // cluster barrier all eight warps of the rank reduce its chunks, two
+      // threads per column (rows 16c .. 16c+7 and 16c+8 .. 16c+15), loading
+      // the other ranks' partials through distributed shared memory and
+      // summing in rank order 0..S-1.
+      static_assert(!DUAL, "the gate/up GEMM always pushes");
+      pushed = true;
+      const int h = threadIdx.x >> 7;    // row half of each chunk
+      const int col = threadIdx.x & 127;  // column of the tile
+      const int ncol = nb * kSwapBN + col;
+      const int r = static_cast<int>(rank);
+      ColLoads<8> L8;
+      griddep_wait();  // every thread: the ending reads C, bias, residual and writes out
+      if (epi)
+        for (int c = r; c < kChunks; c += S) l2_rows(16 * c, 16);
+      if (r < kChunks)  // this rank's first chunk: operands early
+        col_prefetch<8>(L8, static_cast<int64_t>(mb) * MPAD + r * 16 + 8 * h, ncol, a.M, a.N,
+                        a.ep, pol);
+      if (epi) {
+        have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
+        tc_fence_after();
+        // park: red[(chunk * 4 + v) * 128 + lane] = rows 16 chunk + 4v .. +3
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+          float v[16];
+          acc_sum16<Cfg::kAcc, MPAD>(tb + c * 16, v);
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            red[(c * 4 + w) * 128 + tid] =
+                make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+        }
+      }
+      // every rank parked (the other warps only wrote registers: their loads
+      // of the first chunk's operands stay in flight across the barrier)
+      if (epi) cluster_sync_all();
+      else cluster_sync_relaxed_arrive();
+#pragma unroll 1
+      for (int c = r; c < kChunks; c += S) {
+        if (c != r)
+          col_prefetch<8>(L8, static_cast<int64_t>(mb) * MPAD + c * 16 + 8 * h, ncol, a.M, a.N,
+                          a.ep, pol);
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+        for (int p = 0; p < S; ++p) {
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            float4* src = &red[(c * 4 + 2 * h + w) * 128 + col];
+            const float4 f = p == r ? *src
+                                    : ld_dsmem_f4(mapa_shared(smem_u32(src),
+                                                              static_cast<uint32_t>(p)));
+            v[4 * w] += f.x;
+            v[4 * w + 1] += f.y;
+            v[4 * w + 2] += f.z;
+            v[4 * w + 3] += f.w;
+          }
+        }
+        const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16 + 8 * h;
+        switch (a.ep.act) {
+          case kActRelu: epi_col<kActRelu, 8>(v, L8, m0, ncol, a.M, a.N, a.ep, pol); break;
+          case kActSilu: epi_col<kActSilu, 8>(v, L8, m0, ncol, a.M, a.N, a.ep, pol); break;
+          case kActGeluTanh: epi_col<kActGeluTanh, 8>(v, L8, m0, ncol, a.M, a.N, a.ep, pol); break;
+          default: epi_col<kActIdentity, 8>(v, L8, m0, ncol, a.M, a.N, a.ep, pol); break;
+        }
+      }
+      // no rank leaves while another may still read its shared memory
+      cluster_sync_all();
+    }
+  }
+  if (!pushed) {  // S == 1: the accumulator straight from tensor memory
     ColLoads<16> L;
     if (epi) griddep_wait();  // the ending reads C, bias, residual and writes out
-    if (epi)
-      for (int c = static_cast<int>(rank); c < kChunks; c += S) l2_rows(16 * c, 16);
-    if (epi && static_cast<int>(rank) < kChunks)  // this rank's first chunk: operands early
-      col_prefetch<16>(L, static_cast<int64_t>(mb) * MPAD + static_cast<int>(rank) * 16, n, a.M,
-                     a.N, a.ep, pol);
+    if (epi) l2_rows(0, MPAD);
+    if (epi)  // the first chunk's operands early
+      col_prefetch<16>(L, static_cast<int64_t>(mb) * MPAD, n, a.M, a.N, a.ep, pol);
     if (epi) {
       have = wait_bar(dfull, 0, ctl, kSiteEpiAccFull);
       tc_fence_after();
-      if (!Cfg::kPush && S > 1) {  // (with the push exchange this path runs with S = 1 only)
 #pragma unroll 1
-        for (int c = 0; c < Cfg::kProducts * kChunks; ++c) {  // gate chunks, then up chunks
-          float r[16];
-          acc_sum16<Cfg::kAcc, MPAD>(tb + (c / kChunks) * Cfg::kAcc * MPAD + (c % kChunks) * 16,
-                                     r);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            red[(c * 4 + v) * 128 + tid] = make_float4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
-        }
-      }
-    }
-    if (S > 1) cluster_sync_all();
-    if (epi) {
-#pragma unroll 1
-      for (int c = static_cast<int>(rank); c < kChunks; c += S) {
-        if (c != static_cast<int>(rank))
+      for (int c = 0; c < kChunks; ++c) {
+        if (c != 0)
           col_prefetch<16>(L, static_cast<int64_t>(mb) * MPAD + c * 16, n, a.M, a.N, a.ep, pol);
         float v[Cfg::kProducts][16];
 #pragma unroll
         for (int pr = 0; pr < Cfg::kProducts; ++pr) {
-          if (S == 1) {
-            float r[16];
-            acc_sum16<Cfg::kAcc, MPAD>(tb + pr * Cfg::kAcc * MPAD + c * 16, r);
+          float rr[16];
+          acc_sum16<Cfg::kAcc, MPAD>(tb + pr * Cfg::kAcc * MPAD + c * 16, rr);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[pr][j] = have ? r[j] : 0.0f;
-          } else if constexpr (!Cfg::kPush) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[pr][j] = 0.0f;
-            const int cc = pr * kChunks + c;
-            for (int p = 0; p < S; ++p) {
-#pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                float4 f;
-                if (p == static_cast<int>(rank)) {
-                  f = red[(cc * 4 + w) * 128 + tid];
-                } else {
-                  f = ld_dsmem_f4(mapa_shared(smem_u32(&red[(cc * 4 + w) * 128 + tid]),
-                                              static_cast<uint32_t>(p)));
-                }
-                v[pr][4 * w] += f.x;
-                v[pr][4 * w + 1] += f.y;
-                v[pr][4 * w + 2] += f.z;
-                v[pr][4 * w + 3] += f.w;
-              }
-            }
-          }
+          for (int j = 0; j < 16; ++j) v[pr][j] = have ? rr[j] : 0.0f;
         }
         const int64_t m0 = static_cast<int64_t>(mb) * MPAD + c * 16;
         if constexpr (DUAL) {
@@ -839,7 +873,6 @@ __global__ void __launch_bounds__(256, 2)
         }
       }
     }
-    if (S > 1) cluster_sync_all();
   }
 
   if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));

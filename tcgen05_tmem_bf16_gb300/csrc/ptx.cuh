@@ -320,6 +320,15 @@ __device__ __forceinline__ void cluster_sync_all() {
                    : "memory");
 }
 
+// The same barrier for a warp that has written nothing the other CTAs of the
+// cluster read: a relaxed arrival does not first wait for the warp's own
+// loads still in flight.
+__device__ __forceinline__ void cluster_sync_relaxed_arrive() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
 // the shared memory of another CTA of the cluster; the copy completes
 // `bytes` transactions on that CTA's mbarrier.  dst and mbar are
