@@ -756,8 +756,11 @@ __global__ void __launch_bounds__(256, 2)
           }
         }
       }
-      // no rank leaves while copies from or into its shared memory may be in flight
-      cluster_sync_all();
+      // No rank leaves while copies from or into its shared memory may be in
+      // flight: every copy has completed on its receiver's barrier, which the
+      // receiver waited for before arriving.  The arrival is relaxed, so it
+      // does not first wait for this thread's stores of the ending.
+      cluster_sync_relaxed_arrive();
     }
   }
   if constexpr (!Cfg::kPush) {
@@ -828,8 +831,10 @@ __global__ void __launch_bounds__(256, 2)
           default: epi_col<kActIdentity, 8>(v, L8, m0, ncol, a.M, a.N, a.ep, pol); break;
         }
       }
-      // no rank leaves while another may still read its shared memory
-      cluster_sync_all();
+      // No rank leaves while another may still read its shared memory: every
+      // remote load's value has been used before its thread arrives.  The
+      // arrival is relaxed, so it does not first wait for the ending's stores.
+      cluster_sync_relaxed_arrive();
     }
   }
   if (!pushed) {  // S == 1: the accumulator straight from tensor memory
