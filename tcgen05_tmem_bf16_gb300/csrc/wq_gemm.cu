@@ -859,8 +859,11 @@ __global__ void __launch_bounds__(kW4Threads, 2)
           }
         }
       }
-      // no rank leaves while copies from or into its shared memory may be in flight
-      cluster_sync_all();
+      // No rank leaves while copies from or into its shared memory may be in
+      // flight: every copy has completed on its receiver's barrier, which the
+      // receiver waited for before arriving.  The arrival is relaxed, so it
+      // does not first wait for this thread's stores of the ending.
+      cluster_sync_relaxed_arrive();
     }
   }
   if (!pushed) {
@@ -944,7 +947,9 @@ __global__ void __launch_bounds__(kW4Threads, 2)
       }
     }
   }
-  if (S > 1) cluster_sync_all();
+  // no rank leaves while another may still read its shared memory (every
+  // remote load's value is used before its thread arrives: relaxed arrival)
+  if (S > 1) cluster_sync_relaxed_arrive();
   }
 
   if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
