@@ -836,7 +836,7 @@ def measure(name: str, args, dev, stream, peaks, peak_src, world: int, headline:
     kname = {"persistent": "gemm_persistent_kernel", "persistent_splitk": "gemm_persistent_kernel",
              "swap_splitk": "gemm_swap_kernel",
              "w4a16": "wq_gemm_kernel", "pair": "gemm_pair_kernel",
-             "pair_1stream": "gemm_pair_kernel",
+             "pair_1stream": "gemm_pair_kernel", "pair_splitk": "gemm_pair_kernel",
              "add_rmsnorm": "add_rmsnorm_kernel",
              "swiglu_pointwise": "swiglu_pointwise_kernel"}.get(wl.path, wl.path)
     tpeak_name = ("bf16_tflops_sustained (back-to-back loop)" if long_loop

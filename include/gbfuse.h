@@ -321,11 +321,12 @@ GBF_API gbf_status_t gbf_set_wait_timeout_ns(uint64_t ns);
  * when its 512-row units fill the GPU better), 5 = the persistent kernel's
  * split-K form (two CTAs per tile, chosen when the tiles fill at most half
  * of the SMs), 6 = the CTA-pair kernel with one MMA stream (units of 256
- * rows), 0 = no launch (empty output), -1 = the arguments would be
- * rejected.
+ * rows), 7 = its split-K form (two CTA pairs per 256 x 256 tile, each over
+ * half of K, chosen when every tile's cluster fits at once), 0 = no launch
+ * (empty output), -1 = the arguments would be rejected.
  * `*splits` (may be NULL) receives the split-K cluster size.
  *
- * Kernels of families 2, 3 and 4 are launched with programmatic stream
+ * Kernels of families 2, 3, 4, 6 and 7 are launched with programmatic stream
  * serialization: they may begin while the previous kernel in the stream is
  * finishing, and read or write nothing in global memory before it has
  * completed (griddepcontrol.wait), so stream order is preserved. */

@@ -39,10 +39,11 @@ GBF_API gbf_status_t gbf_debug_force_splits(int splits);
 
 /* Tuning hook: for the dense product (and the gate/up GEMM) at M above the
  * swapped kernel's range, run the persistent kernel (1), its split-K form
- * over two CTAs per tile (5), the CTA-pair kernel (4) or the CTA-pair kernel
- * with one MMA stream (6) for later launches instead of the automatic choice
- * (0, the default); 5 and 6 apply to the single product only (the gate/up
- * GEMM then takes the automatic choice).  Other values return GBF_ERR_INVALID_ARG.
+ * over two CTAs per tile (5), the CTA-pair kernel (4), the CTA-pair kernel
+ * with one MMA stream (6) or its split-K form over two pairs per tile (7) for
+ * later launches instead of the automatic choice (0, the default); 5, 6 and 7
+ * apply to the single product only (the gate/up GEMM then takes the
+ * automatic choice; 7 also needs K >= 128).  Other values return GBF_ERR_INVALID_ARG.
  * Changes which kernel computes the result, not the result beyond the order
  * of rounding. */
 GBF_API gbf_status_t gbf_debug_force_path(int path);

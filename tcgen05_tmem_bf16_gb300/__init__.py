@@ -30,7 +30,7 @@ STATUS = {0: "GBF_OK", 1: "GBF_ERR_INVALID_ARG", 2: "GBF_ERR_MISALIGNED",
           3: "GBF_ERR_UNSUPPORTED_SHAPE", 4: "GBF_ERR_WORKSPACE", 5: "GBF_ERR_CUDA",
           6: "GBF_ERR_TIMEOUT", 7: "GBF_ERR_NO_DEVICE"}
 PATH = {0: "none", 1: "persistent", 2: "swap_splitk", 3: "w4a16", 4: "pair",
-        5: "persistent_splitk", 6: "pair_1stream"}
+        5: "persistent_splitk", 6: "pair_1stream", 7: "pair_splitk"}
 
 EXPORTS = ("gemm_epilogue", "swiglu_dual_gemm", "w4a16_gemm", "gemm_epilogue_unfused",
            "swiglu_dual_gemm_unfused", "w4a16_gemm_unfused", "gbf_workspace_size",
@@ -319,10 +319,10 @@ def gbf_debug_force_splits(splits: int) -> int:
 
 def gbf_debug_force_path(path) -> int:
     """Force the dense kernel above the swapped range: "persistent",
-    "persistent_splitk", "pair", "pair_1stream", or None / "auto" for the
-    automatic choice."""
+    "persistent_splitk", "pair", "pair_1stream", "pair_splitk", or None /
+    "auto" for the automatic choice."""
     code = {None: 0, "auto": 0, "persistent": 1, "pair": 4,
-            "persistent_splitk": 5, "pair_1stream": 6}.get(path, path)
+            "persistent_splitk": 5, "pair_1stream": 6, "pair_splitk": 7}.get(path, path)
     return int(load().gbf_debug_force_path(int(code)))
 
 

@@ -71,6 +71,7 @@ gbf_status_t current_device(const DeviceInfo** info, unsigned** err) {
       d.info.sms = sms;
       d.info.pairs = (major == 10 && minor == 3) ? max_active_pairs() : 0;
       if (d.info.pairs <= 0) d.info.pairs = sms / 2;
+      d.info.quads = (major == 10 && minor == 3) ? max_active_quads() : 0;
       d.info.cc_major = major;
       d.info.cc_minor = minor;
       d.ready.store(true, std::memory_order_release);
@@ -238,7 +239,8 @@ gbf_status_t run_gemm(const void* A, const void* W, const void* W2, int layout, 
   const GemmPlan plan = plan_gemm(M, N, K, dual, kn, dev);
   CUtensorMap tmA, tmW, tmW2;
   const uint32_t a_rows = plan.path == kPathSwap ? plan.mpad : kBM;
-  const bool pair = plan.path == kPathPair || plan.path == kPathPairOne;
+  const bool pair =
+      plan.path == kPathPair || plan.path == kPathPairOne || plan.path == kPathPairSplit;
   if (!tmap_2d(&tmA, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, K, M, K * 2, kBK, a_rows,
                CU_TENSOR_MAP_SWIZZLE_128B))
     return GBF_ERR_CUDA;
@@ -384,6 +386,28 @@ GemmPlan persistent_plan(int64_t M, int64_t N, int64_t K, bool dual, bool split,
   return p;
 }
 
+// The one-stream pair kernel's split-K form: a cluster of two CTA pairs per
+// 256 x 256 tile, pair kp over the K half kp, one tile per cluster.
+GemmPlan pair_split_plan(int64_t M, int64_t N, int64_t K) {
+  GemmPlan p;
+  p.path = kPathPairSplit;
+  p.streams = 1;
+  p.bn = 256;
+  p.m_tiles = ceil_div(M, 2 * kBM);
+  p.n_tiles = ceil_div(N, 256);
+  p.num_kb = ceil_div(K, kBK);
+  p.splits = 2;
+  p.grid = 4 * p.m_tiles * p.n_tiles;
+  return p;
+}
+
+// Chosen only when every tile's cluster runs at once (one round) and K has
+// enough blocks to pay for the exchange of the partial sums.
+bool pair_split_fits(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo& dev) {
+  const int64_t tiles = static_cast<int64_t>(ceil_div(M, 2 * kBM)) * ceil_div(N, 256);
+  return !dual && dev.quads > 0 && tiles <= dev.quads && ceil_div(K, kBK) >= 8;
+}
+
 bool split_pays(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo& dev) {
   const int64_t tiles = static_cast<int64_t>(ceil_div(M, kBM)) * ceil_div(N, kPersistBN);
   return !dual && 2 * tiles <= dev.sms && ceil_div(K, kBK) >= 8;
@@ -397,6 +421,8 @@ bool split_pays(int64_t M, int64_t N, int64_t K, bool dual, const DeviceInfo& de
 double plan_time(const GemmPlan& p, bool dual, const DeviceInfo& dev) {
   if (p.path == kPathPersistentSplit)  // one round, half of K per SM, plus the exchange
     return 0.55 * 128.0 * 256.0 / 0.8;
+  if (p.path == kPathPairSplit)  // one round of pairs at one stream's rate, half of K
+    return 0.55 * 256.0 * 256.0 / 2.0 / 0.9;
   if (p.path == kPathPair) {
     const int64_t units = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
     const int64_t rounds = (units + dev.pairs - 1) / dev.pairs;
@@ -441,6 +467,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const De
   // few of them), unless a tuning hook forces one.
   const int force = g_force_path.load();
   if (force == kPathPersistentSplit && !dual) return persistent_plan(M, N, K, dual, true, dev);
+  if (force == kPathPairSplit && !dual && ceil_div(K, kBK) >= 2) return pair_split_plan(M, N, K);
   if (force == kPathPersistent) return persistent_plan(M, N, K, dual, false, dev);
   GemmPlan pp = persistent_plan(M, N, K, dual, split_pays(M, N, K, dual, dev), dev);
   if (dev.pairs <= 0) return pp;
@@ -453,6 +480,10 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool dual, bool kn, const De
     op.num_kb = pp.num_kb;
     if (force == kPathPairOne) return op;
     if (plan_time(op, dual, dev) < plan_time(best, dual, dev)) best = op;
+    if (pair_split_fits(M, N, K, dual, dev)) {
+      const GemmPlan sp = pair_split_plan(M, N, K);
+      if (plan_time(sp, dual, dev) < plan_time(best, dual, dev)) best = sp;
+    }
   }
   return best;
 }
@@ -890,7 +921,7 @@ gbf_status_t gbf_debug_force_splits(int splits) {
 
 gbf_status_t gbf_debug_force_path(int path) {
   if (path != 0 && path != kPathPersistent && path != kPathPair && path != kPathPersistentSplit &&
-      path != kPathPairOne)
+      path != kPathPairOne && path != kPathPairSplit)
     return GBF_ERR_INVALID_ARG;
   g_force_path.store(path);
   return GBF_OK;
@@ -904,8 +935,9 @@ int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int* 
   if (current_device(&d, &err) == GBF_OK) {
     dev = *d;
   } else {
-    dev.sms = 152;
+    dev.sms = 152;  // a GB300 (the planner's answer for a machine without one)
     dev.pairs = 76;
+    dev.quads = 32;
   }
   GemmPlan p;
   switch (op) {

@@ -54,6 +54,8 @@ constexpr int kQGroup = 8;
 constexpr int kQABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int kQThreads = 384;                 // warps 0-3 roles, 4-11 epilogue
 constexpr int kQTileM = 2 * kBM;               // 256 rows per pair tile
+constexpr int kQSplitHalf = 128;               // split-K: columns each K half finishes
+constexpr int kQSplitBytes = kQSplitHalf * kBM * 4;  // 64 KB: the other half's partial
 
 // Tile width BN (MMA N) of the pair: 256, or 224 when that fills the last
 // round of tiles better (the planner picks it for K-contiguous weights).
@@ -98,7 +100,7 @@ __device__ __forceinline__ void settle_after_abort() {
   while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
 }
 
-template <bool W_KN, bool DUAL, int BN, int STREAMS>
+template <bool W_KN, bool DUAL, int BN, int STREAMS, bool SPLIT>
 __global__ void __launch_bounds__(kQThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmO,
@@ -110,6 +112,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
   constexpr int kLoadBytes =
       kQStreams * kQABytes + (W_KN ? 2 * 64 * kBK * 2 : (BN / 2) * kBK * 2);
   static_assert(!DUAL || BN == 256, "narrow tiles only for the single product");
+  static_assert(!SPLIT || (!DUAL && BN == 256 && STREAMS == 1), "split-K: one stream, 256 wide");
+  static_assert(!SPLIT || kQStages * Cfg::kStageBytes >= 2 * kQSplitBytes, "park + receive");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
@@ -118,16 +122,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint64_t* tfull = empty + kQStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* recvb = done + 1;  // split-K: the other K half's partial pushed here
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(recvb + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   uint8_t* staging = smem + kQStages * Cfg::kStageBytes + Cfg::kBarBytes;  // 1024-aligned
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank() & 1u;
+  // CTA pairs are the cluster ranks {2i, 2i+1}; the split-K form runs two
+  // pairs per cluster of four, pair kp over the K half kp of the same tile.
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = crank & 1u;
+  const uint32_t lead = crank & ~1u;  // cluster rank of this pair's even CTA
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
   const bool leader = rank == 0;
-  const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
+  const int kp = SPLIT ? static_cast<int>(crank >> 1) : 0;
+  const int pair = SPLIT ? static_cast<int>(blockIdx.x >> 2) : static_cast<int>(blockIdx.x >> 1);
+  const int npairs = SPLIT ? static_cast<int>(gridDim.x >> 2) : static_cast<int>(gridDim.x >> 1);
+  const int kb_begin = SPLIT ? (kp * a.num_kb) / 2 : 0;
+  const int kb_end = SPLIT ? ((kp + 1) * a.num_kb) / 2 : a.num_kb;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQStages; ++i) {
@@ -139,6 +152,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_init(&tempty[i], 16);  // 8 epilogue warps in each CTA of the pair
     }
     mbar_init(done, kQStreams);
+    if (SPLIT) {
+      mbar_init(recvb, 1);
+      mbar_arrive_expect_tx(recvb, kQSplitBytes);  // the other K half's 128 x 128 partial
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -160,7 +177,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // units: STREAMS M-tiles (the last unit's second tile may be empty) x one N-tile
   const int m_pairs = (a.m_tiles + kQStreams - 1) / kQStreams;
   const int num_super = m_pairs * a.n_tiles;
-  const int num_kb = a.num_kb;
   const int out_bn = DUAL ? 128 : BN;
   if (threadIdx.x == 0) griddep_launch_dependents();
 
@@ -179,14 +195,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
       for (int t = pair; t < num_super && ok; t += npairs) {
         int mp, nb;
         tile_coords(t, m_pairs, a.n_tiles, mp, nb, kQGroup);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bar(&empty[s], ph ^ 1, ctl, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
           uint8_t* sa = stages + s * Cfg::kStageBytes;
           uint8_t* sb = sa + kQStreams * kQABytes;
-          const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead);
           if (leader) mbar_arrive_expect_tx(&full[s], 2 * kLoadBytes);
 #pragma unroll
           for (int i = 0; i < kQStreams; ++i)  // rows past M read as zeros
@@ -236,7 +252,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const uint32_t d = tmem_base + acc * 256;
         if (!wait_bar(&tempty[acc], ((l >> 1) & 1) ^ 1, ctl, kSiteMmaAccEmpty)) break;
         tc_fence_after();
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
             ok = false;
             break;
@@ -250,22 +266,22 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = W_KN ? sdesc_sw128(b0 + k * 2048, 8192, 1024)
                                      : sdesc_sw128(b0 + k * 32, 16, 1024);
-            mma_ss_pair(d, ad, bd, idesc, (kb | k) != 0);
+            mma_ss_pair(d, ad, bd, idesc, (kb != kb_begin || k != 0) ? 1u : 0u);
           }
-          mma_commit_pair(&empty[s], 0x3);
+          mma_commit_pair(&empty[s], pair_mask);
           if (++s == kQStages) {
             s = 0;
             ph ^= 1;
           }
         }
         if (!ok) break;
-        if (!(a.ctl.inject && l == 0)) mma_commit_pair(&tfull[acc], 0x3);
+        if (!(a.ctl.inject && l == 0)) mma_commit_pair(&tfull[acc], pair_mask);
       }
-      mma_commit_pair(done, 0x1);
+      mma_commit_pair(done, static_cast<uint16_t>(1u << lead));
       wait_bar(done, 0, ctl, kSiteDrain, false);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && !SPLIT) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     // the pair's tiles in order: local tile l belongs to stream l % 2
     griddep_wait();  // the ending reads C, bias, residual and writes out
@@ -276,8 +292,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     constexpr int kFirst = (kChunks + 1) / 2;  // chunks of warpgroup 0; the rest go to 1
     const int c_begin = half == 0 ? 0 : kFirst;
     const int c_end = half == 0 ? kFirst : kChunks;
-    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0),
-                                       mapa_shared(smem_u32(&tempty[1]), 0)};
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), lead),
+                                       mapa_shared(smem_u32(&tempty[1]), lead)};
     uint8_t* my_staging = staging + (warp - 4) * 2 * kStageChunkBytes;
     int flip = 0;
     // tile l of the pair: unit pair + (l / STREAMS) * npairs, M-tile l % STREAMS
@@ -329,6 +345,96 @@ __global__ void __launch_bounds__(kQThreads, 1)
     __syncwarp();
   }
 
+  if constexpr (SPLIT) {
+    // ------------------------------------------------------------ split-K exchange + ending
+    // One tile per cluster.  The CTA of K half kp finishes columns
+    // [128 kp, 128 kp + 128) of its 128 rows: it parks the other 128 columns
+    // of its partial as [column][row] fp32 in its idle ring (consecutive
+    // lanes on consecutive words), one thread pushes them with four 16 KB
+    // bulk copies to the CTA holding the same rows in the other pair
+    // (cluster rank crank ^ 2), and each CTA adds the copy it received to its
+    // own columns, K half 0's partial first in both (the result does not
+    // depend on which CTA finishes which columns).
+    const bool epi = warp >= 4;
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;  // warpgroup: chunks 2*half, 2*half + 1 of the 128 columns
+    const int rl = q * 32 + lane;      // row within the CTA's 128 = TMEM lane
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);  // accumulator 0
+    float* park = reinterpret_cast<float*>(stages);
+    const float* recv = reinterpret_cast<const float*>(stages + kQSplitBytes);
+    const bool have_tile = pair < num_super;
+    int mp = 0, nb = 0;
+    if (have_tile) tile_coords(pair, m_pairs, a.n_tiles, mp, nb, kQGroup);
+    const uint64_t pol = l2_evict_first_policy();
+    const int64_t row =
+        static_cast<int64_t>(mp) * kQTileM + static_cast<int>(rank) * kBM + rl;
+    const int mine = kp * kQSplitHalf;         // first column this CTA finishes
+    const int theirs = kQSplitHalf - mine;     // the counterpart's first column
+    if (epi) {
+      griddep_wait();  // the ending reads C, bias, residual and writes out
+      if (have_tile)
+        epi_row_l2_prefetch(row, nb * 256 + mine + half * 64, nb * 256 + mine + half * 64 + 64,
+                            a.M, a.N, a.ep);
+      wait_bar(&tfull[0], 0, ctl, kSiteEpiAccFull);
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
+        uint32_t v[32];
+        tmem_ld32(tb + theirs + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) park[(c * 32 + j) * kBM + rl] = __uint_as_float(v[j]);
+      }
+      fence_proxy_async_smem();  // the bulk copies read what these threads wrote
+    }
+    cluster_sync_all();  // every CTA of the cluster parked, every receive barrier armed
+    if (threadIdx.x == 128) {
+      const uint32_t peer = crank ^ 2u;
+      constexpr int kPiece = kQSplitBytes / 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        bulk_copy_to_peer(mapa_shared(smem_u32(stages + kQSplitBytes + i * kPiece), peer),
+                          smem_u32(stages + i * kPiece), kPiece,
+                          mapa_shared(smem_u32(recvb), peer));
+    }
+    if (epi) {
+      uint8_t* my_staging = staging + (warp - 4) * 2 * kStageChunkBytes;
+      int flip = 0;
+      // not cut short by the abort flag: the counterpart sends whatever its state
+      wait_bar(recvb, 0, ctl, kSiteEpiAccFull, /*honor_abort=*/false);
+      RowLoads L;
+      epi_row_prefetch(L, row, nb * 256 + mine + 2 * half * 32, a.M, a.N, a.ep, pol);
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
+        const int col0 = nb * 256 + mine + c * 32;
+        uint32_t own[32], sum[32];
+        tmem_ld32(tb + mine + c * 32, own);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float o = __uint_as_float(own[j]);
+          const float p = recv[(c * 32 + j) * kBM + rl];
+          sum[j] = __float_as_uint(kp == 0 ? o + p : p + o);
+        }
+        const RowLoads cur = L;
+        if (cc == 0) epi_row_prefetch(L, row, col0 + 32, a.M, a.N, a.ep, pol);
+        uint32_t w[16];
+        switch (a.ep.act) {
+          case kActRelu: epi_row32_pack<kActRelu, false>(sum, sum, cur, a.ep, w); break;
+          case kActSilu: epi_row32_pack<kActSilu, false>(sum, sum, cur, a.ep, w); break;
+          case kActGeluTanh: epi_row32_pack<kActGeluTanh, false>(sum, sum, cur, a.ep, w); break;
+          default: epi_row32_pack<kActIdentity, false>(sum, sum, cur, a.ep, w); break;
+        }
+        if (have_tile) store_chunk32(my_staging, flip, w, &tmO, row - lane, col0, a.M, a.N, pol);
+      }
+      // every staged chunk written to global memory before the CTA may exit
+      if (lane == 0) bulk_wait<0>();
+      __syncwarp();
+    }
+  }
+
   if (ctl.prof && threadIdx.x == 0) atomicAdd(&ctl.prof[31], static_cast<unsigned long long>(clock64() - t_start));
   tc_fence_before();
   __syncthreads();
@@ -341,12 +447,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 namespace {
 
-template <bool W_KN, bool DUAL, int BN, int STREAMS = 2>
+template <bool W_KN, bool DUAL, int BN, int STREAMS = 2, bool SPLIT = false>
 cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
                      const CUtensorMap& tmW2, const CUtensorMap& tmO, const PairArgs& args,
                      cudaStream_t stream) {
   static std::atomic<uint64_t> mask{0};
-  auto kernel = gemm_pair_kernel<W_KN, DUAL, BN, STREAMS>;
+  auto kernel = gemm_pair_kernel<W_KN, DUAL, BN, STREAMS, SPLIT>;
   constexpr int kQSmem = PairCfg<BN, STREAMS>::kSmem;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -364,7 +470,7 @@ cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMa
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = SPLIT ? 4 : 2;  // split-K: two pairs per tile
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   // may start while the previous kernel in the stream finishes (it waits
@@ -378,21 +484,23 @@ cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMa
 
 }  // namespace
 
-int max_active_pairs() {
-  // Clusters of two 1-SM CTAs that fit on the device at once.
+namespace {
+
+// Clusters of `size` 1-SM CTAs of the pair kernel that fit on the device at once.
+int max_active_clusters(int size) {
   cudaLaunchConfig_t cfg = {};
   constexpr int kQSmem = PairCfg<256>::kSmem;
-  cfg.gridDim = dim3(2, 1, 1);
+  cfg.gridDim = dim3(size, 1, 1);
   cfg.blockDim = dim3(kQThreads, 1, 1);
   cfg.dynamicSmemBytes = kQSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = size;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto kernel = gemm_pair_kernel<false, false, 256, 2>;
+  auto kernel = gemm_pair_kernel<false, false, 256, 2, false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return 0;
@@ -401,11 +509,19 @@ int max_active_pairs() {
   return n;
 }
 
+}  // namespace
+
+int max_active_pairs() { return max_active_clusters(2); }
+int max_active_quads() { return max_active_clusters(4); }
+
 cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const CUtensorMap& tmA,
                              const CUtensorMap& tmW, const CUtensorMap& tmW2,
                              const CUtensorMap& tmO, const EpiParams& ep, int M, int N, int K,
                              const KernelCtl& ctl, cudaStream_t stream) {
   PairArgs args{M, N, K, plan.m_tiles, plan.n_tiles, plan.num_kb, ep, ctl};
+  if (plan.path == kPathPairSplit)  // split-K: clusters of two pairs, one tile each
+    return w_kn ? run_pair<true, false, 256, 1, true>(plan, tmA, tmW, tmW2, tmO, args, stream)
+                : run_pair<false, false, 256, 1, true>(plan, tmA, tmW, tmW2, tmO, args, stream);
   if (plan.streams == 1 && !dual)  // one stream: units of one 256-row M-tile
     return w_kn ? run_pair<true, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream)
            : plan.bn == 224

@@ -40,6 +40,7 @@ enum Path {
   kPathPair = 4,
   kPathPersistentSplit = 5,  // the one-SM persistent kernel, K split over a CTA pair per tile
   kPathPairOne = 6,          // the CTA-pair kernel with one MMA stream (units of one M-tile)
+  kPathPairSplit = 7,        // the one-stream CTA-pair kernel, K split over two pairs per tile
 };
 
 struct GemmPlan {
@@ -57,6 +58,7 @@ struct GemmPlan {
 struct DeviceInfo {
   int sms = 0;
   int pairs = 0;  // CTA pairs (clusters of two 1-SM CTAs) that fit at once
+  int quads = 0;  // clusters of four 1-SM CTAs (two pairs) that fit at once
   int cc_major = 0;
   int cc_minor = 0;
 };
@@ -90,6 +92,7 @@ cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const C
                              const CUtensorMap& tmO, const EpiParams& ep, int M, int N, int K,
                              const KernelCtl& ctl, cudaStream_t stream);
 int max_active_pairs();
+int max_active_quads();
 
 // Weight-only quantised GEMM (wq_gemm.cu).  tmA: activations; tmQ: the
 // weight codes (int4, nvfp4: [K][N/2] bytes; fp8: [K][N]); tmS: scales

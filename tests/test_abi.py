@@ -85,12 +85,14 @@ def test_workspace_sizes(lib):
 def test_kernel_path_planning(lib):
     assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096) == ("pair", 1)
     # mid-size M: the pair kernel's 512 x 256 units would leave most SMs idle,
-    # and 128 x 256 tiles fill at most half of them: two CTAs per tile (split K)
-    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096) == ("persistent_splitk", 2)
-    assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 4096) == ("persistent_splitk", 2)
+    # and the 256 x 256 tiles fit one round of clusters of two CTA pairs:
+    # each pair over half of K (split K)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096) == ("pair_splitk", 2)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 4096) == ("pair_splitk", 2)
     assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 4096, 4096)[0] == "pair_1stream"
     # too little K to pay for the exchange of the partial sums
-    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 256)[0] != "persistent_splitk"
+    assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 256)[0] not in ("pair_splitk",
+                                                                          "persistent_splitk")
     assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 8192, 8192, "kn") == ("pair", 1)
     path, splits = gbf.gbf_kernel_path("gemm_epilogue", 16, 8192, 8192, "kn")
     assert path == "swap_splitk" and 1 <= splits <= 8
@@ -158,8 +160,13 @@ def test_force_path_hook(lib):
         assert gbf.gbf_debug_force_path("pair") == 0
         assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096)[0] == "pair"
         assert gbf.gbf_kernel_path("swiglu", 200, 14336, 4096)[0] == "pair"
+        assert gbf.gbf_debug_force_path("pair_splitk") == 0
+        assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 4096) == ("pair_splitk", 2)
+        # one K block cannot be split over two pairs
+        assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 64)[0] != "pair_splitk"
+        assert gbf.gbf_kernel_path("swiglu", 512, 4096, 4096)[0] != "pair_splitk"
         assert gbf.gbf_debug_force_path(2) == 1  # GBF_ERR_INVALID_ARG
-        assert gbf.gbf_debug_force_path(7) == 1
+        assert gbf.gbf_debug_force_path(8) == 1
     finally:
         gbf.gbf_debug_force_path(None)
     assert gbf.gbf_kernel_path("gemm_epilogue", 4096, 4096, 4096)[0] == "pair"
@@ -167,17 +174,21 @@ def test_force_path_hook(lib):
 
 @pytest.mark.parametrize("op,M,N,K,layout,want", [
     # measured on one GB300 with every kernel forced, TFLOP/s
-    # (CTA pair / one-SM / one-SM split-K / CTA pair with one stream):
-    ("gemm_epilogue", 512, 4096, 4096, "nk", "persistent_splitk"),   # 408 / 523 / 707 / 614
+    # (CTA pair / one-SM / one-SM split-K / CTA pair with one stream /
+    # its split-K form over two pairs per tile):
+    ("gemm_epilogue", 256, 4096, 4096, "nk", "pair_splitk"),         # 209 / 265 / 379 / 322 / 450
+    ("gemm_epilogue", 384, 4096, 4096, "nk", "pair_splitk"),         # 314 / 399 / 565 / 482 / 646
+    ("gemm_epilogue", 512, 4096, 4096, "nk", "pair_splitk"),         # 410 / 527 / 720 / 641 / 850
+    ("gemm_epilogue", 512, 2048, 2048, "nk", "pair_splitk"),         # 159 / 209 / 261 / 249 / 308
     ("gemm_epilogue", 640, 4096, 4096, "nk", "pair_1stream"),        # 508 / 655 / 547 / 792
     ("gemm_epilogue", 1024, 4096, 4096, "nk", "pair_1stream"),       # 809 / 1044 / 802 / 1236
     ("gemm_epilogue", 1536, 4096, 4096, "nk", "pair"),               # 1185 / 927 / 838 / 1049
     ("gemm_epilogue", 2048, 4096, 4096, "nk", "pair"),               # 1564 / 1218 / 862 / 1395
-    ("gemm_epilogue", 256, 8192, 8192, "kn", "persistent_splitk"),   # 428 / 620 / 913 / -
-    ("gemm_epilogue", 512, 8192, 8192, "kn", "pair_1stream"),        # 845 / 1196 / 1051 / 1432
+    ("gemm_epilogue", 256, 8192, 8192, "kn", "pair_splitk"),         # 486 / 620 / 925 / 738 / 1077
+    ("gemm_epilogue", 512, 8192, 8192, "kn", "pair_1stream"),        # 958 / 1220 / 1050 / 1411 / 1157
     ("gemm_epilogue", 768, 8192, 8192, "kn", "pair"),                # 1240 / 1014 / 1095 / 1179
     ("gemm_epilogue", 1536, 8192, 8192, "kn", "pair_1stream"),       # 1283 / 1360 / 1185 / 1587
-    ("gemm_epilogue", 384, 14336, 4096, "nk", "pair"),               # 1019 / 744 / 709 / 911
+    ("gemm_epilogue", 384, 14336, 4096, "nk", "pair"),               # 1021 / 737 / 708 / 931 / 594
     ("gemm_epilogue", 640, 14336, 4096, "nk", "persistent"),         # 925 / 1274 / 899 / 1070
     ("gemm_epilogue", 1024, 14336, 4096, "nk", "pair_1stream"),      # 1453 / 1434 / 985 / 1590
     # earlier measurements (pair / one-SM), still the planner's choice:

@@ -113,6 +113,43 @@ def test_persistent_splitk_in_place_residual(cuda_lib):
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,N,K", [(512, 4096, 512), (300, 520, 200), (257, 264, 136),
+                                   (700, 1000, 1000), (256, 256, 128), (1030, 2056, 392)])
+def test_cta_pair_kernel_split_k(cuda_lib, layout, M, N, K):
+    # two CTA pairs per 256 x 256 tile (a cluster of four), each pair over
+    # half of the K blocks (3 blocks split 1 + 2, ragged last blocks), each
+    # CTA finishing half of its rows' columns after a bulk-copy exchange with
+    # the CTA of the other pair; more clusters than fit at once in the last case
+    run_and_check(cuda_lib, M, N, K, layout, "gelu_tanh", 0.75, 0.5, seed=M + 13 * N + K,
+                  expect_path="pair_splitk", force_path="pair_splitk")
+
+
+@pytest.mark.parametrize("act", ["identity", "relu", "silu", "gelu_tanh"])
+@pytest.mark.parametrize("opts", [(False, False, False), (True, True, True)])
+def test_cta_pair_split_k_every_ending(cuda_lib, act, opts):
+    c, bias, res = opts
+    run_and_check(cuda_lib, 384, 520, 384, "nk", act, 1.25, 0.5, seed=35, c=c, bias=bias,
+                  res=res, expect_path="pair_splitk", force_path="pair_splitk")
+
+
+def test_cta_pair_split_k_in_place_residual(cuda_lib):
+    M, N, K = 300, 264, 512
+    A, B, C, bi, r = case(M, N, K, "kn", 811)
+    out = up(r)  # residual == out
+    assert cuda_lib.gbf_debug_force_path("pair_splitk") == 0
+    try:
+        assert cuda_lib.gbf_kernel_path("gemm_epilogue", M, N, K, "kn")[0] == "pair_splitk"
+        cuda_lib.gemm_epilogue(up(A), up(B), "kn", up(C), up(bi), out, out, M, N, K, 0.5, 1.0,
+                               "silu")
+    finally:
+        cuda_lib.gbf_debug_force_path(None)
+    assert cuda_lib.gbf_check_device_error() == 0
+    ref = oracle.gemm_epilogue(A, B, "kn", C, bi, r, M=M, N=N, K=K, alpha=0.5, beta=1.0,
+                               act="silu")
+    assert_parity(down(out), ref, "pair split-K in-place residual")
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("M,N,K", [(512, 2048, 256), (1000, 2000, 320)])
 def test_cta_pair_kernel_224_wide_tiles(cuda_lib, layout, M, N, K):
     # shapes whose last round of 256-wide tiles is thin, so the planner takes

@@ -219,3 +219,31 @@ def test_one_stream_pair_kernel_timeout_is_reported_and_recoverable(cuda_lib):
         cuda_lib.gbf_debug_force_path(None)
     assert cuda_lib.gbf_check_device_error() == 0
     assert_parity(down(out), oracle.gemm_epilogue(A, B, "nk", M=M, N=N, K=K), "after timeout")
+
+
+def test_pair_split_k_timeout_is_reported_and_recoverable(cuda_lib):
+    # the split-K form of the CTA-pair kernel (clusters of two pairs): a
+    # withheld accumulator-ready signal must end in GBF_ERR_TIMEOUT (the
+    # partial-sum exchange still completes), and the next call on the same
+    # context must be correct
+    M, N, K = 512, 1024, 256
+    A = rand_bf16(73, (M, K))
+    B = rand_bf16(74, (N, K), std=K ** -0.5)
+    out = poison_bf16(M, N)
+    assert cuda_lib.gbf_debug_force_path("pair_splitk") == 0
+    try:
+        assert cuda_lib.gbf_kernel_path("gemm_epilogue", M, N, K, "nk")[0] == "pair_splitk"
+        cuda_lib.gbf_set_wait_timeout_ns(20_000_000)
+        cuda_lib.gbf_debug_inject_timeout(True)
+        try:
+            cuda_lib.gemm_epilogue(up(A), up(B), "nk", None, None, None, out, M, N, K)
+            assert cuda_lib.gbf_check_device_error() == 6
+        finally:
+            cuda_lib.gbf_debug_inject_timeout(False)
+            cuda_lib.gbf_set_wait_timeout_ns(2_000_000_000)
+        assert cuda_lib.gbf_check_device_error() == 0
+        cuda_lib.gemm_epilogue(up(A), up(B), "nk", None, None, None, out, M, N, K)
+    finally:
+        cuda_lib.gbf_debug_force_path(None)
+    assert cuda_lib.gbf_check_device_error() == 0
+    assert_parity(down(out), oracle.gemm_epilogue(A, B, "nk", M=M, N=N, K=K), "after timeout")
