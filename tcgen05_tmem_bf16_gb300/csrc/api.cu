@@ -937,7 +937,7 @@ int gbf_kernel_path(int op, int64_t M, int64_t N, int64_t K, int b_layout, int* 
   } else {
     dev.sms = 152;  // a GB300 (the planner's answer for a machine without one)
     dev.pairs = 76;
-    dev.quads = 32;
+    dev.quads = 36;
   }
   GemmPlan p;
   switch (op) {

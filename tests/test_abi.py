@@ -90,6 +90,9 @@ def test_kernel_path_planning(lib):
     assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 4096) == ("pair_splitk", 2)
     assert gbf.gbf_kernel_path("gemm_epilogue", 512, 4096, 4096) == ("pair_splitk", 2)
     assert gbf.gbf_kernel_path("gemm_epilogue", 1024, 4096, 4096)[0] == "pair_1stream"
+    # 37 tiles of 256 x 256: one more than the 36 clusters of two pairs that
+    # fit at once, so the one-SM kernel's split-K form (74 tiles, 148 CTAs)
+    assert gbf.gbf_kernel_path("gemm_epilogue", 256, 256 * 37, 4096) == ("persistent_splitk", 2)
     # too little K to pay for the exchange of the partial sums
     assert gbf.gbf_kernel_path("gemm_epilogue", 300, 4096, 256)[0] not in ("pair_splitk",
                                                                           "persistent_splitk")
