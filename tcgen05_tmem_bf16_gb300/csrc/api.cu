@@ -345,6 +345,9 @@ GemmPlan pair_plan(int64_t M, int64_t N, bool dual, bool kn, const DeviceInfo& d
       p.n_tiles = ceil_div(N, 224);
     }
     p.grid = 2 * std::min(p.m_tiles * p.n_tiles, dev.pairs);
+    // one tile per pair: the two accumulators need not alternate between
+    // tiles, so two MMA streams share the tile's K blocks
+    p.kpar = static_cast<int64_t>(p.m_tiles) * p.n_tiles <= dev.pairs;
     return p;
   }
   if (!dual) {

@@ -94,13 +94,27 @@ struct PairArgs {
   KernelCtl ctl;
 };
 
+// v[j] += the fp32 accumulator column j of this thread's lane at taddr
+// (32 columns, read 16 at a time to keep registers free).
+__device__ __forceinline__ void add_acc32(uint32_t taddr, uint32_t (&v)[32]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t o[16];
+    tmem_ld16(taddr + 16 * h, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      v[16 * h + j] = __float_as_uint(__uint_as_float(v[16 * h + j]) + __uint_as_float(o[j]));
+  }
+}
+
 // Let in-flight copies land before an aborted CTA exits (bounded: ~2 ms).
 __device__ __forceinline__ void settle_after_abort() {
   const uint64_t t0 = globaltimer_ns();
   while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
 }
 
-template <bool W_KN, bool DUAL, int BN, int STREAMS, bool SPLIT>
+template <bool W_KN, bool DUAL, int BN, int STREAMS, bool SPLIT, bool KPAR>
 __global__ void __launch_bounds__(kQThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmO,
@@ -113,6 +127,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       kQStreams * kQABytes + (W_KN ? 2 * 64 * kBK * 2 : (BN / 2) * kBK * 2);
   static_assert(!DUAL || BN == 256, "narrow tiles only for the single product");
   static_assert(!SPLIT || (!DUAL && BN == 256 && STREAMS == 1), "split-K: one stream, 256 wide");
+  static_assert(!KPAR || (!DUAL && STREAMS == 1 && !SPLIT), "two K streams: one M-tile per unit");
+  // MMA issuing threads: two streams of M-tiles, or (KPAR) two streams over
+  // the alternate K blocks of the same tile, one accumulator each
+  constexpr int kIssuers = (STREAMS == 2 || KPAR) ? 2 : 1;
   static_assert(!SPLIT || kQStages * Cfg::kStageBytes >= 2 * kQSplitBytes, "park + receive");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -141,6 +159,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int npairs = SPLIT ? static_cast<int>(gridDim.x >> 2) : static_cast<int>(gridDim.x >> 1);
   const int kb_begin = SPLIT ? (kp * a.num_kb) / 2 : 0;
   const int kb_end = SPLIT ? ((kp + 1) * a.num_kb) / 2 : a.num_kb;
+  // KPAR: K block kb_begin + i goes to stream i % 2; the second stream (and
+  // its accumulator) takes part only when there are two blocks or more
+  const bool two_k = KPAR && kb_end - kb_begin >= 2;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQStages; ++i) {
@@ -151,7 +172,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 16);  // 8 epilogue warps in each CTA of the pair
     }
-    mbar_init(done, kQStreams);
+    mbar_init(done, (KPAR && !two_k) ? 1 : kIssuers);
     if (SPLIT) {
       mbar_init(recvb, 1);
       mbar_arrive_expect_tx(recvb, kQSplitBytes);  // the other K half's 128 x 128 partial
@@ -238,35 +259,48 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // of unit l / STREAMS, accumulated in accumulator l & 1.  With two streams
     // warp 1 lane 0 issues the even tiles and warp 2 lane 0 the odd ones from
     // the same stages (each stream keeps its accumulator); with one stream
-    // warp 1 issues every tile, alternating accumulators.  Warp 2 also
-    // allocates and frees the tensor memory, outside this loop.
+    // warp 1 issues every tile, alternating accumulators.  With two K
+    // streams (KPAR) both issue every tile, warp 1 lane 0 its even and warp 2
+    // lane 0 its odd K blocks, each into its own accumulator, and the ending
+    // adds the two.  Warp 2 also allocates and frees the tensor memory,
+    // outside this loop.
     const int st = warp - 1;
-    if (lane == 0 && leader && st < kQStreams) {
+    if (lane == 0 && leader && st < kIssuers && (!KPAR || st == 0 || two_k)) {
       constexpr uint32_t idesc = idesc_bf16(kQTileM, BN, false, W_KN);
       int s = 0;
       uint32_t ph = 0;
       int l = st;
       bool ok = true;
-      for (int t = pair; t < num_super && ok; t += npairs, l += kQStreams) {
-        const int acc = l & 1;
+      for (int t = pair, u = 0; t < num_super && ok; t += npairs, l += kQStreams, ++u) {
+        const int acc = KPAR ? st : (l & 1);
         const uint32_t d = tmem_base + acc * 256;
-        if (!wait_bar(&tempty[acc], ((l >> 1) & 1) ^ 1, ctl, kSiteMmaAccEmpty)) break;
+        // uses of this accumulator so far: KPAR one per unit, else every other tile
+        const int use = KPAR ? u : (l >> 1);
+        if (!wait_bar(&tempty[acc], (use & 1) ^ 1, ctl, kSiteMmaAccEmpty)) break;
         tc_fence_after();
         for (int kb = kb_begin; kb < kb_end; ++kb) {
+          if (KPAR && ((kb - kb_begin) & 1) != st) {  // the other stream's block
+            if (++s == kQStages) {
+              s = 0;
+              ph ^= 1;
+            }
+            continue;
+          }
           if (!wait_bar(&full[s], ph, ctl, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t s0 = smem_u32(stages + s * Cfg::kStageBytes);
-          const uint32_t a0 = s0 + st * kQABytes;
+          const uint32_t a0 = s0 + (KPAR ? 0 : st) * kQABytes;  // this stream's M-tile
           const uint32_t b0 = s0 + kQStreams * kQABytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = W_KN ? sdesc_sw128(b0 + k * 2048, 8192, 1024)
                                      : sdesc_sw128(b0 + k * 32, 16, 1024);
-            mma_ss_pair(d, ad, bd, idesc, (kb != kb_begin || k != 0) ? 1u : 0u);
+            // the stream's first K step overwrites the accumulator
+            mma_ss_pair(d, ad, bd, idesc, (kb != kb_begin + (KPAR ? st : 0) || k != 0) ? 1u : 0u);
           }
           mma_commit_pair(&empty[s], pair_mask);
           if (++s == kQStages) {
@@ -275,7 +309,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
         }
         if (!ok) break;
-        if (!(a.ctl.inject && l == 0)) mma_commit_pair(&tfull[acc], pair_mask);
+        if (!(a.ctl.inject && l == 0 && u == 0)) mma_commit_pair(&tfull[acc], pair_mask);
       }
       mma_commit_pair(done, static_cast<uint16_t>(1u << lead));
       wait_bar(done, 0, ctl, kSiteDrain, false);
@@ -298,12 +332,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
     int flip = 0;
     // tile l of the pair: unit pair + (l / STREAMS) * npairs, M-tile l % STREAMS
     // of it, in accumulator l & 1 (use (l >> 1) of that accumulator)
+    // (KPAR: tile l in both accumulators, use l of each, summed here)
     for (int local = 0; pair + (local / kQStreams) * npairs < num_super; ++local) {
-      const int st = local & 1;  // accumulator
+      const int st = KPAR ? 0 : (local & 1);  // accumulator
       int mp, nb;
       tile_coords(pair + (local / kQStreams) * npairs, m_pairs, a.n_tiles, mp, nb, kQGroup);
       const int mb = kQStreams * mp + local % kQStreams;
-      const uint32_t aph = (local >> 1) & 1;
+      const uint32_t aph = KPAR ? (local & 1) : ((local >> 1) & 1);
       const int64_t row =
           static_cast<int64_t>(mb) * kQTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
       epi_row_l2_prefetch(row, nb * out_bn + c_begin * 32, nb * out_bn + c_end * 32, a.M, a.N,
@@ -311,6 +346,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       RowLoads L;
       epi_row_prefetch(L, row, nb * out_bn + c_begin * 32, a.M, a.N, a.ep, pol);
       if (!wait_bar(&tfull[st], aph, ctl, kSiteEpiAccFull)) break;
+      if (two_k && !wait_bar(&tfull[1], aph, ctl, kSiteEpiAccFull)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + st * 256 + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
@@ -320,12 +356,19 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_ld32(tb + c * 32, acc);
         if constexpr (DUAL) tmem_ld32(tb + 128 + c * 32, up);
         tmem_wait_ld();
+        if constexpr (KPAR) {
+          if (two_k) add_acc32(tb + 256 + c * 32, acc);  // the odd K blocks' accumulator
+        }
         if (c == c_end - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
             if (leader) mbar_arrive(&tempty[st]);
             else mbar_arrive_cluster(tempty_leader[st]);
+            if (two_k) {
+              if (leader) mbar_arrive(&tempty[1]);
+              else mbar_arrive_cluster(tempty_leader[1]);
+            }
           }
         }
         const RowLoads cur = L;
@@ -409,12 +452,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * half + cc;
         const int col0 = nb * 256 + mine + c * 32;
-        uint32_t own[32], sum[32];
-        tmem_ld32(tb + mine + c * 32, own);
+        uint32_t sum[32];  // this CTA's partial, then the total
+        tmem_ld32(tb + mine + c * 32, sum);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float o = __uint_as_float(own[j]);
+          const float o = __uint_as_float(sum[j]);
           const float p = recv[(c * 32 + j) * kBM + rl];
           sum[j] = __float_as_uint(kp == 0 ? o + p : p + o);
         }
@@ -447,12 +490,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
 namespace {
 
-template <bool W_KN, bool DUAL, int BN, int STREAMS = 2, bool SPLIT = false>
+template <bool W_KN, bool DUAL, int BN, int STREAMS = 2, bool SPLIT = false, bool KPAR = false>
 cudaError_t run_pair(const GemmPlan& p, const CUtensorMap& tmA, const CUtensorMap& tmW,
                      const CUtensorMap& tmW2, const CUtensorMap& tmO, const PairArgs& args,
                      cudaStream_t stream) {
   static std::atomic<uint64_t> mask{0};
-  auto kernel = gemm_pair_kernel<W_KN, DUAL, BN, STREAMS, SPLIT>;
+  auto kernel = gemm_pair_kernel<W_KN, DUAL, BN, STREAMS, SPLIT, KPAR>;
   constexpr int kQSmem = PairCfg<BN, STREAMS>::kSmem;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -500,7 +543,7 @@ int max_active_clusters(int size) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto kernel = gemm_pair_kernel<false, false, 256, 2, false>;
+  auto kernel = gemm_pair_kernel<false, false, 256, 2, false, false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return 0;
@@ -522,6 +565,14 @@ cudaError_t launch_gemm_pair(const GemmPlan& plan, bool w_kn, bool dual, const C
   if (plan.path == kPathPairSplit)  // split-K: clusters of two pairs, one tile each
     return w_kn ? run_pair<true, false, 256, 1, true>(plan, tmA, tmW, tmW2, tmO, args, stream)
                 : run_pair<false, false, 256, 1, true>(plan, tmA, tmW, tmW2, tmO, args, stream);
+  if (plan.streams == 1 && !dual && plan.kpar)  // one tile per pair: two K streams
+    return w_kn ? run_pair<true, false, 256, 1, false, true>(plan, tmA, tmW, tmW2, tmO, args,
+                                                             stream)
+           : plan.bn == 224
+               ? run_pair<false, false, 224, 1, false, true>(plan, tmA, tmW, tmW2, tmO, args,
+                                                             stream)
+               : run_pair<false, false, 256, 1, false, true>(plan, tmA, tmW, tmW2, tmO, args,
+                                                             stream);
   if (plan.streams == 1 && !dual)  // one stream: units of one 256-row M-tile
     return w_kn ? run_pair<true, false, 256, 1>(plan, tmA, tmW, tmW2, tmO, args, stream)
            : plan.bn == 224

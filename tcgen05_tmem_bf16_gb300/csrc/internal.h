@@ -53,6 +53,7 @@ struct GemmPlan {
   int grid = 0;      // persistent kernels: CTAs
   int bn = 256;      // pair kernel: tile width (MMA N)
   int streams = 2;   // pair kernel: M-tiles (MMA streams) per unit of work
+  bool kpar = false; // one-stream pair kernel: two MMA streams over alternate K blocks
 };
 
 struct DeviceInfo {

@@ -183,12 +183,13 @@ def test_force_path_hook(lib):
     ("gemm_epilogue", 384, 4096, 4096, "nk", "pair_splitk"),         # 314 / 399 / 565 / 482 / 646
     ("gemm_epilogue", 512, 4096, 4096, "nk", "pair_splitk"),         # 410 / 527 / 720 / 641 / 850
     ("gemm_epilogue", 512, 2048, 2048, "nk", "pair_splitk"),         # 159 / 209 / 261 / 249 / 308
-    ("gemm_epilogue", 640, 4096, 4096, "nk", "pair_1stream"),        # 508 / 655 / 547 / 792
-    ("gemm_epilogue", 1024, 4096, 4096, "nk", "pair_1stream"),       # 809 / 1044 / 802 / 1236
+    ("gemm_epilogue", 640, 4096, 4096, "nk", "pair_1stream"),        # 508 / 654 / 544 / 815 / 572
+    ("gemm_epilogue", 768, 4096, 4096, "nk", "pair_1stream"),        # 610 / 784 / 624 / 969 / 682
+    ("gemm_epilogue", 1024, 4096, 4096, "nk", "pair_1stream"),       # 810 / 1044 / 802 / 1274 / 883
     ("gemm_epilogue", 1536, 4096, 4096, "nk", "pair"),               # 1185 / 927 / 838 / 1049
     ("gemm_epilogue", 2048, 4096, 4096, "nk", "pair"),               # 1564 / 1218 / 862 / 1395
     ("gemm_epilogue", 256, 8192, 8192, "kn", "pair_splitk"),         # 486 / 620 / 925 / 738 / 1077
-    ("gemm_epilogue", 512, 8192, 8192, "kn", "pair_1stream"),        # 958 / 1220 / 1050 / 1411 / 1157
+    ("gemm_epilogue", 512, 8192, 8192, "kn", "pair_1stream"),        # 951 / 1205 / 1048 / 1456 / 1179
     ("gemm_epilogue", 768, 8192, 8192, "kn", "pair"),                # 1240 / 1014 / 1095 / 1179
     ("gemm_epilogue", 1536, 8192, 8192, "kn", "pair_1stream"),       # 1283 / 1360 / 1185 / 1587
     ("gemm_epilogue", 384, 14336, 4096, "nk", "pair"),               # 1021 / 737 / 708 / 931 / 594

@@ -189,6 +189,17 @@ def test_cta_pair_kernel_one_stream_224_wide_tiles(cuda_lib, layout, M, N, K):
                   expect_path="pair_1stream", force_path="pair_1stream")
 
 
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,N,K", [(512, 512, 64), (600, 1000, 72), (1024, 2048, 136),
+                                   (777, 4096, 1000)])
+def test_cta_pair_one_stream_two_k_streams(cuda_lib, layout, M, N, K):
+    # one tile per pair: two MMA streams over the alternate K blocks of the
+    # tile (one block: the second stream idle; an odd count: 2 + 1), the two
+    # accumulators added in the ending
+    run_and_check(cuda_lib, M, N, K, layout, "relu", 0.5, -0.75, seed=M + 17 * N + K,
+                  expect_path="pair_1stream", force_path="pair_1stream")
+
+
 @pytest.mark.parametrize("M,N,K", [(512, 4096, 256), (768, 2048, 192), (1024, 8192, 128),
                                    (3000, 1024, 64)])
 def test_automatic_kernel_choice(cuda_lib, M, N, K):
