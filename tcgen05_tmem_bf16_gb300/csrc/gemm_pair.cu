@@ -34,6 +34,18 @@
 // the accumulators in tile order (stream 0's, then stream 1's), each taking
 // half of the tile's columns, with the C / residual rows of a tile pulled
 // into L2 before its accumulator is ready.
+//
+// Forms for shapes with few tiles (template flags, chosen by the planner):
+//   * one stream (STREAMS = 1): units of one 256-row M-tile, the single MMA
+//     stream alternating between the two accumulators so that a tile's
+//     ending overlaps the next tile's main loop;
+//   * two K streams (KPAR, one stream per unit and one unit per pair): both
+//     issuers on the one tile, the even and the odd K blocks into the two
+//     accumulators, which the ending adds;
+//   * split K (SPLIT): clusters of four CTAs, two pairs per tile, pair kp
+//     over the K half kp; each CTA then finishes half of its rows' columns
+//     after pushing the other half of its partial to the CTA with the same
+//     rows in the other pair.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
