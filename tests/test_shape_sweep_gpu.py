@@ -1,0 +1,55 @@
+"""Seeded random shapes through every dense kernel form, against the fp64 oracle.
+
+Each case draws M, N, K (N and K multiples of 8, as the boundary requires),
+the weight layout, the activation, alpha / beta and which of C, bias and
+residual are present from its own seed, and runs the product twice: with the
+planner's choice, and with one of the forms the tuning hook can force (the
+one-SM kernel and its split-K form, the CTA-pair kernel with two M-tile
+streams, one stream, or split K over two pairs).  The parametrised tests of
+the other files pin chosen edge shapes; this file covers combinations of
+ragged M, N and K tails, odd K-block counts and operand sets that nobody
+picked by hand."""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import assert_parity, down, poison_bf16, up
+from test_gemm_gpu import case
+
+pytestmark = pytest.mark.gpu
+
+FORMS = ["persistent", "persistent_splitk", "pair", "pair_1stream", "pair_splitk"]
+ACTS = ["identity", "relu", "silu", "gelu_tanh"]
+
+
+def draw(seed):
+    rng = np.random.Generator(np.random.PCG64(9000 + seed))
+    M = int(rng.integers(129, 900))           # above the swapped kernel's range
+    N = 8 * int(rng.integers(1, 160))         # 8 .. 1272
+    K = 8 * int(rng.integers(1, 100))         # 8 .. 792 (1 .. 13 K blocks)
+    layout = ["kn", "nk"][int(rng.integers(0, 2))]
+    act = ACTS[int(rng.integers(0, 4))]
+    alpha = float(rng.choice([0.5, 1.0, 1.25]))
+    beta = float(rng.choice([-0.5, 0.0, 0.75]))
+    c, bias, res = (bool(x) for x in rng.integers(0, 2, size=3))
+    form = FORMS[seed % len(FORMS)]
+    return M, N, K, layout, act, alpha, beta, c, bias, res, form
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_random_shape_every_form(cuda_lib, seed):
+    M, N, K, layout, act, alpha, beta, c, bias, res, form = draw(seed)
+    A, B, C, bi, r = case(M, N, K, layout, 500 + seed, c, bias, res)
+    ref = oracle.gemm_epilogue(A, B, layout, C, bi, r, M=M, N=N, K=K, alpha=alpha, beta=beta,
+                               act=act)
+    for forced in (None, form):
+        assert cuda_lib.gbf_debug_force_path(forced) == 0
+        try:
+            path = cuda_lib.gbf_kernel_path("gemm_epilogue", M, N, K, layout)[0]
+            out = poison_bf16(M, N)
+            cuda_lib.gemm_epilogue(up(A), up(B), layout, up(C), up(bi), up(r), out, M, N, K,
+                                   alpha, beta, act)
+        finally:
+            cuda_lib.gbf_debug_force_path(None)
+        assert cuda_lib.gbf_check_device_error() == 0
+        assert_parity(down(out), ref, f"seed {seed}: {M}x{N}x{K} {layout} {act} via {path}")
