@@ -8,13 +8,15 @@ one-SM kernel and its split-K form, the CTA-pair kernel with two M-tile
 streams, one stream, or split K over two pairs).  The parametrised tests of
 the other files pin chosen edge shapes; this file covers combinations of
 ragged M, N and K tails, odd K-block counts and operand sets that nobody
-picked by hand."""
+picked by hand.  The weight-only kernel gets the same treatment in all three
+weight formats."""
 import numpy as np
 import pytest
 
 import oracle
+import workloads
 from gpu_util import assert_parity, down, poison_bf16, up
-from test_gemm_gpu import case
+from test_gemm_gpu import case, rand_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -53,3 +55,54 @@ def test_random_shape_every_form(cuda_lib, seed):
             cuda_lib.gbf_debug_force_path(None)
         assert cuda_lib.gbf_check_device_error() == 0
         assert_parity(down(out), ref, f"seed {seed}: {M}x{N}x{K} {layout} {act} via {path}")
+
+
+def draw_wq(seed):
+    rng = np.random.Generator(np.random.PCG64(9500 + seed))
+    fmt = ["int4", "fp8", "nvfp4"][seed % 3]
+    M = int(rng.integers(1, 70))
+    N = 32 * int(rng.integers(1, 70))        # 32 .. 2208
+    if fmt == "nvfp4":
+        G = 16
+        K = 16 * int(rng.integers(1, 80))    # 16 .. 1264
+    else:
+        G = int(rng.choice([64, 128, 256]))
+        K = G * int(rng.integers(1, 10))
+    act = ACTS[int(rng.integers(0, 4))]
+    alpha = float(rng.choice([0.5, 1.0, 1.25]))
+    beta = float(rng.choice([-0.5, 0.0, 0.75]))
+    c, bias, res = (bool(x) for x in rng.integers(0, 2, size=3))
+    return fmt, M, N, K, G, act, alpha, beta, c, bias, res, rng
+
+
+@pytest.mark.parametrize("seed", range(15))
+def test_random_shape_weight_only(cuda_lib, seed):
+    # the weight-only kernel at random M (one or more 16 / 32-row M-tiles),
+    # N and K, random scales and operand sets, in all three weight formats
+    fmt, M, N, K, G, act, alpha, beta, c, bias, res, rng = draw_wq(seed)
+    A = rand_bf16(700 + seed, (M, K))
+    C = rand_bf16(720 + seed, (M, N)) if c else None
+    bi = rand_bf16(740 + seed, (N,), std=0.3) if bias else None
+    r = rand_bf16(760 + seed, (M, N)) if res else None
+    if fmt == "fp8":
+        Wq = rng.integers(0, 256, size=(K, N), dtype=np.uint8)
+        Wq[(Wq & 0x7F) == 0x7F] = 0x38  # no NaN codes (not valid weights)
+        s = workloads.to_bf16_bits(rng.uniform(0.25, 2.0, (K // G, N)).astype(np.float32))
+    elif fmt == "int4":
+        Wq = rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+        s = workloads.to_bf16_bits(rng.uniform(0.005, 0.02, (K // G, N)).astype(np.float32))
+    else:
+        Wq = rng.integers(0, 256, size=(K, N // 2), dtype=np.uint8)
+        s = rng.integers(0x28, 0x40, size=(K // 16, N), dtype=np.uint8)  # E4M3 0.25 .. 1.875
+    ref = oracle.wq_gemm(fmt, A, Wq, s, G, C, bi, r, M=M, N=N, K=K, alpha=alpha, beta=beta,
+                         act=act)
+    out = poison_bf16(M, N)
+    args = (up(C), up(bi), up(r), out, M, N, K, alpha, beta, act)
+    if fmt == "int4":
+        cuda_lib.w4a16_gemm(up(A), up(Wq), up(s), G, *args)
+    elif fmt == "fp8":
+        cuda_lib.w8a16_fp8_gemm(up(A), up(Wq), up(s), G, *args)
+    else:
+        cuda_lib.w4a16_nvfp4_gemm(up(A), up(Wq), up(s), *args)
+    assert cuda_lib.gbf_check_device_error() == 0
+    assert_parity(down(out), ref, f"seed {seed}: {fmt} {M}x{N}x{K} G={G} {act}")
