@@ -8,8 +8,9 @@ one-SM kernel and its split-K form, the CTA-pair kernel with two M-tile
 streams, one stream, or split K over two pairs).  The parametrised tests of
 the other files pin chosen edge shapes; this file covers combinations of
 ragged M, N and K tails, odd K-block counts and operand sets that nobody
-picked by hand.  The weight-only kernel gets the same treatment in all three
-weight formats."""
+picked by hand.  The weight-only kernel (all three weight formats), the
+swapped small-M kernel (every split-K cluster size) and the gate/up dual
+GEMM get the same treatment."""
 import numpy as np
 import pytest
 
@@ -106,3 +107,56 @@ def test_random_shape_weight_only(cuda_lib, seed):
         cuda_lib.w4a16_nvfp4_gemm(up(A), up(Wq), up(s), *args)
     assert cuda_lib.gbf_check_device_error() == 0
     assert_parity(down(out), ref, f"seed {seed}: {fmt} {M}x{N}x{K} G={G} {act}")
+
+
+@pytest.mark.parametrize("seed", range(15))
+def test_random_shape_small_m_every_split_count(cuda_lib, seed):
+    # the swapped kernel (M <= 128) at random shapes with the split-K
+    # cluster size forced to a random 1..8 (0: the automatic choice)
+    rng = np.random.Generator(np.random.PCG64(9800 + seed))
+    M = int(rng.integers(1, 129))
+    N = 8 * int(rng.integers(1, 140))
+    K = 8 * int(rng.integers(1, 250))
+    layout = ["kn", "nk"][int(rng.integers(0, 2))]
+    act = ACTS[int(rng.integers(0, 4))]
+    alpha, beta = float(rng.choice([0.5, 1.0])), float(rng.choice([0.0, 0.5]))
+    c, bias, res = (bool(x) for x in rng.integers(0, 2, size=3))
+    splits = int(rng.integers(0, 9))
+    A, B, C, bi, r = case(M, N, K, layout, 800 + seed, c, bias, res)
+    assert cuda_lib.gbf_debug_force_splits(splits) == 0
+    try:
+        path, S = cuda_lib.gbf_kernel_path("gemm_epilogue", M, N, K, layout)
+        assert path == "swap_splitk"
+        out = poison_bf16(M, N)
+        cuda_lib.gemm_epilogue(up(A), up(B), layout, up(C), up(bi), up(r), out, M, N, K, alpha,
+                               beta, act)
+    finally:
+        cuda_lib.gbf_debug_force_splits(0)
+    assert cuda_lib.gbf_check_device_error() == 0
+    ref = oracle.gemm_epilogue(A, B, layout, C, bi, r, M=M, N=N, K=K, alpha=alpha, beta=beta,
+                               act=act)
+    assert_parity(down(out), ref, f"seed {seed}: {M}x{N}x{K} {layout} {act} S={S}")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shape_gate_up(cuda_lib, seed):
+    # the gate/up dual GEMM at random shapes on whichever kernel the planner
+    # picks (swapped for M <= 32, else the persistent or CTA-pair kernel)
+    rng = np.random.Generator(np.random.PCG64(9900 + seed))
+    M = int(rng.integers(1, 600))
+    N = 8 * int(rng.integers(1, 120))
+    K = 8 * int(rng.integers(1, 120))
+    layout = ["kn", "nk"][int(rng.integers(0, 2))]
+    act = ["silu", "gelu_tanh", "relu"][int(rng.integers(0, 3))]
+    alpha, beta = float(rng.choice([0.75, 1.0])), float(rng.choice([0.0, -0.5]))
+    x = rand_bf16(900 + seed, (M, K))
+    shp = (N, K) if layout == "nk" else (K, N)
+    wg = rand_bf16(920 + seed, shp, std=K ** -0.5)
+    wu = rand_bf16(940 + seed, shp, std=K ** -0.5)
+    C = rand_bf16(960 + seed, (M, N)) if beta != 0.0 else None
+    h = poison_bf16(M, N)
+    path = cuda_lib.gbf_kernel_path("swiglu", M, N, K, layout)[0]
+    cuda_lib.swiglu_dual_gemm(up(x), up(wg), up(wu), layout, h, M, N, K, alpha, beta, up(C), act)
+    assert cuda_lib.gbf_check_device_error() == 0
+    ref = oracle.swiglu(x, wg, wu, layout, C, M=M, N=N, K=K, alpha=alpha, beta=beta, act=act)
+    assert_parity(down(h), ref, f"seed {seed}: swiglu {M}x{N}x{K} {layout} {act} via {path}")
