@@ -9,9 +9,12 @@
 //
 // HBM-bound.  One CTA of 256 threads per row (grid-stride over rows); each
 // thread holds R 16-byte vectors of the row in registers between the sum of
-// squares and the scaling, so the row is read from HBM once.
+// squares and the scaling, so the row is read from HBM once, and loads its
+// vectors of the CTA's next row before reducing the current one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -31,8 +34,30 @@ __global__ void __launch_bounds__(kRmsThreads)
   const uint64_t pol = l2_evict_first_policy();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The loads of a CTA's next row are issued before the current row's
+  // reduction, so each CTA keeps two rows of a and x in flight (R <= 4; wider
+  // rows keep one, for registers).
+  constexpr bool kAhead = R <= 4;
+  uint4 ca[R], cx[R];  // this thread's vectors of the current row of a and x
+  auto load_row = [&](int64_t row, uint4 (&ra)[R], uint4 (&rx)[R]) {
+#pragma unroll
+    for (int v = 0; v < R; ++v) {
+      const int col = (threadIdx.x + v * kRmsThreads) * 8;
+      if (col < N) {
+        ra[v] = ld_stream_u4(a + row * N + col, pol);
+        rx[v] = x ? ld_stream_u4(x + row * N + col, pol) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  };
+  if (kAhead && static_cast<int64_t>(blockIdx.x) < M) load_row(blockIdx.x, ca, cx);
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     const int64_t base = row * N;
+    uint4 na[R], nx[R];
+    if (kAhead) {
+      if (row + gridDim.x < M) load_row(row + gridDim.x, na, nx);
+    } else {
+      load_row(row, ca, cx);
+    }
     float r[R][8];
     float ss = 0.0f;
 #pragma unroll
@@ -40,13 +65,8 @@ __global__ void __launch_bounds__(kRmsThreads)
       const int col = (threadIdx.x + v * kRmsThreads) * 8;
       if (col < N) {
         float av[8], xv[8];
-        unpack8(ld_stream_u4(a + base + col, pol), av);
-        if (x) {
-          unpack8(ld_stream_u4(x + base + col, pol), xv);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) xv[i] = 0.0f;
-        }
+        unpack8(ca[v], av);
+        unpack8(cx[v], xv);  // zeros without x: bf16 0x0000 is +0
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           r[v][i] = av[i] + xv[i];
@@ -79,14 +99,36 @@ __global__ void __launch_bounds__(kRmsThreads)
         st_stream_u4(out_norm + base + col, pack8(n), pol);
       }
     }
+    if (kAhead) {
+#pragma unroll
+      for (int v = 0; v < R; ++v) {
+        ca[v] = na[v];
+        cx[v] = nx[v];
+      }
+    }
   }
 }
 
+// One wave of CTAs: as many per SM as fit (from the kernel's registers), so
+// that every CTA's next row is in flight while it reduces the current one
+// (4096 x 4096: 8 per SM 23.9 us, the 4 that fit 23.3 us, 3 or 6 24.6 us).
 template <int R>
 cudaError_t run_rms(const __nv_bfloat16* a, const __nv_bfloat16* x, const __nv_bfloat16* w,
                     __nv_bfloat16* norm, __nv_bfloat16* resid, int64_t M, int N, float eps,
                     int sms, cudaStream_t stream) {
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  static std::atomic<int> per_sm{0};
+  int fit = per_sm.load(std::memory_order_relaxed);
+  if (fit <= 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, add_rmsnorm_kernel<R>, kRmsThreads,
+                                                      0) != cudaSuccess ||
+        fit <= 0) {
+      (void)cudaGetLastError();
+      fit = 4;
+    } else {
+      per_sm.store(fit, std::memory_order_relaxed);
+    }
+  }
+  const int64_t cap = static_cast<int64_t>(sms) * fit;
   const int grid = static_cast<int>(M < cap ? M : cap);
   add_rmsnorm_kernel<R><<<grid, kRmsThreads, 0, stream>>>(a, x, w, norm, resid, M, N, eps);
   return cudaGetLastError();
